@@ -1,0 +1,346 @@
+#!/usr/bin/env python3
+"""Benchmark of the VLA forward scan on GB300.
+
+One "step" is one pass of the whole scan (every row of the hot path: the
+Sherman-Morrison tracking of A, alpha, the state update, renormalisation and
+the readout) over one batch of the workload below.  The headline workload is
+d = d_v = 64, T = 16384 with B = 8, H = 16 (bfloat16 q/k/v/u/o, float32 state,
+associative-recall-shaped keys); its inputs (1.07 GB) exceed the 129 MB L2, so
+no flush is needed between steps.  Successive steps continue the same streams
+(t0 advances by T), so every step does identical work on resident inputs.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the float64 CPU
+oracle instead (the only reference this method has), on a bounded sample.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "VLA scan tokens*heads/s (d=64, T=16384)"
+UNIT = "tokens*heads/s"
+SM_COUNT_NOMINAL = 152
+FP32_LANES_PER_SM = 128
+SM_MAX_MHZ_NOMINAL = 2070.0
+
+
+def flops_per_token_head(d: int, dv: int, r: int) -> int:
+    """Algorithmic flops of one step of one pair (FMA = 2): r (A u: 2d^2, u.z: 2d,
+    rank-1 update: 2d^2) + alpha = A s (2d^2) + S += v alpha^T (2 d dv) + S phi(q) (2 d dv)."""
+    return r * (4 * d * d + 2 * d) + 2 * d * d + 4 * d * dv
+
+
+def flops_per_token_head_short(d: int, dv: int, r: int) -> int:
+    """The shorter count 4 r d^2 + 2 d d_v (omits alpha = A s and the readout)."""
+    return 4 * r * d * d + 2 * d * dv
+
+
+def streamed_bytes_per_token_head(w) -> int:
+    es = 4 if w.io == "f32" else 2
+    return (2 * w.d + w.r * w.d + 2 * w.dv) * es
+
+
+def fp32_peak_tflops(peaks: dict) -> tuple[float, str]:
+    """FP32 CUDA-core peak: SMs x 128 FMA lanes x 2 flops x max SM clock."""
+    mhz = float(peaks.get("sm_max_mhz", SM_MAX_MHZ_NOMINAL))
+    return SM_COUNT_NOMINAL * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12, (
+        f"{SM_COUNT_NOMINAL} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 flop x {mhz:.0f} MHz")
+
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        d["_source"] = "measured"
+        return d
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "sm_max_mhz": SM_MAX_MHZ_NOMINAL, "_source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi sampled during the timed region (clocks and throttle reasons)."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int, period_ms: int = 100):
+        self.proc = None
+        self.lines: list[str] = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(device_index), "-lms", str(period_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0])); smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        return rank, local, world, dist
+    return 0, 0, 1, None
+
+
+def max_over_ranks(x: float, dist, dev) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+class OracleLeg:
+    """The float64 oracle, as it stands, timed on the host cores on a bounded
+    sample of the workload: every pair, the first `steps` steps."""
+
+    def __init__(self, w, T_max: int = 8192):
+        import oracle
+        self.oracle = oracle
+        self.w = w
+        self.T_max = min(w.T, T_max)
+        self.x = workloads.make_inputs(w, T=self.T_max)
+
+    def run(self, steps: int):
+        x, w = self.x, self.w
+        c0, t0 = time.process_time(), time.perf_counter()
+        self.oracle.scan(x["q"][:, :steps], x["k"][:, :steps], x["v"][:, :steps], x["u"][:, :steps],
+                         x["A0"], x["S0"], x["n0"], P=w.P, eps_n=w.eps_n, tau=w.tau)
+        wall = time.perf_counter() - t0
+        cpu = time.process_time() - c0
+        return self.w.pairs * steps / wall, wall, max(1, round(cpu / wall))
+
+    def calibrate(self, budget_s: float) -> int:
+        steps = 16
+        while True:
+            _, wall, _ = self.run(steps)
+            if wall * 2 >= budget_s or steps >= self.T_max:
+                return min(self.T_max, max(1, int(steps * budget_s / max(wall, 1e-6))))
+            steps = min(self.T_max, steps * 4)
+
+    def sample_text(self, steps: int, wall: float) -> str:
+        return f"all {self.w.pairs} pairs x first {steps} of {self.w.T} steps of {self.w.name} ({wall:.1f} s wall)"
+
+
+def oracle_leg(w, budget_s: float = 15.0):
+    leg = OracleLeg(w)
+    steps = leg.calibrate(budget_s)
+    value, wall, cores = leg.run(steps)
+    return value, cores, leg.sample_text(steps, wall)
+
+
+def run_reference(args, w):
+    if int(os.environ.get("RANK", "0")) != 0:      # torchrun: rank 0 alone times the oracle
+        return
+    leg = OracleLeg(w)
+    per_step = max(1.0, 150.0 / (args.warmup + args.steps))
+    steps = leg.calibrate(per_step)
+    for _ in range(args.warmup):
+        leg.run(steps)
+    vals, walls, cores = [], [], 1
+    for _ in range(args.steps):
+        v, wall, cores = leg.run(steps)
+        vals.append(v)
+        walls.append(wall)
+    value = len(vals) * w.pairs * steps / sum(walls)
+    sample = leg.sample_text(steps, statistics.median(walls)) + " per step"
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(walls), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d": w.d, "dv": w.dv, "r": w.r,
+                       "io": w.io},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=40)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="2", help="index or name of the workload")
+    ap.add_argument("--mode", choices=["sequential", "chunked"], default="sequential")
+    ap.add_argument("--chunk", type=int, default=16)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=None)
+    args = ap.parse_args()
+    w = workloads.get(int(args.workload) if args.workload.isdigit() else args.workload)
+
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    import sherman_morrison_inverse_gb300 as vla
+
+    rank, local, world, dist = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    h = vla.Handle(local)
+
+    x = workloads.make_inputs(w)
+    B, H, T = w.B, w.H, w.T
+    g = {k: x[k].reshape(B, H, *x[k].shape[1:]).to(dev).contiguous() for k in ("q", "k", "v", "u")}
+    A = x["A0"].reshape(B, H, w.d, w.d).to(dev).contiguous()
+    S = x["S0"].reshape(B, H, w.dv, w.d).to(dev).contiguous()
+    n = x["n0"].reshape(B, H, w.d).to(dev).contiguous()
+    o = torch.empty((B, H, T, w.dv), dtype=g["q"].dtype, device=dev)
+    kw = dict(P=w.P, eps_n=w.eps_n, tau=w.tau, mode=args.mode, chunk=args.chunk)
+
+    t0 = 0
+    for _ in range(args.warmup):
+        h.scan_fwd(g["q"], g["k"], g["v"], g["u"], A, S, n, o, t0=t0, **kw)
+        t0 += T
+    torch.cuda.synchronize(dev)
+    st_warm = h.status()
+
+    # ---- device-resident timing (inputs already in HBM)
+    barrier(dist)
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        h.scan_fwd(g["q"], g["k"], g["v"], g["u"], A, S, n, o, t0=t0, **kw)
+        t0 += T
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    barrier(dist)
+    ms = ev0.elapsed_time(ev1)
+    ms_max = max_over_ranks(ms, dist, dev)
+    st = h.status()
+    units = B * H * T * args.steps * world
+    value = units / (ms_max / 1e3)
+    ms_per_step = ms_max / args.steps
+
+    # ---- end to end: pinned host buffers -> device, scan, result back, every step
+    e2e_steps = args.e2e_steps or max(3, args.steps // 4)
+    host = {k: x[k].reshape(B, H, *x[k].shape[1:]).contiguous().pin_memory() for k in ("q", "k", "v", "u")}
+    host_state = {"A": x["A0"].reshape(B, H, w.d, w.d).contiguous().pin_memory(),
+                  "S": x["S0"].reshape(B, H, w.dv, w.d).contiguous().pin_memory(),
+                  "n": x["n0"].reshape(B, H, w.d).contiguous().pin_memory()}
+    host_o = torch.empty_like(o, device="cpu").pin_memory()
+    host_out_state = {k: torch.empty_like(v).pin_memory() for k, v in host_state.items()}
+    h2d = sum(t.numel() * t.element_size() for t in list(host.values()) + list(host_state.values()))
+    d2h = host_o.numel() * host_o.element_size() + sum(t.numel() * t.element_size()
+                                                       for t in host_out_state.values())
+    dev_state = {"A": A, "S": S, "n": n}
+    barrier(dist)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for k2 in g:
+            g[k2].copy_(host[k2], non_blocking=True)
+        for k2 in dev_state:
+            dev_state[k2].copy_(host_state[k2], non_blocking=True)
+        h.scan_fwd(g["q"], g["k"], g["v"], g["u"], A, S, n, o, t0=0, **kw)
+        host_o.copy_(o, non_blocking=True)
+        for k2 in dev_state:
+            host_out_state[k2].copy_(dev_state[k2], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(dist)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
+    e2e_value = B * H * T * e2e_steps * world / (e2e_ms / 1e3)
+    st_e2e = h.status()
+
+    # ---- roofline of the (only) kernel: FP32 CUDA-core arithmetic binds
+    peaks = load_peaks()
+    peak_tf, peak_how = fp32_peak_tflops(peaks)
+    F = flops_per_token_head(w.d, w.dv, w.r)
+    achieved_tf = B * H * T * F / (ms_per_step / 1e3) / 1e12
+    bytes_step = B * H * T * streamed_bytes_per_token_head(w)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "B": B, "H": H, "T": T, "d": w.d, "dv": w.dv, "r": w.r,
+                   "io": w.io, "state": "f32", "mode": args.mode,
+                   "l2": f"inputs {bytes_step / 1e9:.2f} GB per step > 129 MB L2 (no flush)",
+                   "parallelism": f"replicas x{world}, one CTA per (b,h) pair"},
+        "roofline": {"bound": "alu", "achieved": achieved_tf, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": achieved_tf / peak_tf, "traffic": None,
+                     "peak_how": peak_how + " (derived; FP32 is not in the measured-peaks file)",
+                     "flops_per_token_head": F,
+                     "frac_short_count": (B * H * T * flops_per_token_head_short(w.d, w.dv, w.r)
+                                          / (ms_per_step / 1e3) / 1e12) / peak_tf,
+                     "hbm_gbs": bytes_step / (ms_per_step / 1e3) / 1e9,
+                     "hbm_frac": bytes_step / (ms_per_step / 1e3) / 1e9 / float(peaks["hbm_gbs"]),
+                     "sm_ceiling": min(1.0, B * H / SM_COUNT_NOMINAL)},
+        "clocks": clk,
+        "gpu_launches": args.steps,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps},
+        "status": {"warmup": st_warm, "timed": st, "e2e": st_e2e},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, cores, sample = oracle_leg(w)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    h.close()
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

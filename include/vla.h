@@ -1,0 +1,134 @@
+/*
+ * vla.h - C ABI of the GB300 (sm_103a) Variational Linear Attention forward scan.
+ *
+ * What the scan computes, for every (batch b, head h) pair independently and
+ * for t = 1..T in order (global step g = t0 + t):
+ *
+ *   for i = 1..r:                                   "Mathematical Primitives" §3
+ *     z = A u_{t,i};  delta = 1 + u_{t,i} . z       §2, execution pipeline
+ *     if |delta| < 1e-6:  A += 1e-6 I               §2, singularity guard
+ *     else:               A -= z z^T / delta        §2, exact inverse update
+ *   if P > 0 and g % P == 0:  A += eps_n I          §2, periodic spectrum stabilisation
+ *   s = phi(k_t) / sqrt(d);  alpha = A s            §1 (s read as a vector), §4
+ *   S += v_t alpha^T;  n += phi(k_t)                §5 (S is d_v x d); README "VLA v3" item 5
+ *   if ||S||_F > tau:  S *= tau / ||S||_F           §5, dynamic renormalisation
+ *   o_t = S phi(q_t) / (n . phi(q_t) + 1e-6)        README "VLA v3" item 5 (calibrated readout)
+ *
+ * with phi(x) = ELU(x) + 1 (README "VLA v3" item 1): x + 1 for x > 0, exp(x)
+ * otherwise.  A tracks M_t^{-1} for M_t = M_{t-1} + u u^T (§2, "Theoretical
+ * Derivation").  q, k are the raw projections; phi is applied inside the scan.
+ * u is taken as given (the pages form it as normalize(W_u k_raw), README item 2);
+ * the scan does not renormalise it.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Device pointers are CUDA device (or managed) memory on the handle's device;
+ *   the caller allocates and owns them.  The library owns only the handle and
+ *   its small device status block.
+ * - Layouts are dense row-major with the pair index p = b * H + h outermost:
+ *     q, k : [B, H, T, d]          io dtype
+ *     v    : [B, H, T, d_v]        io dtype
+ *     u    : [B, H, T, r, d]       io dtype (the r directions of a step are contiguous)
+ *     o    : [B, H, T, d_v]        io dtype, written
+ *     A    : [B, H, d, d]          float32, read and written in place
+ *     S    : [B, H, d_v, d]        float32, read and written in place
+ *     n    : [B, H, d]             float32, read and written in place
+ *   q, k, v and u must start on a 16-byte boundary (they are streamed with bulk
+ *   asynchronous copies).  o must not overlap any input.
+ * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *   stream).  Every call that launches work is asynchronous on that stream; it
+ *   returns after the launch.  Errors of the kernel itself are reported through
+ *   vla_status(), never by trapping.
+ * - A handle is not thread-safe: one host thread uses it at a time.
+ */
+#ifndef VLA_H
+#define VLA_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct vla_handle_s* vla_handle_t;
+
+typedef enum {
+  VLA_OK = 0,
+  VLA_ERR_INVALID_ARG = 1,   /* null pointer, negative size, misaligned pointer, bad parameter */
+  VLA_ERR_UNSUPPORTED = 2,   /* valid but not built: (d, d_v, r, dtype, mode) outside the list below */
+  VLA_ERR_CUDA = 3,          /* a CUDA runtime call failed; see vla_last_error() */
+  VLA_ERR_NOMEM = 4          /* host or device allocation failed */
+} vla_err_t;
+
+typedef enum { VLA_F32 = 0, VLA_BF16 = 1 } vla_dtype_t;        /* dtype of q, k, v, u, o */
+
+typedef enum {
+  VLA_SEQUENTIAL = 0,   /* one step after another (the pages' recurrence) */
+  VLA_CHUNKED = 1       /* `chunk` steps at a time in exact Woodbury / LDL^T form */
+} vla_mode_t;
+
+/* Status flags, ORed over all pairs since the last vla_status() call. */
+#define VLA_STATUS_NONFINITE 1u  /* a NaN/Inf reached delta, the readout or ||S|| ("Mathematical Primitives" §1, finite state enforcement) */
+#define VLA_STATUS_TIMEOUT   2u  /* a bounded wait on an input copy expired; that pair stopped early */
+
+typedef struct {
+  unsigned int flags;                 /* VLA_STATUS_* */
+  unsigned int reserved;
+  unsigned long long guard_count;     /* directions where the singularity guard replaced the update */
+  unsigned long long renorm_count;    /* steps where S was renormalised */
+  unsigned long long chunk_fallbacks; /* VLA_CHUNKED: chunks that were taken step by step */
+} vla_status_t;
+
+/* Create a handle bound to CUDA device `device`.  Allocates the handle and a
+ * small device status block; does not change the caller's current device.
+ * Errors: INVALID_ARG (h == NULL or no such device), CUDA, NOMEM. */
+vla_err_t vla_create(vla_handle_t* h, int device);
+
+/* Run the scan above over T steps for B * H pairs, continuing from the state in
+ * A, S, n (updated in place) and writing o.
+ *
+ *   B, H      >= 0; B * H == 0 is a no-op (pointers may then be NULL).
+ *   T         >= 0; T == 0 leaves the state untouched (q, k, v, u, o may be NULL).
+ *   d, dv     head and value width.  Built: d == dv in {16, 64, 128}.
+ *   r         directions per step.  Built: 1 and 4.
+ *   P         nudge period (>= 0; 0 disables the nudge).
+ *   eps_n     nudge size (finite).
+ *   tau       renormalisation threshold on ||S||_F (> 0; +inf disables it).
+ *   t0        steps already taken by earlier calls on this state (>= 0): the
+ *             nudge fires at global steps t0 + t that are multiples of P, so
+ *             splitting a sequence into several calls gives the same result.
+ *   io_dtype  VLA_F32 or VLA_BF16 for q, k, v, u and o; state is always float32.
+ *   mode      VLA_SEQUENTIAL (every built shape) or VLA_CHUNKED (d == 64 only;
+ *             `chunk` = steps per chunk, see the built list in the library's
+ *             error message).  Both compute the same recurrence; they differ in
+ *             rounding only.
+ *   stream    cudaStream_t as void*.
+ *
+ * Errors (returned before any launch, nothing is written): INVALID_ARG for a
+ * NULL handle or pointer, negative size, misaligned q/k/v/u, P < 0, t0 < 0,
+ * tau <= 0 or NaN, non-finite eps_n; UNSUPPORTED for shapes that are not built;
+ * CUDA if the launch fails.  There is no CPU fallback. */
+vla_err_t vla_scan_fwd(vla_handle_t h,
+                       const void* q, const void* k, const void* v, const void* u,
+                       float* A, float* S, float* n, void* o,
+                       int B, int H, long long T, int d, int dv, int r,
+                       int P, float eps_n, float tau, long long t0,
+                       vla_dtype_t io_dtype, vla_mode_t mode, int chunk,
+                       void* stream);
+
+/* Synchronise `stream`, copy the accumulated status into *out and reset it.
+ * Errors: INVALID_ARG (NULL argument), CUDA. */
+vla_err_t vla_status(vla_handle_t h, void* stream, vla_status_t* out);
+
+/* Message of the last failed call on this handle ("" if none).  The string is
+ * owned by the handle and stays valid until the next call on it.  With h ==
+ * NULL it returns the message of the last failed vla_create on this thread. */
+const char* vla_last_error(vla_handle_t h);
+
+/* Free the handle and its status block (synchronises its device first).
+ * h == NULL is a no-op that returns VLA_OK. */
+vla_err_t vla_destroy(vla_handle_t h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VLA_H */

@@ -1,0 +1,135 @@
+// Internal declarations shared by the scan kernels and the C ABI layer.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace vla {
+
+// Device-side status block, accumulated with atomics by every CTA at its end.
+struct DevStatus {
+  unsigned int flags;
+  unsigned int reserved;
+  unsigned long long guard_count;
+  unsigned long long renorm_count;
+  unsigned long long chunk_fallbacks;
+};
+
+constexpr unsigned int kStatusNonfinite = 1u;
+constexpr unsigned int kStatusTimeout = 2u;
+
+// Arguments of one scan launch (plain pointers; the pair index p = b*H + h is
+// blockIdx.x).
+struct ScanArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* u;
+  float* A;
+  float* S;
+  float* n;
+  void* o;
+  long long T;
+  long long t0;
+  int P;
+  float eps_n;
+  float tau;
+  int pairs;
+  DevStatus* status;
+};
+
+// Host-side launchers, one per built (d, r, dtype); defined in vla_seq_d*.cu.
+// Each returns cudaSuccess or the launch error.
+cudaError_t launch_seq(int d, int r, bool bf16, const ScanArgs& a, cudaStream_t s, bool* built);
+cudaError_t launch_chunked(int d, int r, bool bf16, int chunk, const ScanArgs& a, cudaStream_t s,
+                           bool* built);
+
+// --------------------------------------------------------------------------
+// device helpers (inline PTX: mbarrier, bulk asynchronous copies, timers)
+// --------------------------------------------------------------------------
+
+// Upper bound on any wait for an input copy.  A copy of a few tens of KB lands
+// in microseconds; after this long the CTA gives up and reports a timeout.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: true when the phase completed, false after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t_start = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t_start > kWaitLimitNs) return false;
+  }
+}
+
+// Global -> shared bulk copy completing on an mbarrier (16-byte aligned
+// addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst_smem)),
+      "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ float phi_elu1(float x) {
+  // ELU(x) + 1 with alpha = 1: x + 1 for x > 0, exp(x) otherwise.
+  return x > 0.f ? x + 1.f : expf(x);
+}
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T x);
+template <>
+__device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float x);
+template <>
+__device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+}  // namespace vla

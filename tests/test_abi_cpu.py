@@ -1,0 +1,58 @@
+"""C ABI checks that need no GPU: the library builds, loads and exports every
+function include/vla.h declares, and argument errors come back as codes."""
+import ctypes
+
+import pytest
+import torch
+
+from _util import ensure_built, header_functions
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ensure_built()
+    import sherman_morrison_inverse_gb300 as vla
+    return vla.load_library()
+
+
+def test_header_declares_the_boundary():
+    names = header_functions()
+    for fn in ("vla_create", "vla_scan_fwd", "vla_status", "vla_last_error", "vla_destroy"):
+        assert fn in names, names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+
+
+def test_null_handle_is_rejected_before_any_cuda_call(lib):
+    code = lib.vla_scan_fwd(None, None, None, None, None, None, None, None, None,
+                            1, 1, 4, 64, 64, 1, 0, 0.0, 1.0, 0, 0, 0, 16, None)
+    assert code == 1  # VLA_ERR_INVALID_ARG
+    assert b"handle" in lib.vla_last_error(None)
+
+
+def test_status_and_destroy_with_null(lib):
+    assert lib.vla_status(None, None, None) == 1
+    assert lib.vla_destroy(None) == 0
+
+
+def test_create_rejects_null_out_pointer(lib):
+    assert lib.vla_create(None, 0) == 1
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU error path")
+def test_create_without_a_gpu_reports_an_error(lib):
+    h = ctypes.c_void_p()
+    code = lib.vla_create(ctypes.byref(h), 0)
+    assert code in (1, 3) and not h.value
+    assert lib.vla_last_error(None)
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    import sherman_morrison_inverse_gb300 as vla
+    monkeypatch.setattr(vla, "_lib", None)
+    monkeypatch.setattr(vla, "library_path", lambda: str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        vla.load_library()
