@@ -218,8 +218,13 @@ def main():
     ap.add_argument("--chunk", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--T", type=int, default=None,
+                    help="truncate the sequence (profiling a smaller case; not a bench number)")
     args = ap.parse_args()
     w = workloads.get(int(args.workload) if args.workload.isdigit() else args.workload)
+    T_full = w.T
+    if args.T is not None:
+        w = w.with_(T=args.T)
 
     if args.impl == "reference":
         run_reference(args, w)
@@ -233,7 +238,7 @@ def main():
     stream = torch.cuda.current_stream(dev)
     h = vla.Handle(local)
 
-    x = workloads.make_inputs(w)
+    x = workloads.make_inputs(w.with_(T=T_full), T=w.T)
     B, H, T = w.B, w.H, w.T
     g = {k: x[k].reshape(B, H, *x[k].shape[1:]).to(dev).contiguous() for k in ("q", "k", "v", "u")}
     A = x["A0"].reshape(B, H, w.d, w.d).to(dev).contiguous()

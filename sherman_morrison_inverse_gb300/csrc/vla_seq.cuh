@@ -337,7 +337,7 @@ __global__ void __launch_bounds__(SeqCfg<D>::NT, 1) seq_scan_kernel(ScanArgs a) 
         if (c == 0) go[t_prev * D + row] = from_f32<TIO>(cf * num_prev / den_prev);
       }
       const float yv = sigma * yr;                // S_{t-1} phi(q_t) for this row
-      if (sigma < 1e-30f) {                       // keep S_reg in range: fold the scale in
+      if (sigma < 0x1p-16f) {                     // keep S_reg (and its squared norm) in range
 #pragma unroll
         for (int j = 0; j < CPT; ++j) Sr[j] *= sigma;
         sigma = 1.f;

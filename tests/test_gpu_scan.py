@@ -117,9 +117,13 @@ def test_split_calls_match_one_call():
 
 
 def test_guard_through_the_abi():
+    """A0 = -I and a unit u give delta = 0 at step 1: the guard replaces the update
+    with A += 1e-6 I.  Later directions are scaled by 1/2 so that their deltas
+    (about 3/4) sit far from the threshold in both precisions."""
     d = 16
-    x = workloads.gaussian_inputs(2, 3, d, d, 1, "f32", seed=5)
+    x = workloads.gaussian_inputs(2, 6, d, d, 1, "f32", seed=5)
     x["A0"] = -torch.eye(d).expand(2, d, d).contiguous()
+    x["u"][:, 1:] *= 0.5
     got = gpu_scan(x, 1, 2, P=0, eps_n=0.0, tau=1e30)
     ref = oracle_scan(x, P=0, eps_n=0.0, tau=1e30, trace=True)
     assert ref[4]["guard"][:, 0, 0].all()
