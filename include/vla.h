@@ -34,7 +34,8 @@
  *     S    : [B, H, d_v, d]        float32, read and written in place
  *     n    : [B, H, d]             float32, read and written in place
  *   q, k, v and u must start on a 16-byte boundary (they are streamed with bulk
- *   asynchronous copies).  o must not overlap any input.
+ *   asynchronous copies), and so must A and S (moved as 16-byte vectors).  o
+ *   must not overlap any input.
  * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *   stream).  Every call that launches work is asynchronous on that stream; it
  *   returns after the launch.  Errors of the kernel itself are reported through
@@ -103,7 +104,7 @@ vla_err_t vla_create(vla_handle_t* h, int device);
  *   stream    cudaStream_t as void*.
  *
  * Errors (returned before any launch, nothing is written): INVALID_ARG for a
- * NULL handle or pointer, negative size, misaligned q/k/v/u, P < 0, t0 < 0,
+ * NULL handle or pointer, negative size, misaligned q/k/v/u/A/S, P < 0, t0 < 0,
  * tau <= 0 or NaN, non-finite eps_n; UNSUPPORTED for shapes that are not built;
  * CUDA if the launch fails.  There is no CPU fallback. */
 vla_err_t vla_scan_fwd(vla_handle_t h,

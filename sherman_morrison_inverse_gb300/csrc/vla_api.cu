@@ -12,11 +12,15 @@ cudaError_t launch_seq_d16(int r, bool bf16, const ScanArgs& a, cudaStream_t s, 
 cudaError_t launch_seq_d64(int r, bool bf16, const ScanArgs& a, cudaStream_t s, bool* built);
 cudaError_t launch_seq_d128(int r, bool bf16, const ScanArgs& a, cudaStream_t s, bool* built);
 
+cudaError_t launch_seq_block_d16(int r, bool bf16, const ScanArgs& a, cudaStream_t s, bool* built);
+cudaError_t launch_seq_block_d64(int r, bool bf16, const ScanArgs& a, cudaStream_t s, bool* built);
+cudaError_t launch_seq_block_d128(int r, bool bf16, const ScanArgs& a, cudaStream_t s, bool* built);
+
 cudaError_t launch_seq(int d, int r, bool bf16, const ScanArgs& a, cudaStream_t s, bool* built) {
   switch (d) {
-    case 16: return launch_seq_d16(r, bf16, a, s, built);
-    case 64: return launch_seq_d64(r, bf16, a, s, built);
-    case 128: return launch_seq_d128(r, bf16, a, s, built);
+    case 16: return launch_seq_block_d16(r, bf16, a, s, built);
+    case 64: return launch_seq_block_d64(r, bf16, a, s, built);
+    case 128: return launch_seq_block_d128(r, bf16, a, s, built);
     default: *built = false; return cudaSuccess;
   }
 }
@@ -114,8 +118,8 @@ vla_err_t vla_scan_fwd(vla_handle_t h, const void* q, const void* k, const void*
   if (!A || !S || !n) return fail(h, VLA_ERR_INVALID_ARG, "vla_scan_fwd: NULL state pointer");
   if (T == 0) return VLA_OK;
   if (!q || !k || !v || !u || !o) return fail(h, VLA_ERR_INVALID_ARG, "vla_scan_fwd: NULL stream pointer");
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(u))
-    return fail(h, VLA_ERR_INVALID_ARG, "vla_scan_fwd: q, k, v and u must be 16-byte aligned");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(u) || !aligned16(A) || !aligned16(S))
+    return fail(h, VLA_ERR_INVALID_ARG, "vla_scan_fwd: q, k, v, u, A and S must be 16-byte aligned");
   if (d != dv) return fail(h, VLA_ERR_UNSUPPORTED, "vla_scan_fwd: built only for d == dv");
 
   vla::ScanArgs a{};

@@ -167,6 +167,7 @@ def test_argument_errors_launch_nothing():
     t = _raw_tensors()
     before = {k: v.clone() for k, v in t.items()}
     assert _raw_call(h, t, u=t["u"].data_ptr() + 4) == 1          # misaligned
+    assert _raw_call(h, t, A=t["A"].data_ptr() + 8) == 1
     assert _raw_call(h, t, q=0) == 1                              # NULL
     assert _raw_call(h, t, P=-1) == 1
     assert _raw_call(h, t, tau=0.0) == 1
