@@ -8,10 +8,6 @@
 #include <string>
 
 namespace vla {
-cudaError_t launch_seq_d16(int r, bool bf16, const ScanArgs& a, cudaStream_t s, bool* built);
-cudaError_t launch_seq_d64(int r, bool bf16, const ScanArgs& a, cudaStream_t s, bool* built);
-cudaError_t launch_seq_d128(int r, bool bf16, const ScanArgs& a, cudaStream_t s, bool* built);
-
 cudaError_t launch_seq_block_d16(int r, bool bf16, const ScanArgs& a, cudaStream_t s, bool* built);
 cudaError_t launch_seq_block_d64(int r, bool bf16, const ScanArgs& a, cudaStream_t s, bool* built);
 cudaError_t launch_seq_block_d128(int r, bool bf16, const ScanArgs& a, cudaStream_t s, bool* built);

@@ -1,45 +1,47 @@
-// Blocked sequential VLA scan for sm_103a: KS steps per reduction round.
+// Blocked, warp-specialised sequential VLA scan for sm_103a.
 //
-// Same recurrence as the step-by-step scan ("Mathematical Primitives" §2-§5,
-// README "VLA v3" items 1-5), taken KS steps (M = KS * r directions) per
-// reduction round in exact Woodbury form ("Mathematical Primitives" §3 names the
-// identity; the gist.science summary §2.4 the parallel formulation).  With
-// A_0 the inverse at the start of the round and U = [u_1 .. u_M]:
+// The recurrence ("Mathematical Primitives" §2-§5, README "VLA v3" items 1-5)
+// is taken KS steps (M = KS r directions) per reduction round in exact
+// Woodbury form ("Mathematical Primitives" §3 names the identity; the
+// gist.science summary §2.4 the parallel formulation).  With A_0 the inverse at
+// the start of a round and U = [u_1 .. u_M]:
 //
 //   P = A_0 U,  Q_t = A_0 s_t,  G = I + U^T P = L D L^T   (D_jj = the sequential deltas)
-//   A_after   = A_0 - P G^{-1} P^T                           (= M rank-1 updates)
-//   alpha_t   = Q_t - P_{<=e_t} G_{<=e_t}^{-1} (U^T Q_t)_{<=e_t}
-//               (e_t = last direction of step t; leading blocks of G)
+//   A_after  = A_0 - P G^{-1} P^T                            (= the M rank-1 updates)
+//   alpha_t  = Q_t - P_{<=e_t} G_{<=e_t}^{-1} (U^T Q_t)_{<=e_t}   (e_t: last direction of step t)
 //
-// so one round needs M + KS matrix-vector products with A_0 (the same count as
-// the step-by-step form) but one set of reductions instead of M.  The S side
-// lags one round: round R applies S += v alpha^T for the steps completed in
-// round R-1, whose alpha vectors are then in shared memory, and writes their
-// outputs:  o_t = (S_0 phi(q_t) + sum_{t'<=t} v_t' (alpha_t' . phi(q_t))) / den_t.
+// One round needs M + KS products with A_0 (as many as the step-by-step form)
+// but one set of reductions instead of M.
 //
-// Round structure (one CTA per (batch, head) pair, NT = 2d threads):
-//   phase P  partial products of the thread's 4 x (d/8) pieces of A and S with
-//            every vector of the round (packed FFMA2), reduce-scatter across the
-//            8 lanes of a row group, rows written to shared memory      -> barrier
-//   phase G  the small Gram scalars (u_a.P_b, u_a.Q_t, alpha.phi(q), |alpha|^2)
-//            as 64-element dot products spread over the warps           -> barrier
-//   phase U  LDL^T of G (every thread, in registers), A update, alpha for
-//            this round's steps (one writer per element), and the S side of the
-//            previous round's steps.
+// One CTA per (batch, head) pair, two warp groups of 2d threads each:
+//   A group  owns A in registers; per round: products with A_0 (packed FFMA2),
+//            reduce-scatter over the 8 lanes of a row group, Gram scalars
+//            (u_a.P_b, u_a.Q_t) as dot products, LDL^T of G in registers,
+//            A update, alpha (one writer per element) -> shared memory.
+//   S group  owns S in registers and lags one round: S phi(q) products, the
+//            scalars alpha_t'.phi(q_t) and |alpha_t|^2, renormalisation, the
+//            outputs o_t = (S_0 phi(q_t) + sum_{t'<=t} v_t'(alpha_t'.phi(q_t))) / den_t
+//            and S += v alpha^T.
+// Each SM sub-partition runs one warp of each group, so one group's reduction
+// latency hides behind the other's arithmetic.  alpha is handed over through a
+// double-buffered shared array guarded by per-parity named barriers
+// (FULL[p]: A arrives, S syncs; EMPTY[p]: S arrives, A syncs), so neither side
+// can run two rounds ahead of the other.
 //
-// Singularity guard: a pivot |D_jj| < 1e-6 means the sequential recurrence
-// would take the guard at that direction.  The round then applies nothing and
-// the same directions are replayed one per round, where the pivot is the
-// sequential delta itself and the guard (A += 1e-6 I instead of the update) is
-// taken exactly as the pages state it.
+// Singularity guard: a pivot |D_jj| < 1e-6 means the sequential recurrence would
+// take the guard at that direction.  The round then applies nothing and its
+// directions are replayed one per round, where the pivot is the sequential
+// delta itself and the guard (A += 1e-6 I instead of the update) is taken as the
+// pages state it.
 //
 // Renormalisation: S = sigma * S_reg (lazy scale).  Each round reduces ||S_reg||^2
-// exactly; with ||alpha_t|| and ||v_t|| the bound ||S_t|| <= ||S_0|| + sum ||v|| ||alpha||
-// decides that no step of the chunk can exceed tau.  Otherwise an extra
-// reduction gives the exact per-step norms from
-//   ||S_t||^2 = ||S_{t-1}||^2 + 2 v_t^T S_{t-1} alpha_t + |v_t|^2 |alpha_t|^2
+// exactly; with |alpha_t| and |v_t| the bound ||S_t|| <= ||S_0|| + sum |v||alpha| shows
+// that no step of the chunk can exceed tau.  Otherwise an extra reduction gives the
+// exact per-step norms from ||S_t||^2 = ||S_{t-1}||^2 + 2 v_t^T S_{t-1} alpha_t + |v_t|^2|alpha_t|^2
 // and the decisions are taken step by step.
 #pragma once
+
+#include <type_traits>
 
 #include "vla_internal.cuh"
 
@@ -49,9 +51,20 @@ namespace blk {
 
 constexpr float kGuardEps = 1e-6f;
 constexpr float kReadoutEps = 1e-6f;
+// named barriers (0 is __syncthreads)
+constexpr int BAR_A = 1, BAR_S = 2, BAR_FULL0 = 3, BAR_EMPTY0 = 5;
+
+__device__ __forceinline__ void bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void bar_arrive(int id, int n) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
 
 __host__ __device__ constexpr int pow2_ceil(int x) { return x <= 1 ? 1 : 2 * pow2_ceil((x + 1) / 2); }
 __host__ __device__ constexpr int log2i(int x) { return x <= 1 ? 0 : 1 + log2i(x / 2); }
+__host__ __device__ constexpr int up2(int x) { return (x + 1) / 2 * 2; }
+__host__ __device__ constexpr int up4(int x) { return (x + 3) / 4 * 4; }
 
 template <int D>
 struct Geom {
@@ -59,63 +72,68 @@ struct Geom {
   static constexpr int LPR = (D == 16) ? 4 : 8;   // lanes per row group
   static constexpr int CPT = D / LPR;             // columns per thread
   static constexpr int NCH = CPT / 4;             // float4 pieces per vector
+  static constexpr int NCP = CPT / 2;             // float2 pairs per row piece
   static constexpr int NG = D / RPT;              // row groups
-  static constexpr int NT = NG * LPR;             // threads (2 d)
-  static constexpr int NW = NT / 32;
+  static constexpr int GT = NG * LPR;             // threads per warp group (2 d)
+  static constexpr int GW = GT / 32;              // warps per group
+  static constexpr int NT = 2 * GT;               // threads per CTA
   static constexpr int NSTAGE = 2;
-  static_assert(NT == 2 * D, "two threads per element of a d-vector");
+  static_assert(GT == 2 * D && GT % 32 == 0, "two threads per element of a d-vector");
 };
 
-// shared memory bytes for a tile of ts steps (raw ring + records + scratch + buffers)
 template <int D, int R, int KS, typename TIO>
 __host__ __device__ constexpr size_t smem_bytes_for(int ts) {
   return (size_t)Geom<D>::NSTAGE * ts * (3 * D + R * D) * sizeof(TIO) +
-         sizeof(float) * ((size_t)2 * ts * ((R + 3) * D + 4) + (size_t)ts * D + 4096 + 8 * KS * D * 4);
+         sizeof(float) * ((size_t)2 * ts * ((R + 3) * D + 4) + (size_t)ts * D + 4096 + 10 * KS * D * R);
 }
 template <int D, int R, int KS, typename TIO>
 __host__ __device__ constexpr int pick_ts() {
-  return smem_bytes_for<D, R, KS, TIO>(32) <= 200 * 1024 ? 32 : smem_bytes_for<D, R, KS, TIO>(16) <= 200 * 1024 ? 16 : 8;
+  return smem_bytes_for<D, R, KS, TIO>(32) <= 200 * 1024 ? 32
+         : smem_bytes_for<D, R, KS, TIO>(16) <= 200 * 1024 ? 16 : 8;
 }
 
 template <int D, int R, int KS, typename TIO>
 struct Cfg {
   using Gm = Geom<D>;
-  static constexpr int TS = pick_ts<D, R, KS, TIO>();         // steps per tile
-  static constexpr int M = KS * R;                            // directions per round
-  static constexpr int NV = M + 2 * KS;                       // vectors per round: P, Q, Y
-  static constexpr int NVAL = Gm::RPT * NV;
-  static constexpr int KV = NVAL / Gm::LPR;                   // values a lane keeps after the reduce-scatter
-  static_assert(NVAL % Gm::LPR == 0, "reduce-scatter must split evenly");
-  // dot-product jobs of phase G
-  static constexpr int NJG = M * (M + 1) / 2;                 // u_a . P_b, a <= b
-  static constexpr int NJH = R * KS * (KS + 1) / 2;           // u_a . Q_t, a <= e_t
-  static constexpr int NJQ = KS * (KS + 1) / 2;               // alpha_t' . phi(q_t), t' <= t
-  static constexpr int NJN = KS;                              // alpha_t . alpha_t
-  static constexpr int NJOB = NJG + NJH + NJQ + NJN;
-  static constexpr int JPW = (NJOB + Gm::NW - 1) / Gm::NW;    // jobs per warp
-  static constexpr int NS = pow2_ceil(JPW) < 32 ? pow2_ceil(JPW) : 32;
-  static constexpr int NPASS = (JPW + 31) / 32;
-  static constexpr int NMINI = KS + KS * (KS + 1);            // exact-norm scalars: v^T S alpha, alpha Gram, v Gram
-  // step record (floats): u[R][D] | s[D] | phi(q)[D] | v[D] | den, |v|, 0, 0
+  static constexpr int TS = pick_ts<D, R, KS, TIO>();   // steps per tile
+  static constexpr int M = KS * R;                      // directions per round
+  static constexpr int NVA = up2(M + KS);               // A-group vectors (P, Q, zero padding)
+  static constexpr int NVS = up2(KS);                   // S-group vectors (Y, zero padding)
+  static constexpr int KVA = Gm::RPT * NVA / Gm::LPR;   // values a lane keeps after the reduce-scatter
+  static constexpr int KVS = Gm::RPT * NVS / Gm::LPR;
+  static_assert((Gm::RPT * NVA) % Gm::LPR == 0 && (Gm::RPT * NVS) % Gm::LPR == 0, "even split");
+  // dot-product jobs
+  static constexpr int NJG = M * (M + 1) / 2;           // u_a . P_b, a <= b
+  static constexpr int NJH = R * KS * (KS + 1) / 2;     // u_a . Q_t, a <= e_t
+  static constexpr int NJA = NJG + NJH;
+  static constexpr int NJQ = KS * (KS + 1) / 2;         // alpha_t' . phi(q_t), t' <= t
+  static constexpr int NJS = NJQ + KS;                  // + alpha_t . alpha_t
+  static constexpr int NSA = pow2_ceil((NJA + Gm::GW - 1) / Gm::GW);   // job slots per A warp
+  static constexpr int NSS = pow2_ceil((NJS + Gm::GW - 1) / Gm::GW);
+  static_assert(NSA <= 32 && NSS <= 32, "one pass of job slots");
+  static constexpr int NMINI = KS + KS * (KS + 1);      // exact-norm scalars
+  static constexpr int MSTR = up4(NMINI);
+  // step record (floats): u[R][D] | s[D] | phi(q)[D] | v[D] | 1/den, |v|, 0, 0
   static constexpr int OFF_U = 0, OFF_S = R * D, OFF_Q = (R + 1) * D, OFF_V = (R + 2) * D;
   static constexpr int OFF_SC = (R + 3) * D;
   static constexpr int REC = (R + 3) * D + 4;
-  // raw tile bytes (q, k, v: TS x D; u: TS x R x D)
   static constexpr uint32_t QB = TS * D * sizeof(TIO);
   static constexpr uint32_t UB = TS * R * D * sizeof(TIO);
   static constexpr uint32_t STAGE = 3 * QB + UB;
   // shared memory map (float offsets after the raw ring)
-  static constexpr int F_PRE = 0;                                    // [2][TS][REC]
-  static constexpr int F_ZERO = F_PRE + 2 * TS * REC;                // [REC] zeros
-  static constexpr int F_PROD = F_ZERO + REC;                        // [TS][D] scratch
-  static constexpr int F_P = F_PROD + TS * D;                        // [2][M][D]
-  static constexpr int F_Q = F_P + 2 * M * D;                        // [2][KS][D]
-  static constexpr int F_Y = F_Q + 2 * KS * D;                       // [2][KS][D]
-  static constexpr int F_AL = F_Y + 2 * KS * D;                      // [2][KS][D]
-  static constexpr int F_RES = F_AL + 2 * KS * D;                    // [NJOB] (+pad)
-  static constexpr int F_WP = F_RES + ((NJOB + 3) / 4) * 4;          // [2][NW] norm partials (+pad)
-  static constexpr int F_MINI = F_WP + ((2 * Gm::NW + 3) / 4) * 4;   // [NW][32]
-  static constexpr int F_END = F_MINI + Gm::NW * 32;
+  static constexpr int F_PRE = 0;                          // [2][TS][REC]
+  static constexpr int F_ZERO = F_PRE + 2 * TS * REC;      // [REC]   ghost step: zeros, 1/den = 1
+  static constexpr int F_PROD = F_ZERO + REC;              // [TS][D] prologue scratch
+  static constexpr int F_P = F_PROD + TS * D;              // [2][M][D]
+  static constexpr int F_Q = F_P + 2 * M * D;              // [2][KS][D]
+  static constexpr int F_Y = F_Q + 2 * KS * D;             // [2][KS][D]
+  static constexpr int F_AL = F_Y + 2 * KS * D;            // [2][KS][D]
+  static constexpr int F_RA = F_AL + 2 * KS * D;           // [NJA]
+  static constexpr int F_RS = F_RA + up4(NJA);             // [NJS]
+  static constexpr int F_WP = F_RS + up4(NJS);             // [2][GW]
+  static constexpr int F_MINI = F_WP + up4(2 * Gm::GW);    // [GW][MSTR]
+  static constexpr int F_INFO = F_MINI + Gm::GW * MSTR;    // [2][8] ints
+  static constexpr int F_END = F_INFO + 16;
   static constexpr size_t raw_bytes = (size_t)Gm::NSTAGE * STAGE;
   static constexpr size_t bar_off = raw_bytes + sizeof(float) * (size_t)F_END;
   static constexpr size_t bytes = bar_off + 16 * Gm::NSTAGE + 16;
@@ -126,6 +144,29 @@ struct Cfg {
 
 __device__ __forceinline__ float2 f2(float x, float y) { return make_float2(x, y); }
 
+// Reduce-scatter of N values across the lanes selected by masks LM, LM/2, .., 1:
+// afterwards lane position blk (its bits under those masks) holds the full sums
+// of slots [blk*N/L, (blk+1)*N/L) in v[0 .. N/L).
+template <int N, int LM>
+__device__ __forceinline__ void reduce_scatter(float (&v)[N], int lanebits) {
+  int n = N;
+#pragma unroll
+  for (int m = LM; m >= 1; m >>= 1) {
+    if (n < 2) break;
+    const bool hi = (lanebits & m) != 0;
+    const int h = n / 2;
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) {
+      if (i < h) {
+        const float send = hi ? v[i] : v[i + h];
+        const float keep = hi ? v[i + h] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+      }
+    }
+    n = h;
+  }
+}
+
 }  // namespace blk
 
 template <int D, int R, int KS, typename TIO>
@@ -133,21 +174,23 @@ __global__ void __launch_bounds__(blk::Geom<D>::NT, 1) seq_block_kernel(ScanArgs
   using namespace blk;
   using Gm = Geom<D>;
   using C = Cfg<D, R, KS, TIO>;
-  constexpr int RPT = Gm::RPT, LPR = Gm::LPR, CPT = Gm::CPT, NCH = Gm::NCH, NT = Gm::NT, NW = Gm::NW;
-  constexpr int TS = C::TS, NSTAGE = Gm::NSTAGE;
-  constexpr int M = C::M, NV = C::NV, KV = C::KV, REC = C::REC;
-  constexpr int NCP = CPT / 2;  // float2 pairs per row piece
+  constexpr int RPT = Gm::RPT, LPR = Gm::LPR, NCH = Gm::NCH, NCP = Gm::NCP, GT = Gm::GT, GW = Gm::GW;
+  constexpr int NT = Gm::NT, TS = C::TS, NSTAGE = Gm::NSTAGE;
+  constexpr int M = C::M, REC = C::REC;
   constexpr float kInvSqrtD = (float)(D == 16 ? 0.25 : D == 64 ? 0.125 : 0.08838834764831845);
 
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* raw = smem;
-  float* sf = reinterpret_cast<float*>(smem + C::raw_bytes);   // float-addressed region
+  float* sf = reinterpret_cast<float*>(smem + C::raw_bytes);
+  int* info = reinterpret_cast<int*>(sf + C::F_INFO);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::bar_off);
   volatile int* flag = reinterpret_cast<volatile int*>(smem + C::bar_off + 16 * NSTAGE);
 
   const int tid = threadIdx.x;
-  const int lane = tid & 31, warp = tid >> 5;
-  const int g = tid / LPR, c = tid % LPR;       // row group, lane within the group
+  const bool isA = tid < GT;
+  const int gid = isA ? tid : tid - GT;          // thread index within its group
+  const int lane = tid & 31, gw = gid >> 5;      // warp within the group
+  const int g = gid / LPR, c = gid % LPR;        // row group, lane within it
   const int row0 = g * RPT;
   const long long pair = blockIdx.x;
   const long long T = a.T;
@@ -161,27 +204,9 @@ __global__ void __launch_bounds__(blk::Geom<D>::NT, 1) seq_block_kernel(ScanArgs
   float* gS = a.S + pair * D * D;
   float* gn = a.n + pair * D;
 
-  // column of element (kk, e) of this thread's row piece
   auto colof = [&](int kk, int e) { return 4 * c + 4 * LPR * kk + e; };
 
-  // ---- state into registers: rows row0 .. row0+RPT-1, columns colof(kk, e)
-  float2 A2[RPT][NCP], S2[RPT][NCP];
-#pragma unroll
-  for (int r = 0; r < RPT; ++r) {
-#pragma unroll
-    for (int kk = 0; kk < NCH; ++kk) {
-      const float4 av = *reinterpret_cast<const float4*>(gA + (row0 + r) * D + colof(kk, 0));
-      const float4 sv = *reinterpret_cast<const float4*>(gS + (row0 + r) * D + colof(kk, 0));
-      A2[r][2 * kk] = f2(av.x, av.y);
-      A2[r][2 * kk + 1] = f2(av.z, av.w);
-      S2[r][2 * kk] = f2(sv.x, sv.y);
-      S2[r][2 * kk + 1] = f2(sv.z, sv.w);
-    }
-  }
-  float n_i = (tid < D) ? gn[tid] : 0.f;     // normaliser element tid (prologue prefix sums)
-
-  // zero record, barriers
-  for (int e = tid; e < REC; e += NT) sf[C::F_ZERO + e] = (e == C::OFF_SC) ? 1.f : 0.f;  // ghost: den = 1
+  for (int e = tid; e < REC; e += NT) sf[C::F_ZERO + e] = (e == C::OFF_SC) ? 1.f : 0.f;
   if (tid == 0) {
     for (int s = 0; s < NSTAGE; ++s) mbar_init(&bars[s], 1);
     fence_mbar_init();
@@ -207,702 +232,748 @@ __global__ void __launch_bounds__(blk::Geom<D>::NT, 1) seq_block_kernel(ScanArgs
     for (int j = 0; j < NSTAGE && j < ntiles; ++j) issue(j);
   }
 
-  // ---- per-tile prologue: float32 records, den_t = n_t . phi(q_t) + 1e-6, |v_t|
-  int loaded = -1;
-  bool timed_out = false;
-  auto prologue = [&](int tile) -> bool {
-    const int stage = tile % NSTAGE;
-    if (tid == 0) {
-      if (!mbar_wait_bounded(&bars[stage], (uint32_t)((tile / NSTAGE) & 1))) *flag = 1;
-    }
-    __syncthreads();
-    if (*flag) return false;
-    const long long t_start = (long long)tile * TS;
-    const int nst = (int)min((long long)TS, T - t_start);
-    const TIO* rq = reinterpret_cast<const TIO*>(raw + stage * C::STAGE);
-    const TIO* rk = reinterpret_cast<const TIO*>(raw + stage * C::STAGE + C::QB);
-    const TIO* rv = reinterpret_cast<const TIO*>(raw + stage * C::STAGE + 2 * C::QB);
-    const TIO* ru = reinterpret_cast<const TIO*>(raw + stage * C::STAGE + 3 * C::QB);
-    float* pre = sf + C::F_PRE + (tile & 1) * TS * REC;
-    for (int e = tid; e < nst * R * D; e += NT) {
-      const int t = e / (R * D), off = e - t * (R * D);
-      pre[t * REC + C::OFF_U + off] = to_f32(ru[e]);
-    }
-    for (int e = tid; e < nst * D; e += NT) {
-      const int t = e / D, i = e - t * D;
-      float* rec = pre + t * REC;
-      rec[C::OFF_S + i] = phi_elu1(to_f32(rk[e])) * kInvSqrtD;
-      rec[C::OFF_Q + i] = phi_elu1(to_f32(rq[e]));
-      rec[C::OFF_V + i] = to_f32(rv[e]);
-    }
-    __syncthreads();
-    float* prod = sf + C::F_PROD;
-    if (tid < D) {
-      for (int t = 0; t < nst; ++t) {
-        n_i += phi_elu1(to_f32(rk[t * D + tid]));
-        prod[t * D + tid] = n_i * pre[t * REC + C::OFF_Q + tid];
-      }
-    }
-    __syncthreads();
-    // den_t and |v_t|: warp w takes steps w, w + NW, ...
-    for (int t = warp; t < nst; t += NW) {
-      float dn = 0.f, vv = 0.f;
-      for (int i = lane; i < D; i += 32) {
-        dn += prod[t * D + i];
-        const float x = pre[t * REC + C::OFF_V + i];
-        vv = fmaf(x, x, vv);
-      }
-#pragma unroll
-      for (int m = 16; m >= 1; m >>= 1) {
-        dn += __shfl_xor_sync(0xffffffffu, dn, m);
-        vv += __shfl_xor_sync(0xffffffffu, vv, m);
-      }
-      if (lane == 0) {
-        pre[t * REC + C::OFF_SC] = dn + kReadoutEps;
-        pre[t * REC + C::OFF_SC + 1] = sqrtf(vv);
-      }
-    }
-    __syncthreads();
-    if (tid == 0 && tile + NSTAGE < ntiles) {
-      fence_proxy_async_smem();
-      issue(tile + NSTAGE);
-    }
-    return true;
-  };
-
-  // ---- round state (uniform across the CTA)
-  long long pos = 0;                 // next step to schedule
-  bool replay = false;
-  long long rep_pos = 0;             // first step of the chunk being replayed
-  int rep_total = 0, rep_col = 0;    // its directions, and the next one
-  // S-chunk: the steps completed in the previous round
-  int cS = 0;                        // real steps (0 .. KS)
-  int baseS = 0;                     // float offset of its first record
-  long long gS0 = 0;                 // local index of its first step
-  float sigma = 1.f;
-  int par = 0;
-  unsigned long long guard_cnt = 0, renorm_cnt = 0, replay_cnt = 0;
   unsigned int flags = 0;
-  const float tau = a.tau;
 
-  while (true) {
-    // ================= schedule the A-chunk of this round
-    int cA = 0;                      // real steps completed in this round
-    int baseA = 0;                   // record offset of the chunk's first step (normal) / the replayed step
-    int rep_j = 0;                   // replay: direction within the step
-    bool rep_completes = false;
-    bool nudgeA = false;
-    long long gA0 = 0;
-    bool haveA = false;
-    long long a_step = -1;           // a step inside the chunk (for the tile check)
-    if (replay) {
-      const long long st = rep_pos + rep_col / R;
-      rep_j = rep_col % R;
-      rep_completes = (rep_j == R - 1);
-      a_step = st;
-      gA0 = st;
-      cA = rep_completes ? 1 : 0;
-      haveA = true;
-      if (rep_completes && a.P > 0) nudgeA = ((a.t0 + st + 1) % a.P) == 0;
-    } else if (pos < T) {
-      long long cmax = min((long long)KS, T - pos);
-      cmax = min(cmax, (long long)(TS - (int)(pos % TS)));
-      if (a.P > 0) {
-        const long long to_nudge = a.P - ((a.t0 + pos) % a.P);   // steps up to and including the next nudge
-        if (to_nudge <= cmax) { cmax = to_nudge; nudgeA = true; }
+  if (isA) {
+    // =====================================================================
+    // A group
+    // =====================================================================
+    float2 A2[RPT][NCP];
+#pragma unroll
+    for (int r = 0; r < RPT; ++r)
+#pragma unroll
+      for (int kk = 0; kk < NCH; ++kk) {
+        const float4 av = *reinterpret_cast<const float4*>(gA + (row0 + r) * D + colof(kk, 0));
+        A2[r][2 * kk] = f2(av.x, av.y);
+        A2[r][2 * kk + 1] = f2(av.z, av.w);
       }
-      cA = (int)cmax;
-      gA0 = pos;
-      a_step = pos;
-      haveA = true;
-    }
-    if (!haveA && cS == 0) break;
-    if (haveA) {
-      const int tile = (int)(a_step / TS);
-      if (tile != loaded) {
-        if (!prologue(tile)) { timed_out = true; break; }
-        loaded = tile;
+    float n_i = (gid < D) ? gn[gid] : 0.f;
+
+    // per-tile prologue (A group only): float32 records, 1/den_t, |v_t|
+    auto prologue = [&](int tile) -> bool {
+      const int stage = tile % NSTAGE;
+      if (gid == 0) {
+        if (!mbar_wait_bounded(&bars[stage], (uint32_t)((tile / NSTAGE) & 1))) *flag = 1;
       }
-      baseA = C::F_PRE + (tile & 1) * TS * REC + (int)(a_step % TS) * REC;
-    }
-    // vector offsets of this round (float offsets into sf)
-    auto offU = [&](int col) -> int {        // direction col of the round
-      if (!haveA) return C::F_ZERO;
-      if (replay) return (col == 0) ? baseA + C::OFF_U + rep_j * D : C::F_ZERO;
-      const int t = col / R;
-      return (t < cA) ? baseA + t * REC + C::OFF_U + (col - t * R) * D : C::F_ZERO;
+      bar_sync(BAR_A, GT);
+      if (*flag) return false;
+      const long long t_start = (long long)tile * TS;
+      const int nst = (int)min((long long)TS, T - t_start);
+      const TIO* rq = reinterpret_cast<const TIO*>(raw + stage * C::STAGE);
+      const TIO* rk = reinterpret_cast<const TIO*>(raw + stage * C::STAGE + C::QB);
+      const TIO* rv = reinterpret_cast<const TIO*>(raw + stage * C::STAGE + 2 * C::QB);
+      const TIO* ru = reinterpret_cast<const TIO*>(raw + stage * C::STAGE + 3 * C::QB);
+      float* pre = sf + C::F_PRE + (tile & 1) * TS * REC;
+      float* prod = sf + C::F_PROD;
+      for (int e4 = gid; e4 < nst * R * D / 4; e4 += GT) {
+        const int e = 4 * e4, t = e / (R * D), off = e - t * (R * D);
+        const float4 x = make_float4(to_f32(ru[e]), to_f32(ru[e + 1]), to_f32(ru[e + 2]), to_f32(ru[e + 3]));
+        *reinterpret_cast<float4*>(pre + t * REC + C::OFF_U + off) = x;
+      }
+      for (int e4 = gid; e4 < nst * D / 4; e4 += GT) {
+        const int e = 4 * e4, t = e / D, i = e - t * D;
+        float* rec = pre + t * REC;
+        float kx[4], qx[4], vx[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          kx[j] = phi_elu1(to_f32(rk[e + j]));
+          qx[j] = phi_elu1(to_f32(rq[e + j]));
+          vx[j] = to_f32(rv[e + j]);
+        }
+        *reinterpret_cast<float4*>(rec + C::OFF_S + i) =
+            make_float4(kx[0] * kInvSqrtD, kx[1] * kInvSqrtD, kx[2] * kInvSqrtD, kx[3] * kInvSqrtD);
+        *reinterpret_cast<float4*>(rec + C::OFF_Q + i) = make_float4(qx[0], qx[1], qx[2], qx[3]);
+        *reinterpret_cast<float4*>(rec + C::OFF_V + i) = make_float4(vx[0], vx[1], vx[2], vx[3]);
+        *reinterpret_cast<float4*>(prod + e) = make_float4(kx[0], kx[1], kx[2], kx[3]);
+      }
+      bar_sync(BAR_A, GT);
+      if (gid < D) {   // n_t = n_{t-1} + phi(k_t); products n_t[i] phi(q_t)[i] in place of phi(k)
+        for (int t = 0; t < nst; ++t) {
+          n_i += prod[t * D + gid];
+          prod[t * D + gid] = n_i * pre[t * REC + C::OFF_Q + gid];
+        }
+      }
+      bar_sync(BAR_A, GT);
+      {  // 1/den_t and |v_t|: TPS threads per step
+        constexpr int TPS = GT / TS >= 1 ? GT / TS : 1;
+        constexpr int EPT = D / TPS;
+        static_assert(EPT % 4 == 0 && TPS <= 32, "den reduction layout");
+        const int t = gid / TPS, part = gid - t * TPS;
+        float dn = 0.f, vv = 0.f;
+        if (t < nst) {
+#pragma unroll
+          for (int j = 0; j < EPT; j += 4) {
+            const float4 p = *reinterpret_cast<const float4*>(prod + t * D + part * EPT + j);
+            const float4 w = *reinterpret_cast<const float4*>(pre + t * REC + C::OFF_V + part * EPT + j);
+            dn += (p.x + p.y) + (p.z + p.w);
+            vv = fmaf(w.x, w.x, fmaf(w.y, w.y, fmaf(w.z, w.z, fmaf(w.w, w.w, vv))));
+          }
+        }
+        // every lane of the warp takes part in the shuffles (a ragged tile leaves
+        // some lanes without a step)
+#pragma unroll
+        for (int m = TPS / 2; m >= 1; m >>= 1) {
+          dn += __shfl_xor_sync(0xffffffffu, dn, m);
+          vv += __shfl_xor_sync(0xffffffffu, vv, m);
+        }
+        if (t < nst && part == 0) {
+          pre[t * REC + C::OFF_SC] = __frcp_rn(dn + kReadoutEps);
+          pre[t * REC + C::OFF_SC + 1] = sqrtf(vv);
+        }
+      }
+      bar_sync(BAR_A, GT);
+      if (gid == 0 && tile + NSTAGE < ntiles) {
+        fence_proxy_async_smem();
+        issue(tile + NSTAGE);
+      }
+      return true;
     };
-    auto recA = [&](int t) -> int {          // record of step slot t (s, phi(q), v)
-      if (!haveA) return C::F_ZERO;
-      if (replay) return (t == 0 && rep_completes) ? baseA : C::F_ZERO;
-      return (t < cA) ? baseA + t * REC : C::F_ZERO;
-    };
-    auto recS = [&](int t) -> int { return (t < cS) ? baseS + t * REC : C::F_ZERO; };
-    const int pbuf = C::F_P + par * M * D, qbuf = C::F_Q + par * KS * D, ybuf = C::F_Y + par * KS * D;
-    const int abuf = C::F_AL + par * KS * D, abuf_prev = C::F_AL + (par ^ 1) * KS * D;
 
-    // ================= phase P: partial products
-    float vals[RPT * NV];
-    {
-      float2 acc[RPT][NV];
-#pragma unroll
-      for (int r = 0; r < RPT; ++r)
-#pragma unroll
-        for (int v = 0; v < NV; ++v) acc[r][v] = f2(0.f, 0.f);
-#pragma unroll
-      for (int v = 0; v < NV; ++v) {
-        int base;
-        if (v < M) base = offU(v);
-        else if (v < M + KS) base = recA(v - M) + C::OFF_S;
-        else base = recS(v - M - KS) + C::OFF_Q;
-#pragma unroll
-        for (int kk = 0; kk < NCH; ++kk) {
-          const float4 x = *reinterpret_cast<const float4*>(sf + base + colof(kk, 0));
-          const float2 x0 = f2(x.x, x.y), x1 = f2(x.z, x.w);
-#pragma unroll
-          for (int r = 0; r < RPT; ++r) {
-            if (v < M + KS) {
-              acc[r][v] = __ffma2_rn(A2[r][2 * kk], x0, acc[r][v]);
-              acc[r][v] = __ffma2_rn(A2[r][2 * kk + 1], x1, acc[r][v]);
-            } else {
-              acc[r][v] = __ffma2_rn(S2[r][2 * kk], x0, acc[r][v]);
-              acc[r][v] = __ffma2_rn(S2[r][2 * kk + 1], x1, acc[r][v]);
-            }
+    long long pos = 0;
+    bool replay = false;
+    long long rep_pos = 0;
+    int rep_total = 0, rep_col = 0;
+    int loaded = -1;
+    unsigned long long guard_cnt = 0, replay_cnt = 0;
+    int par = 0;
+    int rnd = 0;
+    while (true) {
+      if (rnd >= 2) bar_sync(BAR_EMPTY0 + (rnd & 1), NT);   // S is done with round rnd-2
+      // ---------------- schedule this round's chunk
+      int cA = 0, rep_j = 0;
+      bool rep_completes = false, nudgeA = false, haveA = false;
+      long long gA0 = 0, a_step = 0;
+      if (replay) {
+        const long long st = rep_pos + rep_col / R;
+        rep_j = rep_col % R;
+        rep_completes = (rep_j == R - 1);
+        a_step = st;
+        gA0 = st;
+        cA = rep_completes ? 1 : 0;
+        haveA = true;
+        if (rep_completes && a.P > 0) nudgeA = ((a.t0 + st + 1) % a.P) == 0;
+      } else if (pos < T) {
+        long long cmax = min((long long)KS, T - pos);
+        cmax = min(cmax, (long long)(TS - (int)(pos % TS)));
+        if (a.P > 0) {
+          const long long to_nudge = a.P - ((a.t0 + pos) % a.P);
+          if (to_nudge <= cmax) { cmax = to_nudge; nudgeA = true; }
+        }
+        cA = (int)cmax;
+        gA0 = pos;
+        a_step = pos;
+        haveA = true;
+      }
+      bool stop = !haveA;
+      if (haveA) {
+        const int tile = (int)(a_step / TS);
+        if (tile != loaded) {
+          if (!prologue(tile)) {
+            stop = true;
+            flags |= kStatusTimeout;
           }
+          loaded = tile;
         }
       }
-#pragma unroll
-      for (int r = 0; r < RPT; ++r)
-#pragma unroll
-        for (int v = 0; v < NV; ++v) vals[r * NV + v] = acc[r][v].x + acc[r][v].y;
-    }
-    float ns;  // ||S_reg||^2 partial
-    {
-      float2 n2 = f2(0.f, 0.f);
-#pragma unroll
-      for (int r = 0; r < RPT; ++r)
-#pragma unroll
-        for (int p = 0; p < NCP; ++p) n2 = __ffma2_rn(S2[r][p], S2[r][p], n2);
-      ns = n2.x + n2.y;
-    }
-    // reduce-scatter across the LPR lanes of the row group
-    {
-      int n = RPT * NV;
-#pragma unroll
-      for (int m = LPR / 2; m >= 1; m >>= 1) {
-        const bool hi = (c & m) != 0;
-        const int h = n / 2;
-#pragma unroll
-        for (int i = 0; i < RPT * NV / 2; ++i) {
-          if (i < h) {
-            const float send = hi ? vals[i] : vals[i + h];
-            const float keep = hi ? vals[i + h] : vals[i];
-            vals[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
-          }
+      if (stop) {   // publish the end of the sequence to the S group
+        if (gid == 0) {
+          int* inf = info + (rnd & 1) * 8;
+          inf[0] = 0; inf[1] = 0; inf[2] = 0; inf[3] = 0; inf[4] = 1;
         }
-        n = h;
+        bar_arrive(BAR_FULL0 + (rnd & 1), NT);
+        ++rnd;
+        break;
       }
-    }
-    // lane c now holds the row sums of slots c*KV .. c*KV + KV - 1 (slot = r*NV + v)
-#pragma unroll
-    for (int i = 0; i < KV; ++i) {
-      const int slot = c * KV + i;
-      const int r = slot / NV, v = slot - r * NV;
-      const int row = row0 + r;
-      int dst;
-      if (v < M) dst = pbuf + v * D + row;
-      else if (v < M + KS) dst = qbuf + (v - M) * D + row;
-      else dst = ybuf + (v - M - KS) * D + row;
-      sf[dst] = vals[i];
-    }
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) ns += __shfl_xor_sync(0xffffffffu, ns, m);
-    if (lane == 0) sf[C::F_WP + par * NW + warp] = ns;
-    __syncthreads();  // ---------------------------------------------------- BAR1
+      const int baseA = C::F_PRE + ((int)(a_step / TS) & 1) * TS * REC + (int)(a_step % TS) * REC;
+      auto offU = [&](int col) -> int {
+        if (replay) return (col == 0) ? baseA + C::OFF_U + rep_j * D : C::F_ZERO;
+        const int t = col / R;
+        return (t < cA) ? baseA + t * REC + C::OFF_U + (col - t * R) * D : C::F_ZERO;
+      };
+      auto recA = [&](int t) -> int {
+        if (replay) return (t == 0 && rep_completes) ? baseA : C::F_ZERO;
+        return (t < cA) ? baseA + t * REC : C::F_ZERO;
+      };
+      const int pbuf = C::F_P + par * M * D, qbuf = C::F_Q + par * KS * D;
+      const int abuf = C::F_AL + (rnd & 1) * KS * D;
 
-    // ================= phase G: Gram scalars as dot products over d elements
-#pragma unroll
-    for (int pass = 0; pass < C::NPASS; ++pass) {
-      constexpr int NSL = C::NPASS > 1 ? 32 : C::NS;
-      float jv[NSL];
-#pragma unroll
-      for (int s = 0; s < NSL; ++s) {
-        const int j = (pass * 32 + s) * NW + warp;   // job index
-        int oa = C::F_ZERO, ob = C::F_ZERO;
-        if (j < C::NJG) {
-          int b = 0;
-#pragma unroll
-          for (int bb = 1; bb < M; ++bb) b += (j >= bb * (bb + 1) / 2) ? 1 : 0;
-          const int aa = j - b * (b + 1) / 2;
-          oa = offU(aa);
-          ob = pbuf + b * D;
-        } else if (j < C::NJG + C::NJH) {
-          const int h = j - C::NJG;
-          int t = 0;
-#pragma unroll
-          for (int tt = 1; tt < KS; ++tt) t += (h >= R * tt * (tt + 1) / 2) ? 1 : 0;
-          const int aa = h - R * t * (t + 1) / 2;
-          oa = offU(aa);
-          ob = qbuf + t * D;
-        } else if (j < C::NJG + C::NJH + C::NJQ) {
-          const int q = j - C::NJG - C::NJH;
-          int t = 0;
-#pragma unroll
-          for (int tt = 1; tt < KS; ++tt) t += (q >= tt * (tt + 1) / 2) ? 1 : 0;
-          const int tp = q - t * (t + 1) / 2;
-          oa = abuf_prev + tp * D;
-          ob = recS(t) + C::OFF_Q;
-        } else if (j < C::NJOB) {
-          const int t = j - C::NJG - C::NJH - C::NJQ;
-          oa = abuf_prev + t * D;
-          ob = oa;
-        }
-        float acc = 0.f;
-        if (D >= 32) {
-#pragma unroll
-          for (int e = 0; e < D / 32; ++e) {
-            const int i = lane + 32 * e;
-            acc = fmaf(sf[oa + i], sf[ob + i], acc);
-          }
-        } else if (lane < D) {
-          acc = sf[oa + lane] * sf[ob + lane];
-        }
-        jv[s] = acc;
-      }
-      // reduce-scatter over the warp: slot s ends in lanes with (lane >> (5 - log2 NSL)) == s
+      // ---------------- phase P: P = A_0 U, Q = A_0 Sigma (row pieces)
       {
-        int n = NSL;
+        float vals[RPT * C::NVA];
+        {
+          float2 acc[RPT][C::NVA];
 #pragma unroll
-        for (int m = 16; m >= 32 / NSL && m >= 1; m >>= 1) {
-          const bool hi = (lane & m) != 0;
-          const int h = n / 2;
+          for (int r = 0; r < RPT; ++r)
 #pragma unroll
-          for (int i = 0; i < NSL / 2; ++i) {
-            if (i < h) {
-              const float send = hi ? jv[i] : jv[i + h];
-              const float keep = hi ? jv[i + h] : jv[i];
-              jv[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+            for (int v = 0; v < C::NVA; ++v) acc[r][v] = f2(0.f, 0.f);
+#pragma unroll
+          for (int v = 0; v < M + KS; ++v) {
+            const int base = (v < M) ? offU(v) : recA(v - M) + C::OFF_S;
+#pragma unroll
+            for (int kk = 0; kk < NCH; ++kk) {
+              const float4 x = *reinterpret_cast<const float4*>(sf + base + colof(kk, 0));
+              const float2 x0 = f2(x.x, x.y), x1 = f2(x.z, x.w);
+#pragma unroll
+              for (int r = 0; r < RPT; ++r) {
+                acc[r][v] = __ffma2_rn(A2[r][2 * kk], x0, acc[r][v]);
+                acc[r][v] = __ffma2_rn(A2[r][2 * kk + 1], x1, acc[r][v]);
+              }
             }
           }
-          n = h;
+#pragma unroll
+          for (int r = 0; r < RPT; ++r)
+#pragma unroll
+            for (int v = 0; v < C::NVA; ++v) vals[r * C::NVA + v] = acc[r][v].x + acc[r][v].y;
         }
+        reduce_scatter<RPT * C::NVA, LPR / 2>(vals, c);
 #pragma unroll
-        for (int m = 32 / NSL / 2; m >= 1; m >>= 1) jv[0] += __shfl_xor_sync(0xffffffffu, jv[0], m);
+        for (int i = 0; i < C::KVA; ++i) {
+          const int slot = c * C::KVA + i;
+          const int r = slot / C::NVA, v = slot - r * C::NVA;
+          if (v < M) sf[pbuf + v * D + row0 + r] = vals[i];
+          else if (v < M + KS) sf[qbuf + (v - M) * D + row0 + r] = vals[i];
+        }
       }
-      constexpr int SH = 5 - log2i(NSL);
-      const int s_mine = lane >> SH;
-      const int j_mine = (pass * 32 + s_mine) * NW + warp;
-      if ((lane & ((1 << SH) - 1)) == 0 && j_mine < C::NJOB) sf[C::F_RES + j_mine] = jv[0];
-    }
-    __syncthreads();  // ---------------------------------------------------- BAR2
-
-    // ================= phase U
-    float res[C::NJOB];
+      bar_sync(BAR_A, GT);
+      // ---------------- phase G: u_a . P_b (a <= b), u_a . Q_t (a <= e_t)
+      {
+        auto jobs = [&](auto wtag) {
+          constexpr int W = decltype(wtag)::value;
+          float jv[C::NSA];
 #pragma unroll
-    for (int j = 0; j < C::NJOB; ++j) res[j] = sf[C::F_RES + j];
-
-    // ---- A side: LDL^T of G = I + U^T A_0 U
-    float Gm_[M][M];
+          for (int s = 0; s < C::NSA; ++s) {
+            const int j = s * GW + W;   // compile-time job index
+            float acc = 0.f;
+            if (j < C::NJA) {
+              int oa, ob;
+              if (j < C::NJG) {
+                int b = 0;
 #pragma unroll
-    for (int b = 0; b < M; ++b)
+                for (int bb = 1; bb < M; ++bb) b += (j >= bb * (bb + 1) / 2) ? 1 : 0;
+                oa = offU(j - b * (b + 1) / 2);
+                ob = pbuf + b * D;
+              } else {
+                const int h = j - C::NJG;
+                int t = 0;
 #pragma unroll
-      for (int aa = 0; aa <= b; ++aa) {
-        const float v = res[b * (b + 1) / 2 + aa] + (aa == b ? 1.f : 0.f);
-        Gm_[aa][b] = v;
-        Gm_[b][aa] = v;
+                for (int tt = 1; tt < KS; ++tt) t += (h >= R * tt * (tt + 1) / 2) ? 1 : 0;
+                oa = offU(h - R * t * (t + 1) / 2);
+                ob = qbuf + t * D;
+              }
+              if (D >= 32) {
+#pragma unroll
+                for (int e = 0; e < D / 32; ++e) acc = fmaf(sf[oa + lane + 32 * e], sf[ob + lane + 32 * e], acc);
+              } else if (lane < D) {
+                acc = sf[oa + lane] * sf[ob + lane];
+              }
+            }
+            jv[s] = acc;
+          }
+          reduce_scatter<C::NSA, 16>(jv, lane);
+          float x = jv[0];
+#pragma unroll
+          for (int m = 32 / C::NSA / 2; m >= 1; m >>= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
+          constexpr int SH = 5 - log2i(C::NSA);
+          const int j = (lane >> SH) * GW + W;
+          if ((lane & ((1 << SH) - 1)) == 0 && j < C::NJA) sf[C::F_RA + j] = x;
+        };
+        switch (gw) {
+          case 0: jobs(std::integral_constant<int, 0>{}); break;
+          case 1: if constexpr (GW > 1) jobs(std::integral_constant<int, 1>{}); break;
+          case 2: if constexpr (GW > 2) jobs(std::integral_constant<int, 2>{}); break;
+          case 3: if constexpr (GW > 3) jobs(std::integral_constant<int, 3>{}); break;
+          case 4: if constexpr (GW > 4) jobs(std::integral_constant<int, 4>{}); break;
+          case 5: if constexpr (GW > 5) jobs(std::integral_constant<int, 5>{}); break;
+          case 6: if constexpr (GW > 6) jobs(std::integral_constant<int, 6>{}); break;
+          case 7: if constexpr (GW > 7) jobs(std::integral_constant<int, 7>{}); break;
+          default: break;
+        }
       }
-    float Lm[M][M], Dv[M], iD[M];
-    bool bad = false;
+      bar_sync(BAR_A, GT);
+      // ---------------- phase U: LDL^T of G, A update, alpha
+      {
+        float res[C::NJA];
 #pragma unroll
-    for (int j = 0; j < M; ++j) {
-      float dj = Gm_[j][j];
+        for (int j = 0; j < C::NJA; ++j) res[j] = sf[C::F_RA + j];
+        float Lm[M][M], Dv[M], iD[M];
+        bool bad = false;
 #pragma unroll
-      for (int k = 0; k < j; ++k) dj = fmaf(-Lm[j][k] * Dv[k], Lm[j][k], dj);
-      Dv[j] = dj;
-      bad = bad || !(fabsf(dj) >= kGuardEps);
-      iD[j] = __frcp_rn(dj);
+        for (int j = 0; j < M; ++j) {
+          float dj = res[j * (j + 1) / 2 + j] + 1.f;
 #pragma unroll
-      for (int i = j + 1; i < M; ++i) {
-        float x = Gm_[i][j];
+          for (int k = 0; k < j; ++k) dj = fmaf(-Lm[j][k] * Dv[k], Lm[j][k], dj);
+          Dv[j] = dj;
+          bad = bad || !(fabsf(dj) >= kGuardEps);
+          iD[j] = __frcp_rn(dj);
 #pragma unroll
-        for (int k = 0; k < j; ++k) x = fmaf(-Lm[i][k] * Dv[k], Lm[j][k], x);
-        Lm[i][j] = x * iD[j];
-      }
-    }
-    // in a replay round only direction 0 is real: a bad pivot there is the guard
-    const bool guard = replay && bad;
-    const bool apply = haveA && (!bad || replay);
-    if (haveA && bad && !replay) {   // start replaying this chunk one direction per round
-      replay = true;
-      rep_pos = gA0;
-      rep_total = cA * R;
-      rep_col = 0;
-      ++replay_cnt;
-    }
-    // inverse of the unit lower triangle
-    float Li[M][M];
+          for (int i = j + 1; i < M; ++i) {
+            float x = res[i * (i + 1) / 2 + j];
 #pragma unroll
-    for (int i = 0; i < M; ++i) {
-#pragma unroll
-      for (int j = 0; j < M; ++j) Li[i][j] = (i == j) ? 1.f : 0.f;
-#pragma unroll
-      for (int j = 0; j < i; ++j) {
-        float x = 0.f;
-#pragma unroll
-        for (int k = j; k < i; ++k) x = fmaf(-Lm[i][k], Li[k][j], x);
-        Li[i][j] = x;
-      }
-    }
-    // per step: coefficients c_t = G_{<=e}^{-1} (U^T Q_t)_{<=e}
-    float cf[KS][M];
-#pragma unroll
-    for (int t = 0; t < KS; ++t) {
-      const int e = (t + 1) * R - 1;
-      float y[M];
-#pragma unroll
-      for (int aa = 0; aa < M; ++aa) {
-        float x = 0.f;
-        if (aa <= e) {
-#pragma unroll
-          for (int b = 0; b <= aa; ++b) {
-            const float h = (b <= e) ? res[C::NJG + R * t * (t + 1) / 2 + b] : 0.f;
-            x = fmaf(Li[aa][b], h, x);
+            for (int k = 0; k < j; ++k) x = fmaf(-Lm[i][k] * Dv[k], Lm[j][k], x);
+            Lm[i][j] = x * iD[j];
           }
         }
-        y[aa] = x * iD[aa];
-      }
-#pragma unroll
-      for (int aa = 0; aa < M; ++aa) {
-        float x = 0.f;
-        if (aa <= e) {
-#pragma unroll
-          for (int b = aa; b < M; ++b)
-            if (b <= e) x = fmaf(Li[b][aa], y[b], x);
+        if (!isfinite(Dv[0])) flags |= kStatusNonfinite;
+        const bool guard = replay && bad;            // replay rounds hold one real direction
+        const bool apply = !bad || replay;
+        if (bad && !replay) {                        // replay this chunk one direction per round
+          replay = true;
+          rep_pos = gA0;
+          rep_total = cA * R;
+          rep_col = 0;
+          ++replay_cnt;
         }
-        cf[t][aa] = x;
-      }
-    }
-    if (apply) {
-      // A -= P G^{-1} P^T   (guard: A += 1e-6 I instead)
-      if (!guard) {
-        float Gi[M][M];   // G^{-1} = L^{-T} D^{-1} L^{-1}
+        float Li[M][M];
 #pragma unroll
-        for (int i = 0; i < M; ++i)
+        for (int i = 0; i < M; ++i) {
 #pragma unroll
-          for (int j = 0; j < M; ++j) {
+          for (int j = 0; j < M; ++j) Li[i][j] = (i == j) ? 1.f : 0.f;
+#pragma unroll
+          for (int j = 0; j < i; ++j) {
             float x = 0.f;
 #pragma unroll
-            for (int k = (i > j ? i : j); k < M; ++k) x = fmaf(Li[k][i] * iD[k], Li[k][j], x);
-            Gi[i][j] = x;
-          }
-        float Pt[RPT][M];   // (P G^{-1}) for this thread's rows
-#pragma unroll
-        for (int r = 0; r < RPT; ++r) {
-          float prow[M];
-#pragma unroll
-          for (int b = 0; b < M; ++b) prow[b] = sf[pbuf + b * D + row0 + r];
-#pragma unroll
-          for (int aa = 0; aa < M; ++aa) {
-            float x = 0.f;
-#pragma unroll
-            for (int b = 0; b < M; ++b) x = fmaf(prow[b], Gi[b][aa], x);
-            Pt[r][aa] = -x;
+            for (int k = j; k < i; ++k) x = fmaf(-Lm[i][k], Li[k][j], x);
+            Li[i][j] = x;
           }
         }
+        if (apply) {
+          if (!guard) {
+            float Gi[M][M];
 #pragma unroll
-        for (int aa = 0; aa < M; ++aa) {
+            for (int i = 0; i < M; ++i)
 #pragma unroll
-          for (int kk = 0; kk < NCH; ++kk) {
-            const float4 pc = *reinterpret_cast<const float4*>(sf + pbuf + aa * D + colof(kk, 0));
-            const float2 p0 = f2(pc.x, pc.y), p1 = f2(pc.z, pc.w);
+              for (int j = i; j < M; ++j) {
+                float x = 0.f;
+#pragma unroll
+                for (int k = j; k < M; ++k) x = fmaf(Li[k][i] * iD[k], Li[k][j], x);
+                Gi[i][j] = x;
+                Gi[j][i] = x;
+              }
+            float Pt[RPT][M];
 #pragma unroll
             for (int r = 0; r < RPT; ++r) {
-              const float2 w = f2(Pt[r][aa], Pt[r][aa]);
-              A2[r][2 * kk] = __ffma2_rn(w, p0, A2[r][2 * kk]);
-              A2[r][2 * kk + 1] = __ffma2_rn(w, p1, A2[r][2 * kk + 1]);
+              float prow[M];
+#pragma unroll
+              for (int b = 0; b < M; ++b) prow[b] = sf[pbuf + b * D + row0 + r];
+#pragma unroll
+              for (int aa = 0; aa < M; ++aa) {
+                float x = 0.f;
+#pragma unroll
+                for (int b = 0; b < M; ++b) x = fmaf(prow[b], Gi[b][aa], x);
+                Pt[r][aa] = -x;
+              }
+            }
+#pragma unroll
+            for (int aa = 0; aa < M; ++aa) {
+#pragma unroll
+              for (int kk = 0; kk < NCH; ++kk) {
+                const float4 pc = *reinterpret_cast<const float4*>(sf + pbuf + aa * D + colof(kk, 0));
+                const float2 p0 = f2(pc.x, pc.y), p1 = f2(pc.z, pc.w);
+#pragma unroll
+                for (int r = 0; r < RPT; ++r) {
+                  const float2 w = f2(Pt[r][aa], Pt[r][aa]);
+                  A2[r][2 * kk] = __ffma2_rn(w, p0, A2[r][2 * kk]);
+                  A2[r][2 * kk + 1] = __ffma2_rn(w, p1, A2[r][2 * kk + 1]);
+                }
+              }
             }
           }
-        }
-      }
-      const float dadd = (guard ? kGuardEps : 0.f) + (nudgeA ? a.eps_n : 0.f);
-      if (dadd != 0.f) {
+          const float dadd = (guard ? kGuardEps : 0.f) + (nudgeA ? a.eps_n : 0.f);
+          if (dadd != 0.f) {
 #pragma unroll
-        for (int r = 0; r < RPT; ++r) {
-          const int row = row0 + r;
-          if (c == ((row >> 2) % LPR)) {
-            const int slot = (row / (4 * LPR)) * 4 + (row & 3);   // element index within the row piece
+            for (int r = 0; r < RPT; ++r) {
+              const int row = row0 + r;
+              if (c == ((row >> 2) % LPR)) {
+                const int slot = (row / (4 * LPR)) * 4 + (row & 3);
 #pragma unroll
-            for (int p = 0; p < NCP; ++p) {
-              if (slot == 2 * p) A2[r][p].x += dadd;
-              if (slot == 2 * p + 1) A2[r][p].y += dadd;
+                for (int p = 0; p < NCP; ++p) {
+                  if (slot == 2 * p) A2[r][p].x += dadd;
+                  if (slot == 2 * p + 1) A2[r][p].y += dadd;
+                }
+              }
             }
           }
+          if (guard) ++guard_cnt;
         }
-      }
-      // alpha for the steps this round completes: one writer per element
-      {
-        const int h = tid / D, i = tid - (tid / D) * D;
+        // alpha of the steps completed this round (zero for ghost steps); one writer per element
+        {
+          const int h = gid / D, i = gid - (gid / D) * D;
 #pragma unroll
-        for (int jj = 0; jj < (KS + 1) / 2; ++jj) {
-          const int t = 2 * jj + h;
-          if (t < KS) {
+          for (int tt = 0; tt < KS; ++tt) {
+            if ((tt & 1) != h) continue;
             float al = 0.f;
-            const int rs = recA(t);
-            if (rs != C::F_ZERO) {
-              al = sf[qbuf + t * D + i];
-              const bool last_step = (replay && rep_completes) ? true : (t == cA - 1);
-              float sadd = 0.f;
-              if (guard) sadd += kGuardEps;
-              if (nudgeA && last_step) sadd += a.eps_n;
+            const int rs = recA(tt);
+            if (apply && rs != C::F_ZERO) {
+              al = sf[qbuf + tt * D + i];
               if (!guard) {
+                // c_t = G_{<=e}^{-1} (U^T Q_t)_{<=e}: forward and back substitution
+                const int e = (tt + 1) * R - 1;
+                float y[M];
 #pragma unroll
-                for (int tt = 0; tt < KS; ++tt) {
-                  if (tt == 2 * jj || tt == 2 * jj + 1) {
-                    if (t == tt) {
+                for (int aa = 0; aa < M; ++aa) {
+                  float x = 0.f;
+                  if (aa <= e) {
 #pragma unroll
-                      for (int b = 0; b < M; ++b)
-                        if (b <= (tt + 1) * R - 1) al = fmaf(-sf[pbuf + b * D + i], cf[tt][b], al);
-                    }
+                    for (int b = 0; b <= aa; ++b) x = fmaf(Li[aa][b], res[C::NJG + R * tt * (tt + 1) / 2 + b], x);
+                  }
+                  y[aa] = x * iD[aa];
+                }
+#pragma unroll
+                for (int aa = 0; aa < M; ++aa) {
+                  if (aa <= e) {
+                    float cfa = 0.f;
+#pragma unroll
+                    for (int b = aa; b < M; ++b)
+                      if (b <= e) cfa = fmaf(Li[b][aa], y[b], cfa);
+                    al = fmaf(-sf[pbuf + aa * D + i], cfa, al);
                   }
                 }
               }
+              const bool last = replay ? rep_completes : (tt == cA - 1);
+              const float sadd = (guard ? kGuardEps : 0.f) + ((nudgeA && last) ? a.eps_n : 0.f);
               if (sadd != 0.f) al = fmaf(sadd, sf[rs + C::OFF_S + i], al);
             }
-            sf[abuf + t * D + i] = al;
+            sf[abuf + tt * D + i] = al;
           }
         }
+        if (gid == 0) {
+          int* inf = info + (rnd & 1) * 8;
+          inf[0] = apply ? cA : 0;
+          inf[1] = recA(0);
+          inf[2] = (int)(gA0 & 0x7fffffff);
+          inf[3] = (int)(gA0 >> 31);
+          inf[4] = 0;
+        }
+        bar_arrive(BAR_FULL0 + (rnd & 1), NT);
+        // ---------------- bookkeeping
+        if (replay && apply) {
+          ++rep_col;
+          if (rep_col == rep_total) {
+            replay = false;
+            pos = rep_pos + rep_total / R;
+          }
+        } else if (!replay) {
+          pos += cA;
+        }
       }
-      if (guard) ++guard_cnt;
-    } else {
-      // nothing applied: no alpha is produced this round
-#pragma unroll
-      for (int jj = 0; jj < (KS + 1) / 2; ++jj) {
-        const int t = 2 * jj + tid / D;
-        if (t < KS) sf[abuf + t * D + (tid - (tid / D) * D)] = 0.f;
-      }
+      par ^= 1;
+      ++rnd;
     }
-
-    // ---- S side: the steps completed in the previous round
-    if (cS > 0) {
-      float ws = 0.f;
+    // rnd rounds were published, the last one the end marker.  S arrived on
+    // EMPTY after each real round 0 .. rnd-2; the syncs at the top of the loop
+    // matched rounds 0 .. rnd-3, so round rnd-2 is still to be matched.
+    if (rnd >= 2) bar_sync(BAR_EMPTY0 + ((rnd - 2) & 1), NT);
+    if (!(flags & kStatusTimeout)) {
 #pragma unroll
-      for (int w = 0; w < NW; ++w) ws += sf[C::F_WP + par * NW + w];
-      const float norm0 = sigma * sqrtf(ws);
-      float bound = norm0;
-      float an[KS];
+      for (int r = 0; r < RPT; ++r)
 #pragma unroll
-      for (int t = 0; t < KS; ++t) {
-        an[t] = res[C::NJG + C::NJH + C::NJQ + t];
-        if (t < cS) bound = fmaf(sf[recS(t) + C::OFF_SC + 1], sqrtf(an[t]), bound);
-      }
-      if (!isfinite(norm0) || !isfinite(bound)) flags |= kStatusNonfinite;
-      // inverse scale before each step (1/sigma_{t-1}) and the scale after it (sigma_t)
-      float isg[KS], sg[KS];
-      const bool exact = !(bound <= tau * (1.f - 0x1p-12f));
-      if (!exact) {
-        const float is = __frcp_rn(sigma);
-#pragma unroll
-        for (int t = 0; t < KS; ++t) { isg[t] = is; sg[t] = sigma; }
-      } else {
-        // extra reduction: v_t^T S_0 alpha_t, alpha Gram, v Gram
-        float mv[C::NMINI];
-#pragma unroll
-        for (int k = 0; k < C::NMINI; ++k) mv[k] = 0.f;
-        float vrow[KS][RPT];
-#pragma unroll
-        for (int t = 0; t < KS; ++t)
-#pragma unroll
-          for (int r = 0; r < RPT; ++r) vrow[t][r] = sf[recS(t) + C::OFF_V + row0 + r];
-#pragma unroll
-        for (int t = 0; t < KS; ++t) {
-          float x = 0.f;
-#pragma unroll
-          for (int kk = 0; kk < NCH; ++kk) {
-            const float4 al = *reinterpret_cast<const float4*>(sf + abuf_prev + t * D + colof(kk, 0));
-#pragma unroll
-            for (int r = 0; r < RPT; ++r) {
-              float y = S2[r][2 * kk].x * al.x;
-              y = fmaf(S2[r][2 * kk].y, al.y, y);
-              y = fmaf(S2[r][2 * kk + 1].x, al.z, y);
-              y = fmaf(S2[r][2 * kk + 1].y, al.w, y);
-              x = fmaf(vrow[t][r], y, x);
-            }
-          }
-          mv[t] = x;
+        for (int kk = 0; kk < NCH; ++kk) {
+          *reinterpret_cast<float4*>(gA + (row0 + r) * D + colof(kk, 0)) =
+              make_float4(A2[r][2 * kk].x, A2[r][2 * kk].y, A2[r][2 * kk + 1].x, A2[r][2 * kk + 1].y);
         }
-        int k = KS;
+      if (gid < D) gn[gid] = n_i;
+    } else if (gid == 0) {
+      for (int j = loaded + 1; j < ntiles && j <= loaded + NSTAGE; ++j)
+        (void)mbar_wait_bounded(&bars[j % NSTAGE], (uint32_t)((j / NSTAGE) & 1));
+    }
+    if (gid == 0) {
+      if (guard_cnt) atomicAdd(&a.status->guard_count, guard_cnt);
+      if (replay_cnt) atomicAdd(&a.status->chunk_fallbacks, replay_cnt);
+    }
+  } else {
+    // =====================================================================
+    // S group (one round behind)
+    // =====================================================================
+    float2 S2[RPT][NCP];
 #pragma unroll
-        for (int t = 0; t < KS; ++t)
+    for (int r = 0; r < RPT; ++r)
 #pragma unroll
-          for (int tp = 0; tp <= t; ++tp) {
-            float xa = 0.f, xv = 0.f;
-            if (g == 0) {   // row group 0 covers every column once
+      for (int kk = 0; kk < NCH; ++kk) {
+        const float4 sv = *reinterpret_cast<const float4*>(gS + (row0 + r) * D + colof(kk, 0));
+        S2[r][2 * kk] = f2(sv.x, sv.y);
+        S2[r][2 * kk + 1] = f2(sv.z, sv.w);
+      }
+    float sigma = 1.f;
+    unsigned long long renorm_cnt = 0;
+    int par = 0;
+    bool timed_out = false;
+    for (int rnd = 0;; ++rnd) {
+      bar_sync(BAR_FULL0 + (rnd & 1), NT);
+      const int* inf = info + (rnd & 1) * 8;
+      const int cS = inf[0], baseS = inf[1];
+      const long long gS0 = (long long)inf[2] | ((long long)inf[3] << 31);
+      if (inf[4]) { timed_out = (*flag != 0); break; }
+      if (cS > 0) {
+        auto recS = [&](int t) -> int { return (t < cS) ? baseS + t * REC : C::F_ZERO; };
+        const int ybuf = C::F_Y + par * KS * D;
+        const int abuf = C::F_AL + (rnd & 1) * KS * D;
+        // ---------------- phase P: Y_t = S_reg phi(q_t), ||S_reg||^2
+        {
+          float ns;
+          float vals[RPT * C::NVS];
+          {
+            float2 acc[RPT][C::NVS];
 #pragma unroll
-              for (int kk = 0; kk < NCH; ++kk)
+            for (int r = 0; r < RPT; ++r)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const int col = colof(kk, e);
-                  xa = fmaf(sf[abuf_prev + t * D + col], sf[abuf_prev + tp * D + col], xa);
+              for (int v = 0; v < C::NVS; ++v) acc[r][v] = f2(0.f, 0.f);
+#pragma unroll
+            for (int v = 0; v < KS; ++v) {
+              const int base = recS(v) + C::OFF_Q;
+#pragma unroll
+              for (int kk = 0; kk < NCH; ++kk) {
+                const float4 x = *reinterpret_cast<const float4*>(sf + base + colof(kk, 0));
+                const float2 x0 = f2(x.x, x.y), x1 = f2(x.z, x.w);
+#pragma unroll
+                for (int r = 0; r < RPT; ++r) {
+                  acc[r][v] = __ffma2_rn(S2[r][2 * kk], x0, acc[r][v]);
+                  acc[r][v] = __ffma2_rn(S2[r][2 * kk + 1], x1, acc[r][v]);
                 }
+              }
             }
-            if (c == 0) {   // lane 0 of every row group covers its rows once
+            float2 n2 = f2(0.f, 0.f);
 #pragma unroll
-              for (int r = 0; r < RPT; ++r) xv = fmaf(vrow[t][r], vrow[tp][r], xv);
-            }
-            mv[k] = xa;
-            mv[k + 1] = xv;
-            k += 2;
+            for (int r = 0; r < RPT; ++r)
+#pragma unroll
+              for (int p = 0; p < NCP; ++p) n2 = __ffma2_rn(S2[r][p], S2[r][p], n2);
+            ns = n2.x + n2.y;
+#pragma unroll
+            for (int r = 0; r < RPT; ++r)
+#pragma unroll
+              for (int v = 0; v < C::NVS; ++v) vals[r * C::NVS + v] = acc[r][v].x + acc[r][v].y;
+          }
+          reduce_scatter<RPT * C::NVS, LPR / 2>(vals, c);
+#pragma unroll
+          for (int i = 0; i < C::KVS; ++i) {
+            const int slot = c * C::KVS + i;
+            const int r = slot / C::NVS, v = slot - r * C::NVS;
+            if (v < KS) sf[ybuf + v * D + row0 + r] = vals[i];
           }
 #pragma unroll
-        for (int k2 = 0; k2 < C::NMINI; ++k2) {
-          float x = mv[k2];
-#pragma unroll
-          for (int m = 16; m >= 1; m >>= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
-          mv[k2] = x;
+          for (int m = 16; m >= 1; m >>= 1) ns += __shfl_xor_sync(0xffffffffu, ns, m);
+          if (lane == 0) sf[C::F_WP + par * GW + gw] = ns;
         }
-        if (lane == 0) {
+        bar_sync(BAR_S, GT);
+        // ---------------- phase G: alpha_t' . phi(q_t) (t' <= t), |alpha_t|^2
+        {
+          auto jobs = [&](auto wtag) {
+            constexpr int W = decltype(wtag)::value;
+            float jv[C::NSS];
 #pragma unroll
-          for (int k2 = 0; k2 < C::NMINI; ++k2) sf[C::F_MINI + warp * 32 + k2] = mv[k2];
-        }
-        __syncthreads();  // ------------------------------------------------ BAR3 (rare)
-        float tot[C::NMINI];
+            for (int s = 0; s < C::NSS; ++s) {
+              const int j = s * GW + W;
+              float acc = 0.f;
+              if (j < C::NJS) {
+                int oa, ob;
+                if (j < C::NJQ) {
+                  int t = 0;
 #pragma unroll
-        for (int k2 = 0; k2 < C::NMINI; ++k2) {
-          float x = 0.f;
+                  for (int tt = 1; tt < KS; ++tt) t += (j >= tt * (tt + 1) / 2) ? 1 : 0;
+                  oa = abuf + (j - t * (t + 1) / 2) * D;
+                  ob = recS(t) + C::OFF_Q;
+                } else {
+                  oa = abuf + (j - C::NJQ) * D;
+                  ob = oa;
+                }
+                if (D >= 32) {
 #pragma unroll
-          for (int w = 0; w < NW; ++w) x += sf[C::F_MINI + w * 32 + k2];
-          tot[k2] = x;
-        }
-        // sequential decisions on ||S_reg_t||^2 (S_reg unscaled, scale sigma before step t)
-        float nreg2 = ws;
-        float sgc = sigma;
-#pragma unroll
-        for (int t = 0; t < KS; ++t) {
-          isg[t] = __frcp_rn(sgc);
-          if (t < cS) {
-            // v_t^T S_reg_{t-1} alpha_t = v_t^T S_reg_0 alpha_t + sum_{t'<t} (v_t.v_t')(alpha_t'.alpha_t)/sigma_{t'-1}
-            float cross = tot[t];
-            int kb = KS + t * (t + 1);   // start of (t, 0) pair in the mini list
-#pragma unroll
-            for (int tp = 0; tp < t; ++tp) cross = fmaf(tot[kb + 2 * tp + 1] * tot[kb + 2 * tp], isg[tp], cross);
-            const float aa = tot[kb + 2 * t], vv = tot[kb + 2 * t + 1];
-            nreg2 = fmaf(2.f * isg[t], cross, nreg2);
-            nreg2 = fmaf(vv * aa, isg[t] * isg[t], nreg2);
-            const float npre = sgc * sqrtf(fmaxf(nreg2, 0.f));
-            if (npre > tau) {
-              sgc *= tau / npre;
-              ++renorm_cnt;
+                  for (int e = 0; e < D / 32; ++e)
+                    acc = fmaf(sf[oa + lane + 32 * e], sf[ob + lane + 32 * e], acc);
+                } else if (lane < D) {
+                  acc = sf[oa + lane] * sf[ob + lane];
+                }
+              }
+              jv[s] = acc;
             }
-            if (!isfinite(npre)) flags |= kStatusNonfinite;
+            reduce_scatter<C::NSS, 16>(jv, lane);
+            float x = jv[0];
+#pragma unroll
+            for (int m = 32 / C::NSS / 2; m >= 1; m >>= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
+            constexpr int SH = 5 - log2i(C::NSS);
+            const int j = (lane >> SH) * GW + W;
+            if ((lane & ((1 << SH) - 1)) == 0 && j < C::NJS) sf[C::F_RS + j] = x;
+          };
+          switch (gw) {
+            case 0: jobs(std::integral_constant<int, 0>{}); break;
+            case 1: if constexpr (GW > 1) jobs(std::integral_constant<int, 1>{}); break;
+            case 2: if constexpr (GW > 2) jobs(std::integral_constant<int, 2>{}); break;
+            case 3: if constexpr (GW > 3) jobs(std::integral_constant<int, 3>{}); break;
+            case 4: if constexpr (GW > 4) jobs(std::integral_constant<int, 4>{}); break;
+            case 5: if constexpr (GW > 5) jobs(std::integral_constant<int, 5>{}); break;
+            case 6: if constexpr (GW > 6) jobs(std::integral_constant<int, 6>{}); break;
+            case 7: if constexpr (GW > 7) jobs(std::integral_constant<int, 7>{}); break;
+            default: break;
           }
-          sg[t] = sgc;
         }
-      }
-      // outputs o_t = sigma_t (Y_t + sum_{t'<=t} v_t' aq_{t,t'} / sigma_{t'-1}) / den_t
-      {
-        const int h = tid / D, i = tid - (tid / D) * D;
+        bar_sync(BAR_S, GT);
+        // ---------------- phase U: renormalisation, outputs, S update
+        {
+          float rs_[C::NJS];
 #pragma unroll
-        for (int jj = 0; jj < (KS + 1) / 2; ++jj) {
+          for (int j = 0; j < C::NJS; ++j) rs_[j] = sf[C::F_RS + j];
+          float ws = 0.f;
 #pragma unroll
-          for (int tt = 2 * jj; tt < 2 * jj + 2 && tt < KS; ++tt) {
-            if (tt == 2 * jj + h && tt < cS) {
-              const int rs = recS(tt);
+          for (int w = 0; w < GW; ++w) ws += sf[C::F_WP + par * GW + w];
+          const float norm0 = sigma * sqrtf(ws);
+          float bound = norm0;
+#pragma unroll
+          for (int t = 0; t < KS; ++t)
+            if (t < cS) bound = fmaf(sf[recS(t) + C::OFF_SC + 1], sqrtf(rs_[C::NJQ + t]), bound);
+          if (!isfinite(bound)) flags |= kStatusNonfinite;
+          float isg[KS], sg[KS];   // 1/sigma before step t, sigma after it
+          const bool exact = !(bound <= a.tau * (1.f - 0x1p-12f));
+          if (!exact) {
+            const float is = __frcp_rn(sigma);
+#pragma unroll
+            for (int t = 0; t < KS; ++t) { isg[t] = is; sg[t] = sigma; }
+          } else {
+            float mv[C::NMINI];
+            float vrow[KS][RPT];
+#pragma unroll
+            for (int t = 0; t < KS; ++t)
+#pragma unroll
+              for (int r = 0; r < RPT; ++r) vrow[t][r] = sf[recS(t) + C::OFF_V + row0 + r];
+#pragma unroll
+            for (int t = 0; t < KS; ++t) {   // v_t^T S_reg alpha_t
+              float x = 0.f;
+#pragma unroll
+              for (int kk = 0; kk < NCH; ++kk) {
+                const float4 al = *reinterpret_cast<const float4*>(sf + abuf + t * D + colof(kk, 0));
+#pragma unroll
+                for (int r = 0; r < RPT; ++r) {
+                  float y = S2[r][2 * kk].x * al.x;
+                  y = fmaf(S2[r][2 * kk].y, al.y, y);
+                  y = fmaf(S2[r][2 * kk + 1].x, al.z, y);
+                  y = fmaf(S2[r][2 * kk + 1].y, al.w, y);
+                  x = fmaf(vrow[t][r], y, x);
+                }
+              }
+              mv[t] = x;
+            }
+#pragma unroll
+            for (int t = 0; t < KS; ++t)
+#pragma unroll
+              for (int tp = 0; tp <= t; ++tp) {
+                float xa = 0.f, xv = 0.f;
+                if (g == 0) {   // row group 0 covers every column once
+#pragma unroll
+                  for (int kk = 0; kk < NCH; ++kk)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                      const int col = colof(kk, e);
+                      xa = fmaf(sf[abuf + t * D + col], sf[abuf + tp * D + col], xa);
+                    }
+                }
+                if (c == 0) {   // lane 0 of each row group covers its rows once
+#pragma unroll
+                  for (int r = 0; r < RPT; ++r) xv = fmaf(vrow[t][r], vrow[tp][r], xv);
+                }
+                mv[KS + t * (t + 1) + 2 * tp] = xa;
+                mv[KS + t * (t + 1) + 2 * tp + 1] = xv;
+              }
+#pragma unroll
+            for (int k2 = 0; k2 < C::NMINI; ++k2) {
+              float x = mv[k2];
+#pragma unroll
+              for (int m = 16; m >= 1; m >>= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
+              mv[k2] = x;
+            }
+            if (lane == 0) {
+#pragma unroll
+              for (int k2 = 0; k2 < C::NMINI; ++k2) sf[C::F_MINI + gw * C::MSTR + k2] = mv[k2];
+            }
+            bar_sync(BAR_S, GT);
+            float tot[C::NMINI];
+#pragma unroll
+            for (int k2 = 0; k2 < C::NMINI; ++k2) {
+              float x = 0.f;
+#pragma unroll
+              for (int w = 0; w < GW; ++w) x += sf[C::F_MINI + w * C::MSTR + k2];
+              tot[k2] = x;
+            }
+            float nreg2 = ws, sgc = sigma;
+#pragma unroll
+            for (int t = 0; t < KS; ++t) {
+              isg[t] = __frcp_rn(sgc);
+              if (t < cS) {
+                float cross = tot[t];
+#pragma unroll
+                for (int tp = 0; tp < t; ++tp)
+                  cross = fmaf(tot[KS + t * (t + 1) + 2 * tp + 1] * tot[KS + t * (t + 1) + 2 * tp], isg[tp], cross);
+                const float aa = tot[KS + t * (t + 1) + 2 * t], vv = tot[KS + t * (t + 1) + 2 * t + 1];
+                nreg2 = fmaf(2.f * isg[t], cross, nreg2);
+                nreg2 = fmaf(vv * aa, isg[t] * isg[t], nreg2);
+                const float npre = sgc * sqrtf(fmaxf(nreg2, 0.f));
+                if (npre > a.tau) {
+                  sgc *= a.tau / npre;
+                  ++renorm_cnt;
+                }
+                if (!isfinite(npre)) flags |= kStatusNonfinite;
+              }
+              sg[t] = sgc;
+            }
+          }
+          // outputs: o_t = sigma_t (Y_t + sum_{t'<=t} v_t' aq_{t,t'} / sigma_{t'-1}) / den_t
+          {
+            const int h = gid / D, i = gid - (gid / D) * D;
+#pragma unroll
+            for (int tt = 0; tt < KS; ++tt) {
+              if ((tt & 1) != h || tt >= cS) continue;
               float x = sf[ybuf + tt * D + i];
 #pragma unroll
-              for (int tp = 0; tp <= tt; ++tp) {
-                const float aq = res[C::NJG + C::NJH + tt * (tt + 1) / 2 + tp];
-                x = fmaf(sf[recS(tp) + C::OFF_V + i] * aq, isg[tp], x);
-              }
-              const float o = sg[tt] * x / sf[rs + C::OFF_SC];
+              for (int tp = 0; tp <= tt; ++tp)
+                x = fmaf(sf[recS(tp) + C::OFF_V + i] * rs_[tt * (tt + 1) / 2 + tp], isg[tp], x);
+              const float o = sg[tt] * x * sf[recS(tt) + C::OFF_SC];
               if (!isfinite(o)) flags |= kStatusNonfinite;
               go[(gS0 + tt) * D + i] = from_f32<TIO>(o);
             }
           }
-        }
-      }
-      // S_reg += sum_t v_t alpha_t^T / sigma_{t-1}
+          // S_reg += sum_t v_t alpha_t^T / sigma_{t-1}
 #pragma unroll
-      for (int t = 0; t < KS; ++t) {
-        if (t < cS) {
-          float vr[RPT];
+          for (int t = 0; t < KS; ++t) {
+            if (t < cS) {
+              float vr[RPT];
 #pragma unroll
-          for (int r = 0; r < RPT; ++r) vr[r] = sf[recS(t) + C::OFF_V + row0 + r] * isg[t];
+              for (int r = 0; r < RPT; ++r) vr[r] = sf[recS(t) + C::OFF_V + row0 + r] * isg[t];
 #pragma unroll
-          for (int kk = 0; kk < NCH; ++kk) {
-            const float4 al = *reinterpret_cast<const float4*>(sf + abuf_prev + t * D + colof(kk, 0));
-            const float2 a0 = f2(al.x, al.y), a1 = f2(al.z, al.w);
+              for (int kk = 0; kk < NCH; ++kk) {
+                const float4 al = *reinterpret_cast<const float4*>(sf + abuf + t * D + colof(kk, 0));
+                const float2 a0 = f2(al.x, al.y), a1 = f2(al.z, al.w);
 #pragma unroll
-            for (int r = 0; r < RPT; ++r) {
-              const float2 w = f2(vr[r], vr[r]);
-              S2[r][2 * kk] = __ffma2_rn(w, a0, S2[r][2 * kk]);
-              S2[r][2 * kk + 1] = __ffma2_rn(w, a1, S2[r][2 * kk + 1]);
+                for (int r = 0; r < RPT; ++r) {
+                  const float2 w = f2(vr[r], vr[r]);
+                  S2[r][2 * kk] = __ffma2_rn(w, a0, S2[r][2 * kk]);
+                  S2[r][2 * kk + 1] = __ffma2_rn(w, a1, S2[r][2 * kk + 1]);
+                }
+              }
             }
+          }
+          sigma = sg[KS - 1];
+          if (sigma < 0x1p-16f) {
+#pragma unroll
+            for (int r = 0; r < RPT; ++r)
+#pragma unroll
+              for (int p = 0; p < NCP; ++p) { S2[r][p].x *= sigma; S2[r][p].y *= sigma; }
+            sigma = 1.f;
           }
         }
       }
-      sigma = sg[KS - 1];
-      if (sigma < 0x1p-16f) {   // fold the scale back into S_reg
+      bar_arrive(BAR_EMPTY0 + (rnd & 1), NT);
+      par ^= 1;
+    }
+    if (!timed_out) {
 #pragma unroll
-        for (int r = 0; r < RPT; ++r)
+      for (int r = 0; r < RPT; ++r)
 #pragma unroll
-          for (int p = 0; p < NCP; ++p) { S2[r][p].x *= sigma; S2[r][p].y *= sigma; }
-        sigma = 1.f;
-      }
-    }
-
-    // ================= advance
-    if (tid == 0) {
-      if (haveA && !isfinite(Dv[0])) flags |= kStatusNonfinite;
-    }
-    if (apply) {
-      cS = cA;
-      baseS = recA(0);
-      gS0 = gA0;
-    } else {
-      cS = 0;
-    }
-    if (haveA) {
-      if (replay && apply) {
-        ++rep_col;
-        if (rep_col == rep_total) {
-          replay = false;
-          pos = rep_pos + rep_total / R;
+        for (int kk = 0; kk < NCH; ++kk) {
+          *reinterpret_cast<float4*>(gS + (row0 + r) * D + colof(kk, 0)) =
+              make_float4(sigma * S2[r][2 * kk].x, sigma * S2[r][2 * kk].y, sigma * S2[r][2 * kk + 1].x,
+                          sigma * S2[r][2 * kk + 1].y);
         }
-      } else if (!replay) {
-        pos += cA;
-      }
     }
-    par ^= 1;
+    if (gid == 0 && renorm_cnt) atomicAdd(&a.status->renorm_count, renorm_cnt);
   }
-
-  if (timed_out) {
-    if (tid == 0) {
-      for (int j = loaded + 1; j < ntiles && j <= loaded + NSTAGE; ++j)
-        (void)mbar_wait_bounded(&bars[j % NSTAGE], (uint32_t)((j / NSTAGE) & 1));
-      atomicOr(&a.status->flags, kStatusTimeout);
-    }
-    return;
-  }
-
-  // ---- state out
-#pragma unroll
-  for (int r = 0; r < RPT; ++r) {
-#pragma unroll
-    for (int kk = 0; kk < NCH; ++kk) {
-      const float4 av = make_float4(A2[r][2 * kk].x, A2[r][2 * kk].y, A2[r][2 * kk + 1].x, A2[r][2 * kk + 1].y);
-      const float4 sv = make_float4(sigma * S2[r][2 * kk].x, sigma * S2[r][2 * kk].y, sigma * S2[r][2 * kk + 1].x,
-                                    sigma * S2[r][2 * kk + 1].y);
-      *reinterpret_cast<float4*>(gA + (row0 + r) * D + colof(kk, 0)) = av;
-      *reinterpret_cast<float4*>(gS + (row0 + r) * D + colof(kk, 0)) = sv;
-    }
-  }
-  if (tid < D) gn[tid] = n_i;
-  if (flags) atomicOr(&a.status->flags, flags);   // any thread may have seen a non-finite value
-  if (tid == 0) {
-    if (guard_cnt) atomicAdd(&a.status->guard_count, guard_cnt);
-    if (renorm_cnt) atomicAdd(&a.status->renorm_count, renorm_cnt);
-    if (replay_cnt) atomicAdd(&a.status->chunk_fallbacks, replay_cnt);
-  }
+  if (flags) atomicOr(&a.status->flags, flags);
 }
 
 template <int D, int R, int KS, typename TIO>
