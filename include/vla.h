@@ -121,12 +121,64 @@ vla_err_t vla_status(vla_handle_t h, void* stream, vla_status_t* out);
 
 /* Message of the last failed call on this handle ("" if none).  The string is
  * owned by the handle and stays valid until the next call on it.  With h ==
- * NULL it returns the message of the last failed vla_create on this thread. */
+ * NULL it returns the message of the last failed vla_create or
+ * vla_scan_fwd_noalloc on this thread. */
 const char* vla_last_error(vla_handle_t h);
 
 /* Free the handle and its status block (synchronises its device first).
  * h == NULL is a no-op that returns VLA_OK. */
 vla_err_t vla_destroy(vla_handle_t h);
+
+/* ------------------------------------------------------------------------
+ * Scan without any allocation.  The pages have no counterpart to this entry
+ * point: it exists for callers that may not allocate device memory.  Typical
+ * ones run inside a framework or server whose allocator owns the device's
+ * memory (a caching allocator, an arena sized at start-up) and must not call
+ * cudaMalloc behind its back: cudaMalloc synchronises the device and takes
+ * memory the owner neither tracks nor can reuse.  Others keep no state between
+ * calls and so have no place to keep a handle, whose creation allocates.
+ *
+ * It runs the same sequential scan as vla_scan_fwd (same arguments, layouts and
+ * results) on the caller's current device, with d == dv == 64 and r in {1, 4}.
+ * Its scratch -- one status record per (b, h) pair -- is a static array inside
+ * the library of VLA_NOALLOC_MAX_PAIRS records (256 KB), which every GPU that
+ * loads the library holds until the process exits.  Nothing is allocated: no
+ * cudaMalloc, cudaFree or allocating library routine is called.
+ *
+ *   pair_status  NULL, or a caller-owned array of B*H records (device memory or
+ *                host memory).  Record b*H+h receives that pair's status for
+ *                this call (flags as in VLA_STATUS_*, guard, renormalisation and
+ *                replay counts).  It is written with cudaMemcpyAsync on `stream`
+ *                and is valid once the stream has reached that point.
+ *
+ * - Each call clears the records it uses before the scan, so a record never
+ *   carries counts from an earlier call.
+ * - All calls share the one array: calls that overlap on the GPU (different
+ *   streams, or different host threads, without ordering between them) race on
+ *   it.  Order such calls, for example on one stream.
+ * - The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) and keeps it for later calls; make that first call
+ *   before any stream capture on that device.
+ *
+ * Errors (returned before any launch): INVALID_ARG as for vla_scan_fwd, and when
+ * B*H exceeds VLA_NOALLOC_MAX_PAIRS; UNSUPPORTED for shapes other than
+ * d == dv == 64, r in {1, 4}; CUDA when a runtime call fails.  The message is
+ * available from vla_last_error(NULL) on the calling thread. */
+#define VLA_NOALLOC_MAX_PAIRS 16384
+
+typedef struct {
+  unsigned int flags;             /* VLA_STATUS_* */
+  unsigned int guard_count;
+  unsigned int renorm_count;
+  unsigned int chunk_fallbacks;   /* chunks replayed one direction at a time */
+} vla_pair_status_t;
+
+vla_err_t vla_scan_fwd_noalloc(const void* q, const void* k, const void* v, const void* u,
+                               float* A, float* S, float* n, void* o,
+                               int B, int H, long long T, int d, int dv, int r,
+                               int P, float eps_n, float tau, long long t0,
+                               vla_dtype_t io_dtype, vla_pair_status_t* pair_status,
+                               void* stream);
 
 #ifdef __cplusplus
 }

@@ -37,6 +37,11 @@ class VlaStatus(ctypes.Structure):
                 ("chunk_fallbacks", ctypes.c_ulonglong)]
 
 
+class VlaPairStatus(ctypes.Structure):
+    _fields_ = [("flags", ctypes.c_uint), ("guard_count", ctypes.c_uint),
+                ("renorm_count", ctypes.c_uint), ("chunk_fallbacks", ctypes.c_uint)]
+
+
 class VlaError(RuntimeError):
     def __init__(self, code: int, msg: str):
         super().__init__(f"{ERR_NAMES.get(code, code)}: {msg}")
@@ -73,6 +78,9 @@ def load_library():
         lib.vla_last_error.restype = ctypes.c_char_p
         lib.vla_destroy.argtypes = [vp]
         lib.vla_destroy.restype = ci
+        lib.vla_scan_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, cll, ci, ci, ci,
+                                             ci, cf, cf, cll, ci, vp, vp]
+        lib.vla_scan_fwd_noalloc.restype = ci
         _lib = lib
         return lib
 

@@ -22,6 +22,12 @@ cudaError_t launch_seq(int d, int r, bool bf16, const ScanArgs& a, cudaStream_t 
 }
 }  // namespace vla
 
+namespace {
+thread_local std::string g_create_error;
+}
+
+void vla::set_thread_error(const char* msg) { g_create_error = msg ? msg : ""; }
+
 struct vla_handle_s {
   int device = 0;
   vla::DevStatus* status = nullptr;
@@ -29,8 +35,6 @@ struct vla_handle_s {
 };
 
 namespace {
-
-thread_local std::string g_create_error;
 
 vla_err_t fail(vla_handle_t h, vla_err_t code, const std::string& msg) {
   if (h) h->last_error = msg; else g_create_error = msg;

@@ -16,6 +16,14 @@ struct DevStatus {
   unsigned long long chunk_fallbacks;
 };
 
+// Per-pair status record (used by the entry point that allocates nothing).
+struct PairStatus {
+  unsigned int flags;
+  unsigned int guard_count;
+  unsigned int renorm_count;
+  unsigned int chunk_fallbacks;
+};
+
 constexpr unsigned int kStatusNonfinite = 1u;
 constexpr unsigned int kStatusTimeout = 2u;
 
@@ -36,14 +44,17 @@ struct ScanArgs {
   float eps_n;
   float tau;
   int pairs;
-  DevStatus* status;
+  DevStatus* status;          // accumulated status (handle entry point)
+  PairStatus* pair_status;    // per-pair status (no-allocation entry point)
 };
 
-// Host-side launchers, one per built (d, r, dtype); defined in vla_seq_d*.cu.
-// Each returns cudaSuccess or the launch error.
+// Host-side launchers; each returns cudaSuccess or the launch error.
 cudaError_t launch_seq(int d, int r, bool bf16, const ScanArgs& a, cudaStream_t s, bool* built);
 cudaError_t launch_chunked(int d, int r, bool bf16, int chunk, const ScanArgs& a, cudaStream_t s,
                            bool* built);
+
+// Message returned by vla_last_error(NULL) on the calling thread.
+void set_thread_error(const char* msg);
 
 // --------------------------------------------------------------------------
 // device helpers (inline PTX: mbarrier, bulk asynchronous copies, timers)

@@ -169,7 +169,9 @@ __device__ __forceinline__ void reduce_scatter(float (&v)[N], int lanebits) {
 
 }  // namespace blk
 
-template <int D, int R, int KS, typename TIO>
+// PS = false: status accumulates into a.status (one block per call);
+// PS = true:  into a.pair_status[pair] (one record per pair).
+template <int D, int R, int KS, typename TIO, bool PS = false>
 __global__ void __launch_bounds__(blk::Geom<D>::NT, 1) seq_block_kernel(ScanArgs a) {
   using namespace blk;
   using Gm = Geom<D>;
@@ -677,8 +679,13 @@ __global__ void __launch_bounds__(blk::Geom<D>::NT, 1) seq_block_kernel(ScanArgs
         (void)mbar_wait_bounded(&bars[j % NSTAGE], (uint32_t)((j / NSTAGE) & 1));
     }
     if (gid == 0) {
-      if (guard_cnt) atomicAdd(&a.status->guard_count, guard_cnt);
-      if (replay_cnt) atomicAdd(&a.status->chunk_fallbacks, replay_cnt);
+      if constexpr (PS) {
+        if (guard_cnt) atomicAdd(&a.pair_status[pair].guard_count, (unsigned int)guard_cnt);
+        if (replay_cnt) atomicAdd(&a.pair_status[pair].chunk_fallbacks, (unsigned int)replay_cnt);
+      } else {
+        if (guard_cnt) atomicAdd(&a.status->guard_count, guard_cnt);
+        if (replay_cnt) atomicAdd(&a.status->chunk_fallbacks, replay_cnt);
+      }
     }
   } else {
     // =====================================================================
@@ -971,15 +978,21 @@ __global__ void __launch_bounds__(blk::Geom<D>::NT, 1) seq_block_kernel(ScanArgs
                           sigma * S2[r][2 * kk + 1].y);
         }
     }
-    if (gid == 0 && renorm_cnt) atomicAdd(&a.status->renorm_count, renorm_cnt);
+    if (gid == 0 && renorm_cnt) {
+      if constexpr (PS) atomicAdd(&a.pair_status[pair].renorm_count, (unsigned int)renorm_cnt);
+      else atomicAdd(&a.status->renorm_count, renorm_cnt);
+    }
   }
-  if (flags) atomicOr(&a.status->flags, flags);
+  if (flags) {
+    if constexpr (PS) atomicOr(&a.pair_status[pair].flags, flags);
+    else atomicOr(&a.status->flags, flags);
+  }
 }
 
-template <int D, int R, int KS, typename TIO>
+template <int D, int R, int KS, typename TIO, bool PS = false>
 cudaError_t launch_seq_block_t(const ScanArgs& a, cudaStream_t s) {
   using C = blk::Cfg<D, R, KS, TIO>;
-  auto kern = seq_block_kernel<D, R, KS, TIO>;
+  auto kern = seq_block_kernel<D, R, KS, TIO, PS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::bytes);
   if (e != cudaSuccess) return e;
   kern<<<a.pairs, blk::Geom<D>::NT, C::bytes, s>>>(a);
