@@ -134,7 +134,7 @@ class Handle:
                     renorm_count=st.renorm_count, chunk_fallbacks=st.chunk_fallbacks)
 
     def scan_fwd(self, q, k, v, u, A, S, n, o=None, *, P: int, eps_n: float, tau: float, t0: int = 0,
-                 mode: str = "sequential", chunk: int = 16, stream=None):
+                 mode: str = "sequential", chunk: int = 0, stream=None):
         if q.dim() != 4:
             raise ValueError("q must be [B, H, T, d]")
         B, H, T, d = q.shape
@@ -182,7 +182,7 @@ def default_handle(device=None) -> Handle:
 
 
 def scan_fwd(q, k, v, u, A, S, n, o=None, *, P: int, eps_n: float, tau: float, t0: int = 0,
-             mode: str = "sequential", chunk: int = 16, stream=None, handle: Handle | None = None):
+             mode: str = "sequential", chunk: int = 0, stream=None, handle: Handle | None = None):
     """Run the scan on q's device (see the module docstring); returns o."""
     h = handle if handle is not None else default_handle(q.device)
     return h.scan_fwd(q, k, v, u, A, S, n, o, P=P, eps_n=eps_n, tau=tau, t0=t0, mode=mode, chunk=chunk,

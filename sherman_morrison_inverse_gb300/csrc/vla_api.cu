@@ -139,7 +139,7 @@ vla_err_t vla_scan_fwd(vla_handle_t h, const void* q, const void* k, const void*
     char buf[256];
     std::snprintf(buf, sizeof buf,
                   "vla_scan_fwd: not built for d=%d dv=%d r=%d dtype=%s mode=%s chunk=%d "
-                  "(sequential: d=dv in {16,64,128}, r in {1,4}; chunked: d=dv=64, r in {1,4}, chunk 16)",
+                  "(sequential: d=dv in {16,64,128}, r in {1,4}; chunked: d=dv=64, bf16, r=1 chunk 64 or r=4 chunk 16, 0 = default)",
                   d, dv, r, bf16 ? "bf16" : "f32", mode == VLA_SEQUENTIAL ? "sequential" : "chunked", chunk);
     return fail(h, VLA_ERR_UNSUPPORTED, buf);
   }

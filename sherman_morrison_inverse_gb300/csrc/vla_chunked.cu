@@ -1,12 +1,15 @@
-// Chunked (exact Woodbury / LDL^T) scan: not built yet.
-#include "vla_internal.cuh"
+// Instantiations of the chunked (Woodbury / LDL^T, tcgen05) scan: d = d_v = 64,
+// bfloat16 I/O, r = 1 (64 steps per chunk) and r = 4 (16 steps per chunk).
+#include "vla_chunk.cuh"
 
 namespace vla {
 
 cudaError_t launch_chunked(int d, int r, bool bf16, int chunk, const ScanArgs& a, cudaStream_t s,
                            bool* built) {
-  (void)d; (void)r; (void)bf16; (void)chunk; (void)a; (void)s;
   *built = false;
+  if (d != 64 || !bf16) return cudaSuccess;
+  if (r == 1 && (chunk == 0 || chunk == 64)) { *built = true; return launch_chunk_t<1, __nv_bfloat16>(a, s); }
+  if (r == 4 && (chunk == 0 || chunk == 16)) { *built = true; return launch_chunk_t<4, __nv_bfloat16>(a, s); }
   return cudaSuccess;
 }
 

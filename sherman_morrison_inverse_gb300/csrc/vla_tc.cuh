@@ -1,0 +1,89 @@
+// tcgen05 (5th-generation tensor core) helpers for sm_103a: TMEM allocation,
+// shared-memory matrix descriptors, kind::tf32 MMA with an mbarrier commit, and
+// TMEM loads.  All inline PTX.
+//
+// Operand layout: "K-major, no swizzle".  A row-major M x K fp32 matrix is
+// stored as 8-row x 16-byte core matrices: element (row, k) sits at float offset
+//   (row / 8) * (8 K) + (k / 4) * 32 + (row % 8) * 4 + (k % 4),
+// i.e. leading-dimension byte offset (between core matrices along K) = 128 and
+// stride-dimension byte offset (between 8-row groups) = 32 K.  One MMA consumes
+// K = 8 (two core matrices); the next K step starts 256 bytes further on.
+//
+// D = X * Y^T with X (M x K) and Y (N x K) both in that layout; D is fp32 in
+// TMEM.  For M = 128, row i of D is TMEM lane i.  For M = 64, rows 16q .. 16q+15
+// are lanes 32q .. 32q+15 (q = 0..3), lanes 32q+16 .. 32q+31 are unused.
+#pragma once
+
+#include <stdint.h>
+
+#include "vla_internal.cuh"
+
+namespace vla {
+namespace tc {
+
+__host__ __device__ constexpr int tk_off(int row, int k, int K) {
+  return (row >> 3) * (8 * K) + (k >> 2) * 32 + (row & 7) * 4 + (k & 3);
+}
+
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((128u >> 4) & 0x3FFFu) << 16;        // leading-dimension byte offset
+  d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;   // stride-dimension byte offset
+  d |= (uint64_t)1 << 46;                              // descriptor version (fixed field)
+  return d;                                            // base offset 0, no swizzle
+}
+
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
+  return (1u << 4)                       // D: f32
+         | (2u << 7) | (2u << 10)        // A, B: tf32
+         | ((uint32_t)(N >> 3) << 17)    // N / 8
+         | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot_smem, uint32_t ncols) {  // one full warp
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot_smem)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {  // one full warp
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// One MMA: D (+)= X * Y^T for one K step.
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t xdesc, uint64_t ydesc, uint32_t idesc,
+                                         bool accumulate) {
+  const uint32_t acc = accumulate ? 1u : 0u;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(xdesc), "l"(ydesc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+// Arrive on `bar` once every MMA this thread issued so far has completed.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// 16 consecutive fp32 columns of this warp's 32 TMEM lanes (lane quadrant of the warp).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+}  // namespace tc
+}  // namespace vla

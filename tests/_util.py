@@ -39,7 +39,7 @@ def to_gpu(x: dict, B: int, H: int):
     return out
 
 
-def gpu_scan(x: dict, B: int, H: int, *, P, eps_n, tau, t0=0, mode="sequential", chunk=16, handle=None):
+def gpu_scan(x: dict, B: int, H: int, *, P, eps_n, tau, t0=0, mode="sequential", chunk=0, handle=None):
     """Run the CUDA scan on workload inputs; returns CPU float64 arrays [N, ...] and the status."""
     import sherman_morrison_inverse_gb300 as vla
     g = to_gpu(x, B, H)

@@ -1,0 +1,97 @@
+"""GPU parity of the chunked (exact Woodbury / LDL^T, tcgen05) scan.
+
+The chunked mode takes 64 directions per chunk (64 steps at r = 1, 16 at r = 4)
+with the dense contractions on tensor cores in tf32, for d = d_v = 64 and
+bfloat16 I/O.  It is checked against the float64 oracle and against the
+sequential kernel at the bfloat16 gate (2e-2), on full-length workloads with a
+sample of pairs and on edge cases: ragged lengths, nudges that split chunks
+(t0 phase), renormalisation firing (the exact per-step path) and the
+singularity guard (the step-by-step fallback).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from _util import ensure_built, errs, gpu_scan, oracle_scan
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    ensure_built()
+    import sherman_morrison_inverse_gb300 as vla
+    vla.load_library()
+
+
+def _check(e, tol, label):
+    print(label, {k: f"{v:.2e}" for k, v in e.items()})
+    assert max(e.values()) <= tol, (label, e)
+
+
+@pytest.mark.parametrize("idx,T,sample", [(2, 16384, [0, 77]), (4, 8192, [3, 200])])
+def test_chunked_workload_parity(idx, T, sample):
+    w = workloads.get(idx)
+    x = workloads.make_inputs(w, T=T)
+    kw = dict(P=w.P, eps_n=w.eps_n, tau=w.tau)
+    got = gpu_scan(x, w.B, w.H, mode="chunked", chunk=0, **kw)
+    ref = oracle_scan(x, idx=sample, **kw)
+    _check(errs(got, ref, idx=sample), TOL, f"chunked {w.name} vs oracle")
+    seq = gpu_scan(x, w.B, w.H, **kw)
+    import oracle
+    _check(oracle.errors(*got[:4], *seq[:4]), TOL, f"chunked vs sequential {w.name}")
+    assert got[4]["flags"] == 0 and got[4]["chunk_fallbacks"] == 0
+
+
+EDGE = [
+    # (N, T, r, P, tau, t0)
+    (2, 1, 1, 64, 1e4, 0),
+    (3, 100, 1, 1024, 1e4, 0),        # ragged: one full chunk and a partial one
+    (2, 300, 1, 50, 1e4, 7),          # nudges split chunks, t0 phase
+    (2, 130, 4, 20, 1e4, 3),
+    (1, 200, 1, 1024, 5.0, 0),        # renormalisation fires: exact per-step path
+    (2, 90, 4, 1024, 3.0, 0),
+    (1, 200, 1, 1024, 0.05, 0),       # scales of a chunk fall below 2^-64: S step by step
+]
+
+
+@pytest.mark.parametrize("N,T,r,P,tau,t0", EDGE)
+def test_chunked_edges(N, T, r, P, tau, t0):
+    x = workloads.gaussian_inputs(N, T, 64, 64, r, "bf16", seed=500 + T + r)
+    kw = dict(P=P, eps_n=1e-3, tau=tau, t0=t0)
+    got = gpu_scan(x, 1, N, mode="chunked", chunk=0, **kw)
+    ref = oracle_scan(x, **kw, trace=True)
+    _check(errs(got, ref), TOL, f"chunked edge N{N} T{T} r{r} P{P} tau{tau}")
+    assert got[4]["renorm_count"] == int(ref[4]["renorm"].sum())
+
+
+def test_chunked_guard_falls_back_step_by_step():
+    N, T = 2, 40
+    x = workloads.gaussian_inputs(N, T, 64, 64, 1, "bf16", seed=77)
+    x["A0"] = -torch.eye(64).expand(N, 64, 64).contiguous()
+    x["u"][:, 0] = 0.0
+    x["u"][:, 0, 0, 5] = 1.0          # exactly unit in bf16: delta = 1 - 1 = 0 at step 1
+    x["u"][:, 1:] = (x["u"][:, 1:].float() * 0.5).bfloat16()
+    kw = dict(P=0, eps_n=0.0, tau=1e30)
+    got = gpu_scan(x, 1, N, mode="chunked", chunk=0, **kw)
+    ref = oracle_scan(x, **kw, trace=True)
+    assert ref[4]["guard"][:, 0, 0].all()
+    assert got[4]["chunk_fallbacks"] >= 1
+    assert got[4]["guard_count"] == int(ref[4]["guard"].sum())
+    _check(errs(got, ref), TOL, "chunked guard fallback")
+
+
+def test_chunked_rejects_shapes_it_does_not_build():
+    import sherman_morrison_inverse_gb300 as vla
+    x = workloads.gaussian_inputs(1, 8, 64, 64, 1, "f32", seed=3)
+    with pytest.raises(vla.VlaError, match="UNSUPPORTED"):
+        gpu_scan(x, 1, 1, mode="chunked", P=0, eps_n=0.0, tau=1e4)
+    x = workloads.gaussian_inputs(1, 8, 16, 16, 1, "bf16", seed=3)
+    with pytest.raises(vla.VlaError, match="UNSUPPORTED"):
+        gpu_scan(x, 1, 1, mode="chunked", P=0, eps_n=0.0, tau=1e4)
