@@ -54,6 +54,20 @@ def streamed_bytes_per_token_head(w) -> int:
     return (2 * w.d + w.r * w.d + 2 * w.dv) * es
 
 
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
+# timed kernel, from the ncu captures summarised under profiles/ (scaled from the
+# captured T to the full launch; traffic grows with T).  None when the kernel has
+# changed since its capture.
+TRAFFIC = {
+    ("b8h16_t16384_d64_bf16_recall", "sequential"):
+        (None, "profiles/seq_block_kernel_b8h16_d64_bf16.md (capture predates the current build)"),
+    ("b8h16_t16384_d64_bf16_recall", "chunked"): (None, "no capture of the current build"),
+}
+
+# arithmetic type of each mode's path
+MODE_DTYPE = {"sequential": "f32", "chunked": "tf32"}
+
+
 def fp32_peak_tflops(peaks: dict) -> tuple[float, str]:
     """FP32 CUDA-core peak: SMs x 128 FMA lanes x 2 flops x max SM clock."""
     mhz = float(peaks.get("sm_max_mhz", SM_MAX_MHZ_NOMINAL))
@@ -313,17 +327,22 @@ def main():
     F = flops_per_token_head(w.d, w.dv, w.r)
     achieved_tf = B * H * T * F / (ms_per_step / 1e3) / 1e12
     bytes_step = B * H * T * streamed_bytes_per_token_head(w)
+    traffic = TRAFFIC.get((w.name, args.mode), (None, "no capture for this workload"))
+    if w.T != T_full:
+        traffic = (None, "not the full-length workload")
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "vs_baseline": None, "dtype": MODE_DTYPE[args.mode], "data": "synthetic",
         "config": {"workload": w.name, "B": B, "H": H, "T": T, "d": w.d, "dv": w.dv, "r": w.r,
                    "io": w.io, "state": "f32", "mode": args.mode,
+                   "precision": ("fp32 CUDA-core arithmetic" if args.mode == "sequential" else
+                                 "tcgen05 kind::tf32, 3xTF32 on the products that carry A; fp32 state"),
                    "l2": f"inputs {bytes_step / 1e9:.2f} GB per step > 129 MB L2 (no flush)",
                    "parallelism": f"replicas x{world}, one CTA per (b,h) pair"},
         "roofline": {"bound": "alu", "achieved": achieved_tf, "peak": peak_tf, "unit": "TFLOP/s",
-                     "frac": achieved_tf / peak_tf, "traffic": None,
+                     "frac": achieved_tf / peak_tf, "traffic": traffic[0], "traffic_source": traffic[1],
                      "peak_how": peak_how + " (derived; FP32 is not in the measured-peaks file)",
                      "flops_per_token_head": F,
                      "frac_short_count": (B * H * T * flops_per_token_head_short(w.d, w.dv, w.r)

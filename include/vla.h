@@ -104,7 +104,8 @@ vla_err_t vla_create(vla_handle_t* h, int device);
  *   stream    cudaStream_t as void*.
  *
  * Errors (returned before any launch, nothing is written): INVALID_ARG for a
- * NULL handle or pointer, negative size, misaligned q/k/v/u/A/S, P < 0, t0 < 0,
+ * NULL handle or pointer, negative size, misaligned q/k/v/u/A/S (and o in
+ * VLA_CHUNKED mode, which writes it in 16-byte pieces), P < 0, t0 < 0,
  * tau <= 0 or NaN, non-finite eps_n; UNSUPPORTED for shapes that are not built;
  * CUDA if the launch fails.  There is no CPU fallback. */
 vla_err_t vla_scan_fwd(vla_handle_t h,

@@ -120,6 +120,8 @@ vla_err_t vla_scan_fwd(vla_handle_t h, const void* q, const void* k, const void*
   if (!q || !k || !v || !u || !o) return fail(h, VLA_ERR_INVALID_ARG, "vla_scan_fwd: NULL stream pointer");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(u) || !aligned16(A) || !aligned16(S))
     return fail(h, VLA_ERR_INVALID_ARG, "vla_scan_fwd: q, k, v, u, A and S must be 16-byte aligned");
+  if (mode == VLA_CHUNKED && !aligned16(o))
+    return fail(h, VLA_ERR_INVALID_ARG, "vla_scan_fwd: VLA_CHUNKED needs o 16-byte aligned");
   if (d != dv) return fail(h, VLA_ERR_UNSUPPORTED, "vla_scan_fwd: built only for d == dv");
 
   vla::ScanArgs a{};

@@ -8,15 +8,25 @@
 // chunk with directions U (rows u_a), s-vectors Sigma (rows s_t) and A_0 = the
 // inverse at its start:
 //
-//   G1  [W^T; Q^T]  = [U; Sigma] A_0                    W = A_0 U, Q = A_0 Sigma
-//   G2  [G - I | .] = [W^T; Q^T] [U; Sigma]^T           G = I + U^T A_0 U; rows 64+ give H^T = (U^T Q)^T
+//   G1  [W^T; Q^T] = [U; Sigma] A_0^T,  W = A_0 U^T     W = A_0 U, Q = A_0 Sigma (two MMAs)
+//   G2  [G - I; H^T] = [W^T; Q^T] U^T                    G = I + U^T A_0 U, H = U^T Q
 //       G = L D L^T (CUDA cores; D_jj are the sequential deltas), Linv = L^{-1}
-//   G3  [Z^T | F]   = Linv [W; H^T]^T                   Z = W L^{-T} (the sequential z's), F = Linv H
+//   G3  [Z; F^T] = [W; H^T] Linv^T                       Z = W L^{-T} (the sequential z's), F = Linv H
 //       E = D^{-1} F, masked to directions of steps <= t
-//   G4  [Z D^{-1} Z^T ; (Z E)^T] = [Z D^{-1}; E^T] Z^T  A_1 = A_0 - Z D^{-1} Z^T,  alpha = Q - Z E
+//   G4  [Z D^{-1} Z^T ; (Z E)^T] = [Z D^{-1}; E^T] Z^T   A_1 = A_0 - Z D^{-1} Z^T,  alpha = Q - Z E
 //   G5  [S alpha_t, alpha.alpha ; S phi(q_t), phi(q_t).alpha] = [alpha; Phi_q] [S; alpha]^T
 //   G6  [tril(aq) V ; V^T alpha]   = [tril(aq); V^T] [V^T; alpha^T]^T
 //       o_t = (S phi(q_t) + sum_{t'<=t} (alpha_t'.phi(q_t)) v_t') / den_t,   S_1 = S + V^T alpha
+//
+// Every product is arranged so that its TMEM drain (lane = row of the result)
+// writes the next operand row-major: float4 stores into the K-major core-matrix
+// layout, free of bank conflicts.  The one transposed operand (alpha^T) is
+// written with a per-lane register rotation that spreads the lanes over all banks.
+//
+// LDL^T and L^{-1} run in 16 x 16 blocks: one warp factors a diagonal block in
+// registers (shuffles, no barriers) and inverts its unit-lower factor, all 256
+// threads form the panel and the trailing update, and the off-diagonal blocks of
+// L^{-1} follow from (L^{-1})_ij = -L_ii^{-1} sum_m L_im (L^{-1})_mj by block diagonals.
 //
 // Renormalisation: ||S_t||^2 = ||S||^2 + 2 sum v_t'^T S alpha_t' + sum (v.v)(alpha.alpha) from the
 // products above; the bound ||S|| + sum |v_t||alpha_t| decides that no step can
@@ -28,8 +38,12 @@
 // guard inside the chunk; the chunk is then taken step by step on CUDA cores.
 // Chunks end at nudge steps (A += eps_n I is not a rank-1 update).
 //
-// Operands are fp32 in shared memory, read by the tensor core as tf32; the
-// state (A, S) stays fp32.  Built for d = d_v = 64 and bfloat16 I/O.
+// Precision: operands are fp32 in shared memory, read by the tensor core as
+// tf32.  The products that carry A forward (G1's A_0, G3, G4) are 3xTF32: each
+// fp32 operand x is split into hi = x with its low 13 mantissa bits cleared
+// (exact in tf32) and lo = x - hi, and hi*hi + lo*hi + hi*lo is accumulated, so A
+// tracks the fp32 recurrence.  G2, G5 and G6 are plain tf32.  The state (A, S)
+// stays fp32.  Built for d = d_v = 64 and bfloat16 I/O.
 #pragma once
 
 #include "vla_tc.cuh"
@@ -40,7 +54,10 @@ namespace chk {
 constexpr int D = 64;
 constexpr int NT = 256;
 constexpr int TILE = 64 * 64;         // floats of a TK(64, 64) operand tile
-constexpr int GLD = 68;               // leading dimension of the fp32 G staging
+constexpr int GLD = 65;               // leading dimension of the fp32 G / L staging
+constexpr int YLD = 65;               // leading dimension of the S phi(q) staging
+constexpr int PLD = 68;               // leading dimension of the prologue's phi(k) / phi(q) scratch
+constexpr int BLK = 272;              // floats per packed 16 x 16 block (leading dimension 17)
 constexpr float kGuardEps = 1e-6f;
 constexpr float kReadoutEps = 1e-6f;
 constexpr float kInvSqrtD = 0.125f;
@@ -48,6 +65,13 @@ constexpr float kInvSqrtD = 0.125f;
 // High part of a 3xTF32 split: the value with the low 13 mantissa bits cleared
 // (exactly representable in tf32); the low part is x - hi.
 __device__ __forceinline__ float tf32_hi(float x) { return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u); }
+
+// ELU(x) + 1 with the fast exponential intrinsic (a few ulp for the x <= 0 branch;
+// the chunked path serves bf16 I/O, whose rounding is far coarser)
+__device__ __forceinline__ float phi_fast(float x) { return x > 0.f ? x + 1.f : __expf(x); }
+
+// packed lower-triangular 16 x 16 block (bi >= bj) of a 64 x 64 matrix
+__host__ __device__ constexpr int pblk(int bi, int bj) { return (bi * (bi + 1) / 2 + bj) * BLK; }
 
 template <int R, typename TIO>
 struct Cfg {
@@ -58,26 +82,40 @@ struct Cfg {
   static constexpr uint32_t STAGE = 3 * QB + UB;
   static constexpr uint32_t STAGE_PAD = (STAGE + 1023) / 1024 * 1024;
   static constexpr int T6T = 64 * C;                      // floats of a TK(64, C) tile
-  // float offsets (after the raw stage)
+  // float offsets (after the raw stage); the lifetimes are listed per region
   static constexpr int F_A = 0;                           // A
   static constexpr int F_S = F_A + TILE;                  // S       } [S][alpha][phi(q)] contiguous
   static constexpr int F_AL = F_S + TILE;                 // alpha   }
   static constexpr int F_PQ = F_AL + TILE;                // phi(q)  }
-  static constexpr int F_P = F_PQ + TILE;                 // 2 tiles: [U; Sigma] -> G staging -> [Z/D; E^T] -> Y staging
-  static constexpr int F_Q = F_P + 2 * TILE;              // 2 tiles: [W^T; Q^T] -> (Z, Q^T) -> alpha Gram
-  static constexpr int F_R = F_Q + 2 * TILE;              // 2 tiles: prologue scratch -> [W; H^T] -> T6 (with L)
-  static constexpr int F_L = F_R + 2 * TILE;              // 1 tile:  Linv
+  static constexpr int F_P = F_PQ + TILE;                 // 2 tiles: [U; Sigma] -> G/L staging -> [W; H^T] lo
+                                                          //          -> [Z/D; E^T] lo -> S phi(q) staging
+  static constexpr int F_Q = F_P + 2 * TILE;              // 2 tiles: [W^T; Q^T]; tile 0 -> L^{-1} blocks ->
+                                                          //          Linv lo -> Z lo -> alpha Gram; tile 1 -> v Gram
+  static constexpr int F_R = F_Q + 2 * TILE;              // 2 tiles: prologue scratch -> A hi/lo -> [W; H^T] (hi)
+                                                          //          -> [Z/D; E^T] hi -> T6
+  static constexpr int F_L = F_R + 2 * TILE;              // 1 tile:  prologue scratch -> products of the Linv
+                                                          //          assembly -> Linv hi -> Z hi -> T6 (alpha^T)
   static constexpr int F_T6 = F_R;                        // [tril(aq)][V^T][alpha^T], TK(64, C) each
   static constexpr int F_MISC = F_L + TILE;
   // misc block
   static constexpr int M_D = 0, M_ID = 64, M_RDEN = 128, M_VN = 192, M_SL = 256, M_XS = 320, M_AN = 384;
   static constexpr int M_SG = 448, M_IS = 512, M_RED = 576, M_VEC = 640, M_VEC2 = 704, M_SCAL = 768;
-  static constexpr int F_VB = F_MISC + 800;               // V of the chunk (TIO) [C][64]
+  static constexpr int M_N = 800, M_NSEG = 864, M_AN2 = 1120;
+  static constexpr int MISC = 1248;
+  static constexpr int F_VB = F_MISC + MISC;              // V of the chunk (TIO) [C][64]
   static constexpr size_t float_bytes = sizeof(float) * (size_t)F_VB + sizeof(TIO) * C * 64;
   static constexpr size_t bar_off = STAGE_PAD + (float_bytes + 15) / 16 * 16;
   static constexpr size_t bytes = bar_off + 64;
   static_assert(3 * T6T <= 3 * TILE, "T6 fits in R and L");
+  static_assert(64 * GLD <= 2 * TILE && 64 * YLD <= 2 * TILE, "stagings fit in P");
+  static_assert(2 * C * PLD <= 3 * TILE, "prologue scratch fits in R and L");
+  static_assert(pblk(3, 3) + BLK <= TILE, "packed blocks fit in one tile");
   static_assert(bytes <= 227 * 1024, "shared memory");
+};
+
+struct MmaPass {
+  int x, y, m, n, col;   // operand offsets (floats), shape, TMEM column
+  bool acc;              // accumulate into the column's previous value
 };
 
 }  // namespace chk
@@ -88,6 +126,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
   using Cf = Cfg<R, TIO>;
   constexpr int C = Cf::C, TS = Cf::TS;
   using tc::tk_off;
+  static_assert(sizeof(TIO) == 2, "bfloat16 I/O");
 
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char* raw = smem;
@@ -118,7 +157,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     sf[Cf::F_A + tk_off(i, j, 64)] = gA[e];
     sf[Cf::F_S + tk_off(i, j, 64)] = gS[e];
   }
-  float n_i = (tid < D) ? gn[tid] : 0.f;
+  if (tid < D) misc[Cf::M_N + tid] = gn[tid];
   if (tid == 0) {
     mbar_init(in_bar, 1);
     mbar_init(mma_bar, 1);
@@ -157,17 +196,16 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     __syncthreads();
     tc::fence_after_sync();
   };
-  // D = sum over passes of X_p * Y_p^T into TMEM columns 0.. (X_p: M rows, Y_p: N_p rows,
-  // both K-major with K columns).  Three passes (hi*hi, lo*hi, hi*lo) give 3xTF32.
-  auto gemm_passes = [&](int M, int K, int np, const int* xo, const int* yo, const int* nn) -> bool {
+  // Issue the passes (each D (+)= X Y^T over K), wait for them; false on a timeout.
+  auto mma_run = [&](const MmaPass* ps, int np, int K) -> bool {
     sync_tc();
     if (tid == 0) {
       const uint32_t sbo = 32u * (uint32_t)K;
       for (int p = 0; p < np; ++p) {
-        const uint32_t idesc = tc::idesc_tf32(M, nn[p]);
+        const uint32_t idesc = tc::idesc_tf32(ps[p].m, ps[p].n);
         for (int kk = 0; kk < K / 8; ++kk)
-          tc::mma_tf32(tmem, tc::sdesc(sbase + 4u * xo[p] + 256u * kk, sbo),
-                       tc::sdesc(sbase + 4u * yo[p] + 256u * kk, sbo), idesc, p > 0 || kk > 0);
+          tc::mma_tf32(tmem + (uint32_t)ps[p].col, tc::sdesc(sbase + 4u * ps[p].x + 256u * kk, sbo),
+                       tc::sdesc(sbase + 4u * ps[p].y + 256u * kk, sbo), idesc, ps[p].acc || kk > 0);
       }
       tc::mma_commit(mma_bar);
       if (!mbar_wait_bounded(mma_bar, mma_phase)) *flag = 1;
@@ -178,25 +216,45 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     tc::fence_after_sync();
     return *flag == 0;
   };
-  auto gemm = [&](int xoff, int yoff, int M, int N, int K) -> bool {
-    const int xo[1] = {xoff}, yo[1] = {yoff}, nn[1] = {N};
-    return gemm_passes(M, K, 1, xo, yo, nn);
-  };
   // the warp's TMEM lane quadrant and column half
   const int q4 = warp & 3, half = warp >> 2;
+  const int row = 32 * q4 + lane;   // row of an M = 128 result held by this thread
   auto tld = [&](int col, float (&v)[16]) { tc::tmem_ld16(tmem + ((uint32_t)(32 * q4) << 16) + (uint32_t)col, v); };
+  auto st4 = [&](int off, float x0, float x1, float x2, float x3) {
+    *reinterpret_cast<float4*>(sf + off) = make_float4(x0, x1, x2, x3);
+  };
+  auto st4_split = [&](int off_hi, int off_lo, const float* x) {
+    const float h0 = tf32_hi(x[0]), h1 = tf32_hi(x[1]), h2 = tf32_hi(x[2]), h3 = tf32_hi(x[3]);
+    st4(off_hi, h0, h1, h2, h3);
+    st4(off_lo, x[0] - h0, x[1] - h1, x[2] - h2, x[3] - h3);
+  };
 
-  // block reduction of one float over the CTA (all threads call it)
+  // block reduction of two floats over the CTA (all threads call it)
+  auto block_sum2 = [&](float& x, float& y) {
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) {
+      x += __shfl_xor_sync(0xffffffffu, x, m);
+      y += __shfl_xor_sync(0xffffffffu, y, m);
+    }
+    __syncthreads();
+    if (lane == 0) {
+      misc[Cf::M_RED + warp] = x;
+      misc[Cf::M_RED + 8 + warp] = y;
+    }
+    __syncthreads();
+    float s = 0.f, s2 = 0.f;
+#pragma unroll
+    for (int w = 0; w < NT / 32; ++w) {
+      s += misc[Cf::M_RED + w];
+      s2 += misc[Cf::M_RED + 8 + w];
+    }
+    x = s;
+    y = s2;
+  };
   auto block_sum = [&](float x) -> float {
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
-    __syncthreads();
-    if (lane == 0) misc[Cf::M_RED + warp] = x;
-    __syncthreads();
-    float s = 0.f;
-#pragma unroll
-    for (int w = 0; w < NT / 32; ++w) s += misc[Cf::M_RED + w];
-    return s;
+    float y = 0.f;
+    block_sum2(x, y);
+    return x;
   };
 
   long long pos = 0;
@@ -222,54 +280,87 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     const TIO* rv = reinterpret_cast<const TIO*>(raw + 2 * Cf::QB);
     const TIO* ru = reinterpret_cast<const TIO*>(raw + 3 * Cf::QB);
 
-    // ---------------- prologue: [U; Sigma] -> P, phi(q) -> PQ, V -> vb, phi(k) -> R scratch
+    // ---------------- prologue: [U; Sigma] -> P, phi(q) -> PQ, V -> vb, n, 1/den, |v|
     {
-      float* prod = sf + Cf::F_R;
-      for (int e4 = tid; e4 < 64 * 16; e4 += NT) {   // U rows a (64), 4 columns each
-        const int arow = e4 >> 4, col = (e4 & 15) * 4;
-        const int t = arow / R, i = arow - t * R;
-        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (t < c) {
-          const TIO* src = ru + ((ts + t) * R + i) * D + col;
-          x = make_float4(to_f32(src[0]), to_f32(src[1]), to_f32(src[2]), to_f32(src[3]));
+      float* pk = sf + Cf::F_R;              // phi(k_t)[i] at t * PLD + i, then n_t[i] phi(q_t)[i]
+      float* pq = sf + Cf::F_R + C * PLD;    // phi(q_t)[i]
+      // Rows of 8-element pieces: in each group of 8 lanes the rows (row % 8) and the pieces
+      // differ, so the 16-byte reads of the bf16 rows and the float4 stores into the
+      // core-matrix layout are both free of bank conflicts.
+      auto unpack8 = [](const uint4& w, float (&x)[8]) {
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ww[m]));
+          x[2 * m] = f.x;
+          x[2 * m + 1] = f.y;
         }
-        *reinterpret_cast<float4*>(sf + Cf::F_P + tk_off(arow, col, 64)) = x;
+      };
+      for (int f = tid; f < 64 * 8; f += NT) {   // U rows a (64 x 8 pieces)
+        const int arow = (f >> 6) * 8 + (f & 7), pc = ((f & 7) + (f >> 3)) & 7;
+        float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (arow / R < c) unpack8(*reinterpret_cast<const uint4*>(ru + (ts * R + arow) * D + 8 * pc), x);
+        st4(Cf::F_P + tk_off(arow, 8 * pc, 64), x[0], x[1], x[2], x[3]);
+        st4(Cf::F_P + tk_off(arow, 8 * pc + 4, 64), x[4], x[5], x[6], x[7]);
       }
-      for (int e4 = tid; e4 < C * 16; e4 += NT) {    // step rows t < C
-        const int t = e4 >> 4, col = (e4 & 15) * 4;
-        float kx[4] = {0.f, 0.f, 0.f, 0.f}, qx[4] = {0.f, 0.f, 0.f, 0.f};
-        TIO vx[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) vx[j] = from_f32<TIO>(0.f);
+      for (int f = tid; f < C * 8; f += NT) {    // step rows t < C; rows c.. are zero (Sigma, phi(q), V)
+        const int t = (f >> 6) * 8 + (f & 7), pc = ((f & 7) + (f >> 3)) & 7;
+        float kx[8], qx[8];
+        uint4 vw = make_uint4(0u, 0u, 0u, 0u);
         if (t < c) {
+          const int off = (ts + t) * D + 8 * pc;
+          unpack8(*reinterpret_cast<const uint4*>(rk + off), kx);
+          unpack8(*reinterpret_cast<const uint4*>(rq + off), qx);
+          vw = *reinterpret_cast<const uint4*>(rv + off);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            kx[j] = phi_elu1(to_f32(rk[(ts + t) * D + col + j]));
-            qx[j] = phi_elu1(to_f32(rq[(ts + t) * D + col + j]));
-            vx[j] = rv[(ts + t) * D + col + j];
+          for (int m = 0; m < 8; ++m) {
+            kx[m] = phi_fast(kx[m]);
+            qx[m] = phi_fast(qx[m]);
           }
-        }
-        *reinterpret_cast<float4*>(sf + Cf::F_P + tk_off(64 + t, col, 64)) =
-            make_float4(kx[0] * kInvSqrtD, kx[1] * kInvSqrtD, kx[2] * kInvSqrtD, kx[3] * kInvSqrtD);
-        *reinterpret_cast<float4*>(sf + Cf::F_PQ + tk_off(t, col, 64)) = make_float4(qx[0], qx[1], qx[2], qx[3]);
-        *reinterpret_cast<float4*>(prod + t * 64 + col) = make_float4(kx[0], kx[1], kx[2], kx[3]);
+        } else {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) vb[t * 64 + col + j] = vx[j];
+          for (int m = 0; m < 8; ++m) kx[m] = qx[m] = 0.f;
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int col = 8 * pc + 4 * h;
+          const float* k4 = kx + 4 * h;
+          const float* q4p = qx + 4 * h;
+          st4(Cf::F_P + tk_off(64 + t, col, 64), k4[0] * kInvSqrtD, k4[1] * kInvSqrtD, k4[2] * kInvSqrtD,
+              k4[3] * kInvSqrtD);
+          st4(Cf::F_PQ + tk_off(t, col, 64), q4p[0], q4p[1], q4p[2], q4p[3]);
+          *reinterpret_cast<float4*>(pk + t * PLD + col) = make_float4(k4[0], k4[1], k4[2], k4[3]);
+          *reinterpret_cast<float4*>(pq + t * PLD + col) = make_float4(q4p[0], q4p[1], q4p[2], q4p[3]);
+        }
+        *reinterpret_cast<uint4*>(vb + t * 64 + 8 * pc) = vw;
       }
       for (int e4 = tid; e4 < (64 - C) * 16; e4 += NT) {   // zero rows C..63 of Sigma and phi(q)
         const int t = C + (e4 >> 4), col = (e4 & 15) * 4;
-        *reinterpret_cast<float4*>(sf + Cf::F_P + tk_off(64 + t, col, 64)) = make_float4(0.f, 0.f, 0.f, 0.f);
-        *reinterpret_cast<float4*>(sf + Cf::F_PQ + tk_off(t, col, 64)) = make_float4(0.f, 0.f, 0.f, 0.f);
+        st4(Cf::F_P + tk_off(64 + t, col, 64), 0.f, 0.f, 0.f, 0.f);
+        st4(Cf::F_PQ + tk_off(t, col, 64), 0.f, 0.f, 0.f, 0.f);
       }
       __syncthreads();
-      if (tid < D) {   // n_t = n_{t-1} + phi(k_t); products n_t[i] phi(q_t)[i]
-        for (int t = 0; t < c; ++t) {
-          n_i += prod[t * 64 + tid];
-          prod[t * 64 + tid] = n_i * sf[Cf::F_PQ + tk_off(t, tid, 64)];
-        }
-        misc[Cf::M_SL + tid] = sf[Cf::F_P + tk_off(64 + c - 1, tid, 64)];   // s of the chunk's last step
+      // n_t = n_{t-1} + phi(k_t): column i, four segments of C/4 steps (one per thread)
+      constexpr int SEG = C / 4;
+      const int ci = tid & 63, sg4 = tid >> 6;
+      {
+        float tot = 0.f;
+#pragma unroll
+        for (int j = 0; j < SEG; ++j) tot += pk[(SEG * sg4 + j) * PLD + ci];
+        misc[Cf::M_NSEG + sg4 * 64 + ci] = tot;
+      }
+      if (tid < D) misc[Cf::M_SL + tid] = sf[Cf::F_P + tk_off(64 + c - 1, tid, 64)];   // s of the chunk's last step
+      __syncthreads();
+      float nrun = misc[Cf::M_N + ci];
+      for (int s2 = 0; s2 < sg4; ++s2) nrun += misc[Cf::M_NSEG + s2 * 64 + ci];
+#pragma unroll
+      for (int j = 0; j < SEG; ++j) {
+        const int t = SEG * sg4 + j;
+        nrun += pk[t * PLD + ci];
+        pk[t * PLD + ci] = nrun * pq[t * PLD + ci];
       }
       __syncthreads();
+      if (sg4 == 3) misc[Cf::M_N + ci] = nrun;   // n after the chunk (zero rows past c add nothing)
       {  // 1/den_t and |v_t|: NT / C threads per step (every lane takes part in the shuffles)
         constexpr int TPS = NT / C;
         constexpr int EPT = 64 / TPS;
@@ -278,7 +369,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
         if (t < c) {
 #pragma unroll
           for (int j = 0; j < EPT; ++j) {
-            dn += prod[t * 64 + part * EPT + j];
+            dn += pk[t * PLD + part * EPT + j];
             const float x = to_f32(vb[t * 64 + part * EPT + j]);
             vv = fmaf(x, x, vv);
           }
@@ -299,130 +390,185 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
         fence_proxy_async_smem();
         issue(tile + 1);
       }
+      // A -> hi (R tile 0) + lo (R tile 1)
+      for (int e4 = tid; e4 < TILE / 4; e4 += NT) {
+        const float4 x = *reinterpret_cast<const float4*>(sf + Cf::F_A + 4 * e4);
+        const float xv[4] = {x.x, x.y, x.z, x.w};
+        st4_split(Cf::F_R + 4 * e4, Cf::F_R + TILE + 4 * e4, xv);
+      }
     }
 
-    // ---------------- G1: [W^T; Q^T] = [U; Sigma] A_0^T  (M 128, N 64, K 64), A split hi + lo
-    // (U is exact in tf32, so two passes make W as accurate as fp32)
-    for (int e4 = tid; e4 < TILE / 4; e4 += NT) {
-      const float4 x = *reinterpret_cast<const float4*>(sf + Cf::F_A + 4 * e4);
-      const float4 h = make_float4(tf32_hi(x.x), tf32_hi(x.y), tf32_hi(x.z), tf32_hi(x.w));
-      *reinterpret_cast<float4*>(sf + Cf::F_R + 4 * e4) = h;
-      *reinterpret_cast<float4*>(sf + Cf::F_R + TILE + 4 * e4) = make_float4(x.x - h.x, x.y - h.y, x.z - h.z, x.w - h.w);
-    }
+    // ---------------- G1: [W^T; Q^T] = [U; Sigma] A_0^T (cols 0..63), W = A_0 U^T (cols 64..127, M 64)
     {
-      const int xo[2] = {Cf::F_P, Cf::F_P}, yo[2] = {Cf::F_R, Cf::F_R + TILE}, nn[2] = {64, 64};
-      if (!gemm_passes(128, 64, 2, xo, yo, nn)) { failed = true; break; }
+      const MmaPass ps[4] = {{Cf::F_P, Cf::F_R, 128, 64, 0, false},
+                             {Cf::F_P, Cf::F_R + TILE, 128, 64, 0, true},
+                             {Cf::F_R, Cf::F_P, 64, 64, 64, false},
+                             {Cf::F_R + TILE, Cf::F_P, 64, 64, 64, true}};
+      if (!mma_run(ps, 4, 64)) { failed = true; break; }
     }
     {
       float v[16];
-      const int row = 32 * q4 + lane;
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {   // [W^T; Q^T] -> Q tiles (X of G2)
+        const int col0 = 32 * half + 16 * cc;
+        tld(col0, v);
+#pragma unroll
+        for (int j = 0; j < 16; j += 4) st4(Cf::F_Q + tk_off(row, col0 + j, 64), v[j], v[j + 1], v[j + 2], v[j + 3]);
+      }
+      const int wi = 16 * q4 + (lane & 15);   // M = 64 result: row wi in lane 32 q4 + wi % 16
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {   // W (rows i) fp32 -> R tile 0
+        const int col0 = 32 * half + 16 * cc;
+        tld(64 + col0, v);
+        if (lane < 16) {
+#pragma unroll
+          for (int j = 0; j < 16; j += 4) st4(Cf::F_R + tk_off(wi, col0 + j, 64), v[j], v[j + 1], v[j + 2], v[j + 3]);
+        }
+      }
+    }
+    // ---------------- G2: [G - I; H^T] = [W^T; Q^T] U^T  (M 128, N 64, K 64)
+    {
+      const MmaPass ps[1] = {{Cf::F_Q, Cf::F_P, 128, 64, 0, false}};
+      if (!mma_run(ps, 1, 64)) { failed = true; break; }
+    }
+    float* Gs = sf + Cf::F_P;   // [64][GLD]: G, then L (strict lower) in place
+    {
+      float v[16];
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int col0 = 32 * half + 16 * cc;
         tld(col0, v);
-#pragma unroll
-        for (int j = 0; j < 16; j += 4)
-          *reinterpret_cast<float4*>(sf + Cf::F_Q + tk_off(row, col0 + j, 64)) =
-              make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-        if (row < 64) {   // W (rows i, K = direction) for G3
-#pragma unroll
-          for (int j = 0; j < 16; ++j) sf[Cf::F_R + tk_off(col0 + j, row, 64)] = v[j];
-        }
-      }
-    }
-    // ---------------- G2: [G - I | .] = [W^T; Q^T] [U; Sigma]^T  (M 128, N 128, K 64)
-    if (!gemm(Cf::F_Q, Cf::F_P, 128, 128, 64)) { failed = true; break; }
-    if (half == 0) {   // columns 0..63 only
-      float v[16];
-      const int row = 32 * q4 + lane;
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        const int col0 = 16 * cc;
-        tld(col0, v);
         if (row < 64) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) sf[Cf::F_P + row * GLD + col0 + j] = v[j] + ((row == col0 + j) ? 1.f : 0.f);
-        } else {   // H^T rows t for G3 (rows 64.. of [W; H^T])
+          for (int j = 0; j < 16; ++j) Gs[row * GLD + col0 + j] = v[j] + ((row == col0 + j) ? 1.f : 0.f);
+        } else {   // H^T (rows t) fp32 -> R tile 1 (rows 64 + t of [W; H^T])
 #pragma unroll
-          for (int j = 0; j < 16; j += 4)
-            *reinterpret_cast<float4*>(sf + Cf::F_R + tk_off(row, col0 + j, 64)) =
-                make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+          for (int j = 0; j < 16; j += 4) st4(Cf::F_R + tk_off(row, col0 + j, 64), v[j], v[j + 1], v[j + 2], v[j + 3]);
         }
       }
     }
     tc::fence_before_sync();
     __syncthreads();
 
-    // ---------------- LDL^T of G (fp32, in place in the staging), blocks of 4 columns
-    float* Gs = sf + Cf::F_P;
-    for (int j0 = 0; j0 < 64; j0 += 4) {
-      // the 4 x 4 diagonal block, redundantly in every thread
-      float g[4][4], Lb[4][4], Db[4];
+    // ---------------- LDL^T of G and X = L^{-1} in 16 x 16 blocks (fp32)
+    // Right-looking block LDL^T with the inverse carried along as a forward
+    // elimination of the identity: for block column k,
+    //   [a] one warp factors the diagonal block G'_kk = L_kk D_k L_kk^T in registers;
+    //   [b] 64 independent forward substitutions with L_kk, one per thread: the columns
+    //       of X_kk = L_kk^{-1}, the panel rows (L D)_r = L_kk^{-1} G'_rk (i > k) and the
+    //       columns of X_kj = L_kk^{-1} B_kj (j < k);
+    //   [c] trailing G'_ij -= L_ik D_k L_jk^T (k < j <= i) and B_ij -= L_ik X_kj (j <= k < i),
+    // where B is the identity being eliminated (B_ij = 0 for i != j at the start).
+    // L D (the panel before D^{-1}) is kept, transposed, in the unused upper blocks of the staging.
+    float* XB = sf + Cf::F_Q;   // packed blocks: B, then X = L^{-1}
+#pragma unroll 1
+    for (int k = 0; k < 4; ++k) {
+      if (warp == 0) {   // [a]: lane i (both half-warps) holds row i of G'_kk
+        const int i = lane & 15;
+        float g[16];
 #pragma unroll
-      for (int r = 0; r < 4; ++r)
+        for (int j = 0; j < 16; ++j) g[j] = Gs[(16 * k + i) * GLD + 16 * k + j];
+        float dmy = 1.f, idmy = 1.f;
 #pragma unroll
-        for (int s = 0; s <= r; ++s) g[r][s] = Gs[(j0 + r) * GLD + j0 + s];
+        for (int j = 0; j < 16; ++j) {
+          const float dj = __shfl_sync(0xffffffffu, g[j], j);
+          const float rj = __fdividef(1.f, dj);
+          if (i == j) { dmy = dj; idmy = rj; }
+          const float lij = (i > j) ? g[j] * rj : 0.f;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        float dj = g[j][j];
-#pragma unroll
-        for (int k = 0; k < j; ++k) dj = fmaf(-Lb[j][k] * Db[k], Lb[j][k], dj);
-        Db[j] = dj;
-#pragma unroll
-        for (int i = j + 1; i < 4; ++i) {
-          float x = g[i][j];
-#pragma unroll
-          for (int k = 0; k < j; ++k) x = fmaf(-Lb[i][k] * Db[k], Lb[j][k], x);
-          Lb[i][j] = x / dj;
+          for (int m = j + 1; m < 16; ++m)   // G'[j][m] = L[m][j] D_j (the block stays symmetric)
+            g[m] = fmaf(-lij, __shfl_sync(0xffffffffu, g[m], j), g[m]);
+          if (i > j) g[j] = lij;
         }
-      }
-      float iDb[4];
+        if (lane < 16) {
+          misc[Cf::M_D + 16 * k + i] = dmy;
+          misc[Cf::M_ID + 16 * k + i] = idmy;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) iDb[j] = 1.f / Db[j];
-      __syncthreads();   // everyone has read the block before the panel is overwritten
-      if (tid < 4) {
-        misc[Cf::M_D + j0 + tid] = Db[tid];
-        misc[Cf::M_ID + j0 + tid] = iDb[tid];
-      }
-      if (tid == 0) {
-#pragma unroll
-        for (int r = 1; r < 4; ++r)
-#pragma unroll
-          for (int s = 0; s < r; ++s) Gs[(j0 + r) * GLD + j0 + s] = Lb[r][s];
-      }
-      // panel rows i >= j0 + 4: L[i][j0 + k]
-      const int i = j0 + 4 + tid;
-      float li[4] = {0.f, 0.f, 0.f, 0.f};
-      if (i < 64) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          float x = Gs[i * GLD + j0 + k];
-#pragma unroll
-          for (int kp = 0; kp < k; ++kp) x = fmaf(-li[kp] * Db[kp], Lb[k][kp], x);
-          li[k] = x * iDb[k];
+          for (int j = 0; j < 15; ++j)
+            if (j < i) Gs[(16 * k + i) * GLD + 16 * k + j] = g[j];
         }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) Gs[i * GLD + j0 + k] = li[k];
       }
       __syncthreads();
-      // trailing update of the lower triangle: G[i][k] -= sum_k' L[i][k'] D[k'] L[k][k']
-      for (int e = tid; e < (64 - j0 - 4) * 16; e += NT) {
-        const int ii = j0 + 4 + (e >> 4), kq = (e & 15) * 4;
-        float lir[4];
+      if (tid < 64) {   // [b]: chain q = tid
+        const int npan = 48 - 16 * k;
+        float y[16];
+        if (tid < 16) {                        // column tid of X_kk
 #pragma unroll
-        for (int k = 0; k < 4; ++k) lir[k] = Gs[ii * GLD + j0 + k] * Db[k];
+          for (int m = 0; m < 16; ++m) y[m] = (m == tid) ? 1.f : 0.f;
+        } else if (tid < 16 + npan) {          // panel row r
+          const int r = 16 * (k + 1) + (tid - 16);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int kk = kq + j;
-          if (kk >= j0 + 4 && kk <= ii) {
-            float x = Gs[ii * GLD + kk];
+          for (int m = 0; m < 16; ++m) y[m] = Gs[r * GLD + 16 * k + m];
+        } else {                               // column of B_kj, j < k
+          const int idx = tid - 16 - npan, bj = idx >> 4, cl = idx & 15;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) x = fmaf(-lir[k], Gs[kk * GLD + j0 + k], x);
-            Gs[ii * GLD + kk] = x;
+          for (int m = 0; m < 16; ++m) y[m] = XB[pblk(k, bj) + m * 17 + cl];
+        }
+        // y <- L_kk^{-1} y (unit lower, L_kk strict lower part in the staging)
+#pragma unroll
+        for (int m = 0; m < 15; ++m)
+#pragma unroll
+          for (int ii = m + 1; ii < 16; ++ii) y[ii] = fmaf(-Gs[(16 * k + ii) * GLD + 16 * k + m], y[m], y[ii]);
+        if (tid < 16) {
+#pragma unroll
+          for (int m = 0; m < 16; ++m) XB[pblk(k, k) + m * 17 + tid] = y[m];
+        } else if (tid < 16 + npan) {
+          const int r = 16 * (k + 1) + (tid - 16);
+#pragma unroll
+          for (int m = 0; m < 16; ++m) {
+            Gs[(16 * k + m) * GLD + r] = y[m];                          // L D, transposed (upper block)
+            Gs[r * GLD + 16 * k + m] = y[m] * misc[Cf::M_ID + 16 * k + m];   // L
           }
+        } else {
+          const int idx = tid - 16 - npan, bj = idx >> 4, cl = idx & 15;
+#pragma unroll
+          for (int m = 0; m < 16; ++m) XB[pblk(k, bj) + m * 17 + cl] = y[m];
         }
       }
       __syncthreads();
+      if (k < 3) {
+        // [c]: trailing blocks (bi, bj), k < bj <= bi, then B blocks (bi, bj), bj <= k < bi
+        constexpr int NTR = 6;                     // largest count of trailing blocks (k = 0)
+        const int ntr = (3 - k) * (4 - k) / 2, nb = (3 - k) * (k + 1);
+        for (int e = tid; e < (ntr + nb) * 256; e += NT) {
+          const int blk = e >> 8, r = (e >> 4) & 15, cl = e & 15;
+          const float* lrow;   // L_ik row r (16 values)
+          const float* xcol;   // column cl of (L D)^T_jk or X_kj, stride sx
+          float* dst;
+          float acc;
+          int sx;
+          if (blk < ntr) {
+            // blk -> (bi, bj) over the lower block triangle of rows/columns k+1..3
+            int bi = k + 1, cnt = blk;
+#pragma unroll
+            for (int q = 0; q < NTR; ++q)
+              if (cnt > bi - (k + 1)) { cnt -= bi - k; ++bi; }
+            const int gr = 16 * bi + r, gc = 16 * (k + 1 + cnt) + cl;
+            lrow = Gs + gr * GLD + 16 * k;
+            xcol = Gs + 16 * k * GLD + gc;
+            sx = GLD;
+            dst = Gs + gr * GLD + gc;
+            acc = *dst;
+          } else {
+            const int b2 = blk - ntr, bi = k + 1 + b2 / (k + 1), bj = b2 % (k + 1);
+            lrow = Gs + (16 * bi + r) * GLD + 16 * k;
+            xcol = XB + pblk(k, bj) + cl;
+            sx = 17;
+            dst = XB + pblk(bi, bj) + r * 17 + cl;
+            acc = (k == bj) ? 0.f : *dst;   // B_ij starts at 0
+          }
+          float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+#pragma unroll
+          for (int m = 0; m < 16; m += 4) {
+            p0 = fmaf(lrow[m], xcol[m * sx], p0);
+            p1 = fmaf(lrow[m + 1], xcol[(m + 1) * sx], p1);
+            p2 = fmaf(lrow[m + 2], xcol[(m + 2) * sx], p2);
+            p3 = fmaf(lrow[m + 3], xcol[(m + 3) * sx], p3);
+          }
+          *dst = acc - ((p0 + p1) + (p2 + p3));
+        }
+        __syncthreads();
+      }
     }
     // pivot check: the guard would fire inside the chunk
     int bad = 0;
@@ -436,7 +582,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
       ++fallback_cnt;
       float* vec = misc + Cf::M_VEC;     // u, then s
       float* vec2 = misc + Cf::M_VEC2;   // z, alpha
-      const int row = tid >> 2, cq = tid & 3;   // row of A / S and a 16-column quarter
+      const int ar = tid >> 2, cq = tid & 3;   // row of A / S and a 16-column quarter
       for (int t = 0; t < c; ++t) {
         const long long st = pos + t;
         for (int i = 0; i < R; ++i) {
@@ -444,10 +590,10 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
           __syncthreads();
           float zp = 0.f;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) zp = fmaf(sf[Cf::F_A + tk_off(row, 16 * cq + j, 64)], vec[16 * cq + j], zp);
+          for (int j = 0; j < 16; ++j) zp = fmaf(sf[Cf::F_A + tk_off(ar, 16 * cq + j, 64)], vec[16 * cq + j], zp);
           zp += __shfl_xor_sync(0xffffffffu, zp, 1);
           zp += __shfl_xor_sync(0xffffffffu, zp, 2);
-          if (cq == 0) vec2[row] = zp;
+          if (cq == 0) vec2[ar] = zp;
           __syncthreads();
           const float dl = 1.f + block_sum(tid < 64 ? vec[tid] * vec2[tid] : 0.f);
           const bool gd = fabsf(dl) < kGuardEps;
@@ -455,30 +601,30 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int col = 16 * cq + j;
-            float& ar = sf[Cf::F_A + tk_off(row, col, 64)];
-            if (gd) ar += (row == col) ? kGuardEps : 0.f;
-            else ar = fmaf(-vec2[row] / dl, vec2[col], ar);
+            float& av = sf[Cf::F_A + tk_off(ar, col, 64)];
+            if (gd) av += (ar == col) ? kGuardEps : 0.f;
+            else av = fmaf(-vec2[ar] / dl, vec2[col], av);
           }
           __syncthreads();
         }
         const bool nd = nudge && t == c - 1;
-        if (nd && cq == (row >> 4)) sf[Cf::F_A + tk_off(row, row, 64)] += a.eps_n;
+        if (nd && cq == (ar >> 4)) sf[Cf::F_A + tk_off(ar, ar, 64)] += a.eps_n;
         if (tid < 64) vec[tid] = phi_elu1(to_f32(gk[st * D + tid])) * kInvSqrtD;
         __syncthreads();
         float ap = 0.f;   // alpha = A s
 #pragma unroll
-        for (int j = 0; j < 16; ++j) ap = fmaf(sf[Cf::F_A + tk_off(row, 16 * cq + j, 64)], vec[16 * cq + j], ap);
+        for (int j = 0; j < 16; ++j) ap = fmaf(sf[Cf::F_A + tk_off(ar, 16 * cq + j, 64)], vec[16 * cq + j], ap);
         ap += __shfl_xor_sync(0xffffffffu, ap, 1);
         ap += __shfl_xor_sync(0xffffffffu, ap, 2);
-        if (cq == 0) vec2[row] = ap;
+        if (cq == 0) vec2[ar] = ap;
         __syncthreads();
         // S += v alpha^T, then the norm
-        const float vr = to_f32(vb[t * 64 + row]);   // v of step t
+        const float vr = to_f32(vb[t * 64 + ar]);   // v of step t
         float sq = 0.f;
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int col = 16 * cq + j;
-          float& sr = sf[Cf::F_S + tk_off(row, col, 64)];
+          float& sr = sf[Cf::F_S + tk_off(ar, col, 64)];
           sr = fmaf(vr, vec2[col], sr);
           sq = fmaf(sr, sr, sq);
         }
@@ -486,7 +632,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
         if (nrm > a.tau) {
           const float cf = a.tau / nrm;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) sf[Cf::F_S + tk_off(row, 16 * cq + j, 64)] *= cf;
+          for (int j = 0; j < 16; ++j) sf[Cf::F_S + tk_off(ar, 16 * cq + j, 64)] *= cf;
           if (tid == 0) ++renorm_cnt;
         }
         if (!isfinite(nrm)) flags |= kStatusNonfinite;
@@ -494,182 +640,238 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
         __syncthreads();
         float op = 0.f;   // o = S phi(q) / den
 #pragma unroll
-        for (int j = 0; j < 16; ++j) op = fmaf(sf[Cf::F_S + tk_off(row, 16 * cq + j, 64)], vec[16 * cq + j], op);
+        for (int j = 0; j < 16; ++j) op = fmaf(sf[Cf::F_S + tk_off(ar, 16 * cq + j, 64)], vec[16 * cq + j], op);
         op += __shfl_xor_sync(0xffffffffu, op, 1);
         op += __shfl_xor_sync(0xffffffffu, op, 2);
-        if (cq == 0) go[st * D + row] = from_f32<TIO>(op * misc[Cf::M_RDEN + t]);
+        if (cq == 0) go[st * D + ar] = from_f32<TIO>(op * misc[Cf::M_RDEN + t]);
         __syncthreads();
       }
       pos += c;
       continue;
     }
-    // ---------------- Linv = L^{-1} (unit lower), 4 threads per column, into the L tile
+    // ---------------- Linv -> hi / lo operand tiles
     {
-      const int acol = tid >> 2, sub = tid & 3;   // column a, rows 16 sub .. 16 sub + 15
-      float x[16];
+      const float* Xp = XB;
+      // Linv (rows l, K = j) -> hi (L tile) + lo (Q tile 0); [W; H^T] -> hi in place + lo (P tiles)
+      float lv[4][4];
+      int loff[4];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) x[j] = (16 * sub + j == acol) ? 1.f : 0.f;
+      for (int s = 0; s < 4; ++s) {
+        const int f = tid + NT * s;
+        const int l = (f >> 7) * 8 + (f & 7), j4 = ((f >> 3) & 15) * 4;
+        const int bi = l >> 4, bj = j4 >> 4;
+        loff[s] = tk_off(l, j4, 64);
 #pragma unroll
-      for (int bb = 0; bb < 4; ++bb) {
-#pragma unroll
-        for (int jb = 0; jb < 16; ++jb) {
-          const int b = 16 * bb + jb;
-          // x_b (held by the thread with sub == bb) is final: take it out of the rows below
-          const float xb = __shfl_sync(0xffffffffu, x[jb], (lane & ~3) | bb);
-          if (b >= acol && b < 63) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int l = 16 * sub + j;
-              if (l > b) x[j] = fmaf(-Gs[l * GLD + b], xb, x[j]);
-            }
-          }
-        }
+        for (int m = 0; m < 4; ++m) lv[s][m] = (bi >= bj) ? Xp[pblk(bi, bj) + (l & 15) * 17 + (j4 & 15) + m] : 0.f;
       }
-      __syncthreads();   // every thread is done with the L factor in P
+      __syncthreads();
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int o = tk_off(16 * sub + j, acol, 64);
-        const float h = tf32_hi(x[j]);
-        sf[Cf::F_L + o] = h;
-        sf[Cf::F_P + o] = x[j] - h;   // Linv lo
-      }
-      // W (rows 0..63 of [W; H^T]) -> hi in place, lo into the second P tile
-      for (int e = tid; e < TILE; e += NT) {
-        const float w = sf[Cf::F_R + e];
-        const float h = tf32_hi(w);
-        sf[Cf::F_R + e] = h;
-        sf[Cf::F_P + TILE + e] = w - h;
+      for (int s = 0; s < 4; ++s) st4_split(Cf::F_L + loff[s], Cf::F_Q + loff[s], lv[s]);
+      for (int e4 = tid; e4 < 2 * TILE / 4; e4 += NT) {
+        const float4 x = *reinterpret_cast<const float4*>(sf + Cf::F_R + 4 * e4);
+        const float xv[4] = {x.x, x.y, x.z, x.w};
+        st4_split(Cf::F_R + 4 * e4, Cf::F_P + 4 * e4, xv);
       }
     }
-    // ---------------- G3: [Z^T | F] = Linv [W; H^T]^T  (M 64, N 128, K 64), 3xTF32 on Z
+    // ---------------- G3: [Z; F^T] = [W; H^T] Linv^T  (M 128, N 64, K 64), 3xTF32
     {
-      const int xo[3] = {Cf::F_L, Cf::F_P, Cf::F_L}, yo[3] = {Cf::F_R, Cf::F_R, Cf::F_P + TILE}, nn[3] = {128, 128, 64};
-      if (!gemm_passes(64, 64, 3, xo, yo, nn)) { failed = true; break; }
+      const MmaPass ps[3] = {{Cf::F_R, Cf::F_L, 128, 64, 0, false},
+                             {Cf::F_R, Cf::F_Q, 128, 64, 0, true},
+                             {Cf::F_P, Cf::F_L, 128, 64, 0, true}};
+      if (!mma_run(ps, 3, 64)) { failed = true; break; }
     }
     {
-      // M = 64 result: rows 16 q .. 16 q + 15 in lanes 0..15 of quadrant q.  The
-      // TMEM load is warp-collective: every lane executes it, lanes 16..31 drop it.
       float v[16];
-      const int l = 16 * q4 + (lane & 15);
-      const float idl = misc[Cf::M_ID + l];
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        const int col0 = 64 * half + 16 * cc;
+      for (int cc = 0; cc < 2; ++cc) {
+        const int col0 = 32 * half + 16 * cc;
         tld(col0, v);
-        if (lane >= 16) continue;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int col = col0 + j;
-          if (half == 0) {   // Z^T[l][i]: Z (rows i, K = l) and Z D^{-1} (rows i of [Z/D; E^T]), hi + lo
-            const int oz = tk_off(col, l, 64);
-            const float z = v[j], zh = tf32_hi(z), zd = z * idl, zdh = tf32_hi(zd);
-            sf[Cf::F_Q + oz] = zh;
-            sf[Cf::F_L + oz] = z - zh;
-            sf[Cf::F_P + oz] = zdh;
-            sf[Cf::F_R + oz] = zd - zdh;
-          } else {           // F[l][t] -> E^T[t][l] (rows 64 + t of [Z/D; E^T]), hi + lo
-            const int t = col - 64;
-            if (t < C) {
-              const float e = (l <= (t + 1) * R - 1) ? v[j] * idl : 0.f, eh = tf32_hi(e);
-              const int oe = tk_off(64 + t, l, 64);
-              sf[Cf::F_P + oe] = eh;
-              sf[Cf::F_R + oe] = e - eh;
-            }
+        for (int j = 0; j < 16; j += 4) {
+          const int l = col0 + j;
+          const float id4[4] = {misc[Cf::M_ID + l], misc[Cf::M_ID + l + 1], misc[Cf::M_ID + l + 2],
+                                misc[Cf::M_ID + l + 3]};
+          if (row < 64) {   // Z (rows i, K = l): hi -> L tile, lo -> Q tile 0; Z D^{-1} -> R / P rows i
+            const float zd[4] = {v[j] * id4[0], v[j + 1] * id4[1], v[j + 2] * id4[2], v[j + 3] * id4[3]};
+            st4_split(Cf::F_L + tk_off(row, l, 64), Cf::F_Q + tk_off(row, l, 64), v + j);
+            st4_split(Cf::F_R + tk_off(row, l, 64), Cf::F_P + tk_off(row, l, 64), zd);
+          } else {          // E^T (rows t, K = l), masked to directions of steps <= t
+            const int t = row - 64, lim = (t + 1) * R - 1;
+            float e4[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) e4[m] = (l + m <= lim) ? v[j + m] * id4[m] : 0.f;
+            st4_split(Cf::F_R + tk_off(row, l, 64), Cf::F_P + tk_off(row, l, 64), e4);
           }
         }
       }
     }
     // ---------------- G4: [Z D^{-1} Z^T ; (Z E)^T] = [Z/D; E^T] Z^T  (M 128, N 64, K 64), 3xTF32
     {
-      const int xo[3] = {Cf::F_P, Cf::F_R, Cf::F_P}, yo[3] = {Cf::F_Q, Cf::F_Q, Cf::F_L}, nn[3] = {64, 64, 64};
-      if (!gemm_passes(128, 64, 3, xo, yo, nn)) { failed = true; break; }
+      const MmaPass ps[3] = {{Cf::F_R, Cf::F_L, 128, 64, 0, false},
+                             {Cf::F_P, Cf::F_L, 128, 64, 0, true},
+                             {Cf::F_R, Cf::F_Q, 128, 64, 0, true}};
+      if (!mma_run(ps, 3, 64)) { failed = true; break; }
     }
     {
       float v[16];
-      const int row = 32 * q4 + lane;
+      float an = 0.f;
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int col0 = 32 * half + 16 * cc;
         tld(col0, v);
         if (row < 64) {   // A_1 = A_0 - Z D^{-1} Z^T (+ eps_n I at a nudge)
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            float& ar = sf[Cf::F_A + tk_off(row, col0 + j, 64)];
-            ar = ar - v[j] + ((nudge && row == col0 + j) ? a.eps_n : 0.f);
+          for (int j = 0; j < 16; j += 4) {
+            float4* ap = reinterpret_cast<float4*>(sf + Cf::F_A + tk_off(row, col0 + j, 64));
+            float4 x = *ap;
+            x.x -= v[j];
+            x.y -= v[j + 1];
+            x.z -= v[j + 2];
+            x.w -= v[j + 3];
+            if (nudge && (row >> 2) == ((col0 + j) >> 2)) {
+              const int dg = row & 3;
+              if (dg == 0) x.x += a.eps_n;
+              if (dg == 1) x.y += a.eps_n;
+              if (dg == 2) x.z += a.eps_n;
+              if (dg == 3) x.w += a.eps_n;
+            }
+            *ap = x;
           }
         } else {          // alpha_t = Q_t - (Z E)_t (+ eps_n s_t at a nudge step)
           const int t = row - 64;
+          float al[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int col = col0 + j;
-            float al = 0.f;
+            float x = 0.f;
             if (t < c) {
-              al = sf[Cf::F_Q + TILE + tk_off(t, col, 64)] - v[j];
-              if (nudge && t == c - 1) al = fmaf(a.eps_n, misc[Cf::M_SL + col], al);
+              x = sf[Cf::F_Q + tk_off(64 + t, col, 64)] - v[j];
+              if (nudge && t == c - 1) x = fmaf(a.eps_n, misc[Cf::M_SL + col], x);
             }
-            sf[Cf::F_AL + tk_off(t, col, 64)] = al;
-            if (t < C) sf[Cf::F_T6 + 2 * Cf::T6T + tk_off(col, t, C)] = al;   // alpha^T (rows j, K = t)
+            al[j] = x;
+            an = fmaf(x, x, an);
+          }
+#pragma unroll
+          for (int j = 0; j < 16; j += 4) st4(Cf::F_AL + tk_off(t, col0 + j, 64), al[j], al[j + 1], al[j + 2], al[j + 3]);
+          if (t < C) {
+            // alpha^T (rows j, K = t): lane group g = lane / 4 writes column col0 + ((jj + g) & 15) in
+            // store jj, so the 8 groups hit 8 different core-matrix rows (32 distinct banks)
+            const int g = (lane >> 2) & 7;
+            if (g & 1) {
+              const float f0 = al[0];
+#pragma unroll
+              for (int m = 0; m < 15; ++m) al[m] = al[m + 1];
+              al[15] = f0;
+            }
+            if (g & 2) {
+              const float f0 = al[0], f1 = al[1];
+#pragma unroll
+              for (int m = 0; m < 14; ++m) al[m] = al[m + 2];
+              al[14] = f0;
+              al[15] = f1;
+            }
+            if (g & 4) {
+              float f[4];
+#pragma unroll
+              for (int m = 0; m < 4; ++m) f[m] = al[m];
+#pragma unroll
+              for (int m = 0; m < 12; ++m) al[m] = al[m + 4];
+#pragma unroll
+              for (int m = 0; m < 4; ++m) al[12 + m] = f[m];
+            }
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj)
+              sf[Cf::F_T6 + 2 * Cf::T6T + tk_off(col0 + ((jj + g) & 15), t, C)] = al[jj];
           }
         }
       }
-      // V^T (rows i, K = t) for G6
+      if (row >= 64) misc[Cf::M_AN2 + 64 * half + (row - 64)] = an;   // |alpha_t|^2, two halves
+      // V^T (rows i, K = t) for G6: lanes cover 8 rows x 4 steps of one core matrix
       for (int e = tid; e < 64 * C; e += NT) {
-        const int t = e >> 6, i = e & 63;
+        const int i = ((e >> 5) & 7) * 8 + ((e >> 2) & 7), t = (e >> 8) * 4 + (e & 3);
         sf[Cf::F_T6 + Cf::T6T + tk_off(i, t, C)] = to_f32(vb[t * 64 + i]);
       }
     }
     // ---------------- G5: [S alpha ; S phi(q) | alpha.alpha ; phi(q).alpha] = [alpha; phi(q)] [S; alpha]^T
-    if (!gemm(Cf::F_AL, Cf::F_S, 128, 128, 64)) { failed = true; break; }
     {
+      const MmaPass ps[1] = {{Cf::F_AL, Cf::F_S, 128, 128, 0, false}};
+      if (!mma_run(ps, 1, 64)) { failed = true; break; }
+    }
+    if (row >= 64) {   // warp-uniform: quadrants 2, 3 (rows 64 + t)
       float v[16];
-      const int row = 32 * q4 + lane;
-      float xs = 0.f;
+      const int t = row - 64;
+      if (half == 0) {   // Y_t[i] = (S phi(q_t))[i] -> staging in P
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        const int col0 = 64 * half + 16 * cc;
-        tld(col0, v);
+        for (int cc = 0; cc < 4; ++cc) {
+          tld(16 * cc, v);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int col = col0 + j;
-          if (row < 64) {
-            const int t = row;
-            if (half == 0) {          // (S alpha_t)[i] -> v_t . S alpha_t
-              if (t < c) xs = fmaf(to_f32(vb[t * 64 + col]), v[j], xs);
-            } else {                  // alpha_t . alpha_t'
-              const int tp = col - 64;
-              if (tp < C && t < C) sf[Cf::F_Q + t * C + tp] = v[j];
-              if (tp == t) misc[Cf::M_AN + t] = v[j];
-            }
-          } else {
-            const int t = row - 64;
-            if (half == 0) {          // Y_t[i] = (S phi(q_t))[i]
-              if (t < C) sf[Cf::F_P + t * 64 + col] = v[j];
-            } else {                  // aq[t][t'] = phi(q_t) . alpha_t', t' <= t
-              const int tp = col - 64;
-              if (t < C && tp < C) sf[Cf::F_T6 + tk_off(t, tp, C)] = (tp <= t && t < c) ? v[j] : 0.f;
+          for (int j = 0; j < 16; ++j) sf[Cf::F_P + t * YLD + 16 * cc + j] = v[j];
+        }
+      } else {           // aq[t][t'] = phi(q_t) . alpha_t', t' <= t -> tril(aq) rows t of T6
+#pragma unroll
+        for (int cc = 0; cc < (C + 15) / 16; ++cc) {
+          tld(64 + 16 * cc, v);
+          if (t < C) {
+#pragma unroll
+            for (int j = 0; j < 16; j += 4) {
+              const int tp = 16 * cc + j;
+              float x[4];
+#pragma unroll
+              for (int m = 0; m < 4; ++m) x[m] = (tp + m <= t && t < c) ? v[j + m] : 0.f;
+              if (tp < C) st4(Cf::F_T6 + tk_off(t, tp, C), x[0], x[1], x[2], x[3]);
             }
           }
         }
       }
-      if (row < 64 && half == 0) misc[Cf::M_XS + row] = xs;
     }
-    // ||S||^2 and the renormalisation decisions
+    // ||S||^2, the bound and the renormalisation decisions
     {
-      float sq = 0.f;
-      for (int e = tid; e < D * D; e += NT) {
-        const float x = sf[Cf::F_S + e];   // every element of the tile, in tile order
-        sq = fmaf(x, x, sq);
+      float sq = 0.f, bsum = 0.f;
+      for (int e4 = tid; e4 < TILE / 4; e4 += NT) {
+        const float4 x = *reinterpret_cast<const float4*>(sf + Cf::F_S + 4 * e4);
+        sq = fmaf(x.x, x.x, fmaf(x.y, x.y, fmaf(x.z, x.z, fmaf(x.w, x.w, sq))));
       }
-      const float ns = block_sum(sq);      // contains __syncthreads: D5 drain writes are visible
-      float bound = sqrtf(ns);
-      for (int t = 0; t < c; ++t) bound = fmaf(misc[Cf::M_VN + t], sqrtf(fmaxf(misc[Cf::M_AN + t], 0.f)), bound);
-      const bool exact = !(bound <= a.tau * (1.f - 0x1p-12f));
+      __syncthreads();   // the |alpha_t|^2 halves from the G4 drain
+      if (tid < c) {
+        const float an = misc[Cf::M_AN2 + tid] + misc[Cf::M_AN2 + 64 + tid];
+        misc[Cf::M_AN + tid] = an;
+        bsum = misc[Cf::M_VN + tid] * sqrtf(fmaxf(an, 0.f));
+      }
+      block_sum2(sq, bsum);   // contains __syncthreads: the drain writes above are visible
+      const float ns = sq;
+      const bool exact = !(sqrtf(ns) + bsum <= a.tau * (1.f - 0x1p-12f));
       if (!exact) {
         if (tid < 64) {
           misc[Cf::M_SG + tid] = 1.f;   // sigma after step t
           misc[Cf::M_IS + tid] = 1.f;   // 1 / sigma before step t
         }
       } else {
+        // v_t . S alpha_t and the alpha Gram from the G5 result still in TMEM (rows t < 64)
+        if (row < 64) {
+          float v[16];
+          const int t = row;
+          if (half == 0) {
+            float xs = 0.f;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+              tld(16 * cc, v);
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (t < c) xs = fmaf(to_f32(vb[t * 64 + 16 * cc + j]), v[j], xs);
+            }
+            misc[Cf::M_XS + t] = xs;
+          } else {
+#pragma unroll
+            for (int cc = 0; cc < (C + 15) / 16; ++cc) {
+              tld(64 + 16 * cc, v);
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const int tp = 16 * cc + j;
+                if (tp < C && t < C) sf[Cf::F_Q + tp * C + t] = v[j];   // alpha_t' . alpha_t (symmetric)
+              }
+            }
+          }
+        }
         float* VV = sf + Cf::F_Q + TILE;   // v_t . v_t' for t, t' < c  ([C][C])
         for (int e = tid; e < C * C; e += NT) {
           const int t = e / C, tp = e - t * C;
@@ -719,32 +921,32 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
         __syncthreads();
         if (misc[Cf::M_SCAL] != 0.f) {
           // S and the outputs step by step with the chunk's alpha (A and alpha are final)
-          const int row = tid >> 2, cq = tid & 3;
+          const int ar = tid >> 2, cq = tid & 3;
           for (int t = 0; t < c; ++t) {
-            const float vr = to_f32(vb[t * 64 + row]);
-            float sq = 0.f;
+            const float vr = to_f32(vb[t * 64 + ar]);
+            float sq2 = 0.f;
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const int col = 16 * cq + j;
-              float& sr = sf[Cf::F_S + tk_off(row, col, 64)];
+              float& sr = sf[Cf::F_S + tk_off(ar, col, 64)];
               sr = fmaf(vr, sf[Cf::F_AL + tk_off(t, col, 64)], sr);
-              sq = fmaf(sr, sr, sq);
+              sq2 = fmaf(sr, sr, sq2);
             }
-            const float nrm = sqrtf(block_sum(sq));
+            const float nrm = sqrtf(block_sum(sq2));
             if (nrm > a.tau) {
               const float cf = a.tau / nrm;
 #pragma unroll
-              for (int j = 0; j < 16; ++j) sf[Cf::F_S + tk_off(row, 16 * cq + j, 64)] *= cf;
+              for (int j = 0; j < 16; ++j) sf[Cf::F_S + tk_off(ar, 16 * cq + j, 64)] *= cf;
               if (tid == 0) ++renorm_cnt;
             }
             if (!isfinite(nrm)) flags |= kStatusNonfinite;
             float op = 0.f;   // o_t = S_t phi(q_t) / den_t (the thread's own S elements)
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-              op = fmaf(sf[Cf::F_S + tk_off(row, 16 * cq + j, 64)], sf[Cf::F_PQ + tk_off(t, 16 * cq + j, 64)], op);
+              op = fmaf(sf[Cf::F_S + tk_off(ar, 16 * cq + j, 64)], sf[Cf::F_PQ + tk_off(t, 16 * cq + j, 64)], op);
             op += __shfl_xor_sync(0xffffffffu, op, 1);
             op += __shfl_xor_sync(0xffffffffu, op, 2);
-            if (cq == 0) go[(pos + t) * D + row] = from_f32<TIO>(op * misc[Cf::M_RDEN + t]);
+            if (cq == 0) go[(pos + t) * D + ar] = from_f32<TIO>(op * misc[Cf::M_RDEN + t]);
           }
           tc::fence_before_sync();
           __syncthreads();
@@ -761,35 +963,48 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
       }
     }
     // ---------------- G6: [tril(aq) V ; V^T alpha] = [tril(aq); V^T] [V^T; alpha^T]^T  (M 128, N 128, K C)
-    if (!gemm(Cf::F_T6, Cf::F_T6 + Cf::T6T, 128, 128, C)) { failed = true; break; }
+    {
+      const MmaPass ps[1] = {{Cf::F_T6, Cf::F_T6 + Cf::T6T, 128, 128, 0, false}};
+      if (!mma_run(ps, 1, C)) { failed = true; break; }
+    }
     {
       float v[16];
-      const int row = 32 * q4 + lane;
-      const float sgl = misc[Cf::M_SG + c - 1];
+      if (row < 64 && half == 0) {   // outputs of step t (warp-uniform)
+        const int t = row;
+        const float sgt = misc[Cf::M_SG + t], rd = misc[Cf::M_RDEN + t];
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        const int col0 = 64 * half + 16 * cc;
-        if ((row < 64) != (half == 0)) continue;   // only the two useful blocks
-        tld(col0, v);
-        if (row < 64) {   // outputs of step t
-          const int t = row;
+        for (int cc = 0; cc < 4; ++cc) {
+          tld(16 * cc, v);
           if (t < c) {
-            const float sgt = misc[Cf::M_SG + t], rd = misc[Cf::M_RDEN + t];
+            uint32_t pk[8];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int i = col0 + j;
-              const float o = sgt * (sf[Cf::F_P + t * 64 + i] + v[j]) * rd;
-              if (!isfinite(o)) flags |= kStatusNonfinite;
-              go[(pos + t) * D + i] = from_f32<TIO>(o);
+            for (int j = 0; j < 16; j += 2) {
+              const float o0 = sgt * (sf[Cf::F_P + t * YLD + 16 * cc + j] + v[j]) * rd;
+              const float o1 = sgt * (sf[Cf::F_P + t * YLD + 16 * cc + j + 1] + v[j + 1]) * rd;
+              if (!isfinite(o0) || !isfinite(o1)) flags |= kStatusNonfinite;
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(o0, o1);
+              pk[j / 2] = *reinterpret_cast<const uint32_t*>(&b2);
             }
+            uint4* dst = reinterpret_cast<uint4*>(go + (pos + t) * D + 16 * cc);
+            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
           }
-        } else {          // S_1 = sigma (S + V^T alpha)
-          const int i = row - 64;
+        }
+      } else if (row >= 64 && half == 1) {   // S_1 = sigma (S + V^T alpha)
+        const int i = row - 64;
+        const float sgl = misc[Cf::M_SG + c - 1];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int col = col0 - 64 + j;
-            float& sr = sf[Cf::F_S + tk_off(i, col, 64)];
-            sr = sgl * (sr + v[j]);
+        for (int cc = 0; cc < 4; ++cc) {
+          tld(64 + 16 * cc, v);
+#pragma unroll
+          for (int j = 0; j < 16; j += 4) {
+            float4* sp = reinterpret_cast<float4*>(sf + Cf::F_S + tk_off(i, 16 * cc + j, 64));
+            float4 x = *sp;
+            x.x = sgl * (x.x + v[j]);
+            x.y = sgl * (x.y + v[j + 1]);
+            x.z = sgl * (x.z + v[j + 2]);
+            x.w = sgl * (x.w + v[j + 3]);
+            *sp = x;
           }
         }
       }
@@ -808,7 +1023,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
       gA[e] = sf[Cf::F_A + tk_off(i, j, 64)];
       gS[e] = sf[Cf::F_S + tk_off(i, j, 64)];
     }
-    if (tid < D) gn[tid] = n_i;
+    if (tid < D) gn[tid] = misc[Cf::M_N + tid];
   } else if (tid == 0) {
     flags |= kStatusTimeout;
     if (loaded + 1 < ntiles) (void)mbar_wait_bounded(in_bar, (uint32_t)((loaded + 1) & 1));

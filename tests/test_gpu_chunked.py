@@ -95,3 +95,15 @@ def test_chunked_rejects_shapes_it_does_not_build():
     x = workloads.gaussian_inputs(1, 8, 16, 16, 1, "bf16", seed=3)
     with pytest.raises(vla.VlaError, match="UNSUPPORTED"):
         gpu_scan(x, 1, 1, mode="chunked", P=0, eps_n=0.0, tau=1e4)
+
+
+def test_chunked_needs_aligned_o():
+    import sherman_morrison_inverse_gb300 as vla
+    x = workloads.gaussian_inputs(1, 8, 64, 64, 1, "bf16", seed=4)
+    q, k, v = (x[n].reshape(1, 1, 8, 64).cuda() for n in ("q", "k", "v"))
+    u = x["u"].reshape(1, 1, 8, 1, 64).cuda()
+    A, S, n = x["A0"].reshape(1, 1, 64, 64).cuda(), x["S0"].reshape(1, 1, 64, 64).cuda(), x["n0"].reshape(1, 1, 64).cuda()
+    buf = torch.empty(8 * 64 + 8, dtype=torch.bfloat16, device="cuda")
+    o = buf[1:1 + 8 * 64].view(1, 1, 8, 64)   # 2-byte offset
+    with pytest.raises(vla.VlaError, match="INVALID_ARG"):
+        vla.scan_fwd(q, k, v, u, A, S, n, o, P=0, eps_n=0.0, tau=1e4, mode="chunked")
