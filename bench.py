@@ -9,6 +9,11 @@ associative-recall-shaped keys); its inputs (1.07 GB) exceed the 129 MB L2, so
 no flush is needed between steps.  Successive steps continue the same streams
 (t0 advances by T), so every step does identical work on resident inputs.
 
+The scan runs in the chunked tensor-core kernel where it is built (d = d_v =
+64, bfloat16 I/O, r = 1 or 4; ``--mode auto``, the default) and in the
+sequential CUDA-core kernel otherwise; ``--mode`` picks one explicitly.  Both
+pass the same parity tests against the oracle.
+
 Prints one JSON line (rank 0).  ``--impl reference`` times the float64 CPU
 oracle instead (the only reference this method has), on a bounded sample.
 """
@@ -228,7 +233,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="2", help="index or name of the workload")
-    ap.add_argument("--mode", choices=["sequential", "chunked"], default="sequential")
+    ap.add_argument("--mode", choices=["auto", "sequential", "chunked"], default="auto",
+                    help="auto: the chunked tensor-core kernel where it is built (d = d_v = 64, bf16 I/O, "
+                         "r = 1 or 4), else the sequential one")
     ap.add_argument("--chunk", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=None)
@@ -240,6 +247,8 @@ def main():
     if args.T is not None:
         w = w.with_(T=args.T)
 
+    if args.mode == "auto":
+        args.mode = "chunked" if (w.d == 64 and w.dv == 64 and w.io == "bf16" and w.r in (1, 4)) else "sequential"
     if args.impl == "reference":
         run_reference(args, w)
         return

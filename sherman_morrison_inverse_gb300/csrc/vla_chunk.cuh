@@ -8,14 +8,15 @@
 // chunk with directions U (rows u_a), s-vectors Sigma (rows s_t) and A_0 = the
 // inverse at its start:
 //
-//   G1  [W^T; Q^T] = [U; Sigma] A_0^T,  W = A_0 U^T     W = A_0 U, Q = A_0 Sigma (two MMAs)
+//   G1  [W^T; Q^T] = [U; Sigma] A_0^T                    W = A_0 U, Q = A_0 Sigma
 //   G2  [G - I; H^T] = [W^T; Q^T] U^T                    G = I + U^T A_0 U, H = U^T Q
 //       G = L D L^T (CUDA cores; D_jj are the sequential deltas), Linv = L^{-1}
 //   G3  [Z; F^T] = [W; H^T] Linv^T                       Z = W L^{-T} (the sequential z's), F = Linv H
 //       E = D^{-1} F, masked to directions of steps <= t
 //   G4  [Z D^{-1} Z^T ; (Z E)^T] = [Z D^{-1}; E^T] Z^T   A_1 = A_0 - Z D^{-1} Z^T,  alpha = Q - Z E
 //   G5  [S alpha_t, alpha.alpha ; S phi(q_t), phi(q_t).alpha] = [alpha; Phi_q] [S; alpha]^T
-//   G6  [tril(aq) V ; V^T alpha]   = [tril(aq); V^T] [V^T; alpha^T]^T
+//   G6  [. ; tril(aq) V] += [V^T; tril(aq)] (V^T)^T     onto G5's S phi(q_t) rows, still in TMEM
+//       [V^T alpha ; .]   = [V^T; tril(aq)] (alpha^T)^T
 //       o_t = (S phi(q_t) + sum_{t'<=t} (alpha_t'.phi(q_t)) v_t') / den_t,   S_1 = S + V^T alpha
 //
 // Every product is arranged so that its TMEM drain (lane = row of the result)
@@ -55,12 +56,12 @@ constexpr int D = 64;
 constexpr int NT = 256;
 constexpr int TILE = 64 * 64;         // floats of a TK(64, 64) operand tile
 constexpr int GLD = 65;               // leading dimension of the fp32 G / L staging
-constexpr int YLD = 65;               // leading dimension of the S phi(q) staging
 constexpr int PLD = 68;               // leading dimension of the prologue's phi(k) / phi(q) scratch
 constexpr int BLK = 272;              // floats per packed 16 x 16 block (leading dimension 17)
 constexpr float kGuardEps = 1e-6f;
 constexpr float kReadoutEps = 1e-6f;
 constexpr float kInvSqrtD = 0.125f;
+constexpr uint32_t kTmemCols = 256;   // 0..127: the products; 128..191: V^T alpha of G6
 
 // High part of a 3xTF32 split: the value with the low 13 mantissa bits cleared
 // (exactly representable in tf32); the low part is x - hi.
@@ -88,14 +89,15 @@ struct Cfg {
   static constexpr int F_AL = F_S + TILE;                 // alpha   }
   static constexpr int F_PQ = F_AL + TILE;                // phi(q)  }
   static constexpr int F_P = F_PQ + TILE;                 // 2 tiles: [U; Sigma] -> G/L staging -> [W; H^T] lo
-                                                          //          -> [Z/D; E^T] lo -> S phi(q) staging
+                                                          //          -> [Z/D; E^T] lo
   static constexpr int F_Q = F_P + 2 * TILE;              // 2 tiles: [W^T; Q^T]; tile 0 -> L^{-1} blocks ->
                                                           //          Linv lo -> Z lo -> alpha Gram; tile 1 -> v Gram
   static constexpr int F_R = F_Q + 2 * TILE;              // 2 tiles: prologue scratch -> A hi/lo -> [W; H^T] (hi)
                                                           //          -> [Z/D; E^T] hi -> T6
   static constexpr int F_L = F_R + 2 * TILE;              // 1 tile:  prologue scratch -> products of the Linv
                                                           //          assembly -> Linv hi -> Z hi -> T6 (alpha^T)
-  static constexpr int F_T6 = F_R;                        // [tril(aq)][V^T][alpha^T], TK(64, C) each
+  static constexpr int F_T6 = F_R;                        // [V^T][tril(aq)][alpha^T], TK(64, C) each
+  static constexpr int T6_V = 0, T6_Q = T6T, T6_A = 2 * T6T;
   static constexpr int F_MISC = F_L + TILE;
   // misc block
   static constexpr int M_D = 0, M_ID = 64, M_RDEN = 128, M_VN = 192, M_SL = 256, M_XS = 320, M_AN = 384;
@@ -107,7 +109,7 @@ struct Cfg {
   static constexpr size_t bar_off = STAGE_PAD + (float_bytes + 15) / 16 * 16;
   static constexpr size_t bytes = bar_off + 64;
   static_assert(3 * T6T <= 3 * TILE, "T6 fits in R and L");
-  static_assert(64 * GLD <= 2 * TILE && 64 * YLD <= 2 * TILE, "stagings fit in P");
+  static_assert(64 * GLD <= 2 * TILE, "staging fits in P");
   static_assert(2 * C * PLD <= 3 * TILE, "prologue scratch fits in R and L");
   static_assert(pblk(3, 3) + BLK <= TILE, "packed blocks fit in one tile");
   static_assert(bytes <= 227 * 1024, "shared memory");
@@ -164,7 +166,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     fence_mbar_init();
     *flag = 0;
   }
-  if (warp == 0) tc::tmem_alloc(tslot, 128);
+  if (warp == 0) tc::tmem_alloc(tslot, kTmemCols);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -227,6 +229,34 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     const float h0 = tf32_hi(x[0]), h1 = tf32_hi(x[1]), h2 = tf32_hi(x[2]), h3 = tf32_hi(x[3]);
     st4(off_hi, h0, h1, h2, h3);
     st4(off_lo, x[0] - h0, x[1] - h1, x[2] - h2, x[3] - h3);
+  };
+
+  // x[jj] <- x[(jj + g) & 15]: with g = (lane / 4) % 8, store jj of a transposed write then
+  // goes to column (jj + g) & 15 and the 8 lane groups hit 8 different core-matrix rows
+  // (32 distinct banks)
+  auto rot16 = [](float (&x)[16], int g) {
+    if (g & 1) {
+      const float f0 = x[0];
+#pragma unroll
+      for (int m = 0; m < 15; ++m) x[m] = x[m + 1];
+      x[15] = f0;
+    }
+    if (g & 2) {
+      const float f0 = x[0], f1 = x[1];
+#pragma unroll
+      for (int m = 0; m < 14; ++m) x[m] = x[m + 2];
+      x[14] = f0;
+      x[15] = f1;
+    }
+    if (g & 4) {
+      float f[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) f[m] = x[m];
+#pragma unroll
+      for (int m = 0; m < 12; ++m) x[m] = x[m + 4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) x[12 + m] = f[m];
+    }
   };
 
   // block reduction of two floats over the CTA (all threads call it)
@@ -398,31 +428,25 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
       }
     }
 
-    // ---------------- G1: [W^T; Q^T] = [U; Sigma] A_0^T (cols 0..63), W = A_0 U^T (cols 64..127, M 64)
+    // ---------------- G1: [W^T; Q^T] = [U; Sigma] A_0^T  (M 128, N 64, K 64), A_0 hi + lo
     {
-      const MmaPass ps[4] = {{Cf::F_P, Cf::F_R, 128, 64, 0, false},
-                             {Cf::F_P, Cf::F_R + TILE, 128, 64, 0, true},
-                             {Cf::F_R, Cf::F_P, 64, 64, 64, false},
-                             {Cf::F_R + TILE, Cf::F_P, 64, 64, 64, true}};
-      if (!mma_run(ps, 4, 64)) { failed = true; break; }
+      const MmaPass ps[2] = {{Cf::F_P, Cf::F_R, 128, 64, 0, false},
+                             {Cf::F_P, Cf::F_R + TILE, 128, 64, 0, true}};
+      if (!mma_run(ps, 2, 64)) { failed = true; break; }
     }
     {
       float v[16];
+      const int g = (lane >> 2) & 7;
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {   // [W^T; Q^T] -> Q tiles (X of G2)
+      for (int cc = 0; cc < 2; ++cc) {   // [W^T; Q^T] -> Q tiles (X of G2); W (rows i) fp32 -> R tile 0
         const int col0 = 32 * half + 16 * cc;
         tld(col0, v);
 #pragma unroll
         for (int j = 0; j < 16; j += 4) st4(Cf::F_Q + tk_off(row, col0 + j, 64), v[j], v[j + 1], v[j + 2], v[j + 3]);
-      }
-      const int wi = 16 * q4 + (lane & 15);   // M = 64 result: row wi in lane 32 q4 + wi % 16
+        if (row < 64) {   // W[i][a] = W^T[a][i], a = row (warp-uniform)
+          rot16(v, g);
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {   // W (rows i) fp32 -> R tile 0
-        const int col0 = 32 * half + 16 * cc;
-        tld(64 + col0, v);
-        if (lane < 16) {
-#pragma unroll
-          for (int j = 0; j < 16; j += 4) st4(Cf::F_R + tk_off(wi, col0 + j, 64), v[j], v[j + 1], v[j + 2], v[j + 3]);
+          for (int jj = 0; jj < 16; ++jj) sf[Cf::F_R + tk_off(col0 + ((jj + g) & 15), row, 64)] = v[jj];
         }
       }
     }
@@ -452,18 +476,77 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
 
     // ---------------- LDL^T of G and X = L^{-1} in 16 x 16 blocks (fp32)
     // Right-looking block LDL^T with the inverse carried along as a forward
-    // elimination of the identity: for block column k,
+    // elimination of the identity.  For block column k:
     //   [a] one warp factors the diagonal block G'_kk = L_kk D_k L_kk^T in registers;
     //   [b] 64 independent forward substitutions with L_kk, one per thread: the columns
     //       of X_kk = L_kk^{-1}, the panel rows (L D)_r = L_kk^{-1} G'_rk (i > k) and the
     //       columns of X_kj = L_kk^{-1} B_kj (j < k);
     //   [c] trailing G'_ij -= L_ik D_k L_jk^T (k < j <= i) and B_ij -= L_ik X_kj (j <= k < i),
     // where B is the identity being eliminated (B_ij = 0 for i != j at the start).
+    // [c] of step k runs beside [a] of step k + 1: warp 0 updates the next diagonal
+    // block itself and factors it while the other warps update the remaining blocks.
     // L D (the panel before D^{-1}) is kept, transposed, in the unused upper blocks of the staging.
     float* XB = sf + Cf::F_Q;   // packed blocks: B, then X = L^{-1}
+    // a 2 x 4 tile of [c] for step kc: block blk in the order (trailing blocks, B blocks),
+    // rows 2 rr, 2 rr + 1 and columns 4 cc .. 4 cc + 3 of the block
+    auto trail_tile = [&](int kc, int blk, int rr, int cc) {
+      const int ntr = (3 - kc) * (4 - kc) / 2;
+      const float* lrow;   // L_ik rows (16 values each, stride GLD)
+      const float* xcol;   // columns of (L D)^T_jk or X_kj, row stride sx
+      float* dst;          // destination rows, stride sd
+      int sx, sd;
+      bool fresh = false;
+      if (blk < ntr) {
+        int bi = kc + 1, cnt = blk;   // blk -> (bi, bj) over the lower block triangle of kc+1..3
+#pragma unroll
+        for (int q = 0; q < 6; ++q)
+          if (cnt > bi - (kc + 1)) { cnt -= bi - kc; ++bi; }
+        const int gr = 16 * bi + 2 * rr, gc = 16 * (kc + 1 + cnt) + 4 * cc;
+        lrow = Gs + gr * GLD + 16 * kc;
+        xcol = Gs + 16 * kc * GLD + gc;
+        sx = GLD;
+        dst = Gs + gr * GLD + gc;
+        sd = GLD;
+      } else {
+        const int b2 = blk - ntr, bi = kc + 1 + b2 / (kc + 1), bj = b2 % (kc + 1);
+        lrow = Gs + (16 * bi + 2 * rr) * GLD + 16 * kc;
+        xcol = XB + pblk(kc, bj) + 4 * cc;
+        sx = 17;
+        dst = XB + pblk(bi, bj) + 2 * rr * 17 + 4 * cc;
+        sd = 17;
+        fresh = (kc == bj);   // B_ij starts at 0
+      }
+      float acc[2][4];
+#pragma unroll
+      for (int a2 = 0; a2 < 2; ++a2)
+#pragma unroll
+        for (int b4 = 0; b4 < 4; ++b4) acc[a2][b4] = 0.f;
+#pragma unroll
+      for (int m = 0; m < 16; ++m) {
+        const float l0 = lrow[m], l1 = lrow[GLD + m];
+#pragma unroll
+        for (int b4 = 0; b4 < 4; ++b4) {
+          const float x = xcol[m * sx + b4];
+          acc[0][b4] = fmaf(l0, x, acc[0][b4]);
+          acc[1][b4] = fmaf(l1, x, acc[1][b4]);
+        }
+      }
+#pragma unroll
+      for (int a2 = 0; a2 < 2; ++a2)
+#pragma unroll
+        for (int b4 = 0; b4 < 4; ++b4) {
+          float& dv = dst[a2 * sd + b4];
+          dv = (fresh ? 0.f : dv) - acc[a2][b4];
+        }
+    };
 #pragma unroll 1
     for (int k = 0; k < 4; ++k) {
-      if (warp == 0) {   // [a]: lane i (both half-warps) holds row i of G'_kk
+      if (warp == 0) {
+        if (k > 0) {   // step k-1's update of diagonal block k (block 0 of the trailing list)
+          trail_tile(k - 1, 0, lane >> 2, lane & 3);
+          __syncwarp();
+        }
+        // [a]: lane i (both half-warps) holds row i of G'_kk
         const int i = lane & 15;
         float g[16];
 #pragma unroll
@@ -487,6 +570,13 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
           for (int j = 0; j < 15; ++j)
             if (j < i) Gs[(16 * k + i) * GLD + 16 * k + j] = g[j];
         }
+      } else if (k > 0 && warp != 4) {   // the rest of step k-1's [c]; warp 4 leaves warp 0's
+                                         // sub-partition to it
+        const int kc = k - 1;
+        const int nblk = (3 - kc) * (4 - kc) / 2 + (3 - kc) * (kc + 1);
+        const int w6 = (warp < 4) ? warp - 1 : warp - 2;   // 0..5
+        for (int q = 32 * w6 + lane; q < 32 * (nblk - 1); q += 6 * 32)
+          trail_tile(kc, 1 + (q >> 5), (q >> 2) & 7, q & 3);
       }
       __syncthreads();
       if (tid < 64) {   // [b]: chain q = tid
@@ -516,7 +606,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
           const int r = 16 * (k + 1) + (tid - 16);
 #pragma unroll
           for (int m = 0; m < 16; ++m) {
-            Gs[(16 * k + m) * GLD + r] = y[m];                          // L D, transposed (upper block)
+            Gs[(16 * k + m) * GLD + r] = y[m];                               // L D, transposed (upper block)
             Gs[r * GLD + 16 * k + m] = y[m] * misc[Cf::M_ID + 16 * k + m];   // L
           }
         } else {
@@ -526,50 +616,8 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
         }
       }
       __syncthreads();
-      if (k < 3) {
-        // [c]: trailing blocks (bi, bj), k < bj <= bi, then B blocks (bi, bj), bj <= k < bi
-        constexpr int NTR = 6;                     // largest count of trailing blocks (k = 0)
-        const int ntr = (3 - k) * (4 - k) / 2, nb = (3 - k) * (k + 1);
-        for (int e = tid; e < (ntr + nb) * 256; e += NT) {
-          const int blk = e >> 8, r = (e >> 4) & 15, cl = e & 15;
-          const float* lrow;   // L_ik row r (16 values)
-          const float* xcol;   // column cl of (L D)^T_jk or X_kj, stride sx
-          float* dst;
-          float acc;
-          int sx;
-          if (blk < ntr) {
-            // blk -> (bi, bj) over the lower block triangle of rows/columns k+1..3
-            int bi = k + 1, cnt = blk;
-#pragma unroll
-            for (int q = 0; q < NTR; ++q)
-              if (cnt > bi - (k + 1)) { cnt -= bi - k; ++bi; }
-            const int gr = 16 * bi + r, gc = 16 * (k + 1 + cnt) + cl;
-            lrow = Gs + gr * GLD + 16 * k;
-            xcol = Gs + 16 * k * GLD + gc;
-            sx = GLD;
-            dst = Gs + gr * GLD + gc;
-            acc = *dst;
-          } else {
-            const int b2 = blk - ntr, bi = k + 1 + b2 / (k + 1), bj = b2 % (k + 1);
-            lrow = Gs + (16 * bi + r) * GLD + 16 * k;
-            xcol = XB + pblk(k, bj) + cl;
-            sx = 17;
-            dst = XB + pblk(bi, bj) + r * 17 + cl;
-            acc = (k == bj) ? 0.f : *dst;   // B_ij starts at 0
-          }
-          float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
-#pragma unroll
-          for (int m = 0; m < 16; m += 4) {
-            p0 = fmaf(lrow[m], xcol[m * sx], p0);
-            p1 = fmaf(lrow[m + 1], xcol[(m + 1) * sx], p1);
-            p2 = fmaf(lrow[m + 2], xcol[(m + 2) * sx], p2);
-            p3 = fmaf(lrow[m + 3], xcol[(m + 3) * sx], p3);
-          }
-          *dst = acc - ((p0 + p1) + (p2 + p3));
-        }
-        __syncthreads();
-      }
     }
+    // step 3 has no [c]
     // pivot check: the guard would fire inside the chunk
     int bad = 0;
     if (tid < 64) {
@@ -741,13 +789,18 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
           const int t = row - 64;
           float al[16];
 #pragma unroll
+          for (int j = 0; j < 16; j += 4) {
+            const float4 qv = *reinterpret_cast<const float4*>(sf + Cf::F_Q + tk_off(64 + t, col0 + j, 64));
+            al[j] = qv.x - v[j];
+            al[j + 1] = qv.y - v[j + 1];
+            al[j + 2] = qv.z - v[j + 2];
+            al[j + 3] = qv.w - v[j + 3];
+          }
+#pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const int col = col0 + j;
-            float x = 0.f;
-            if (t < c) {
-              x = sf[Cf::F_Q + tk_off(64 + t, col, 64)] - v[j];
-              if (nudge && t == c - 1) x = fmaf(a.eps_n, misc[Cf::M_SL + col], x);
-            }
+            float x = al[j];
+            if (nudge && t == c - 1) x = fmaf(a.eps_n, misc[Cf::M_SL + col0 + j], x);
+            if (t >= c) x = 0.f;
             al[j] = x;
             an = fmaf(x, x, an);
           }
@@ -757,31 +810,10 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
             // alpha^T (rows j, K = t): lane group g = lane / 4 writes column col0 + ((jj + g) & 15) in
             // store jj, so the 8 groups hit 8 different core-matrix rows (32 distinct banks)
             const int g = (lane >> 2) & 7;
-            if (g & 1) {
-              const float f0 = al[0];
-#pragma unroll
-              for (int m = 0; m < 15; ++m) al[m] = al[m + 1];
-              al[15] = f0;
-            }
-            if (g & 2) {
-              const float f0 = al[0], f1 = al[1];
-#pragma unroll
-              for (int m = 0; m < 14; ++m) al[m] = al[m + 2];
-              al[14] = f0;
-              al[15] = f1;
-            }
-            if (g & 4) {
-              float f[4];
-#pragma unroll
-              for (int m = 0; m < 4; ++m) f[m] = al[m];
-#pragma unroll
-              for (int m = 0; m < 12; ++m) al[m] = al[m + 4];
-#pragma unroll
-              for (int m = 0; m < 4; ++m) al[12 + m] = f[m];
-            }
+            rot16(al, g);
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj)
-              sf[Cf::F_T6 + 2 * Cf::T6T + tk_off(col0 + ((jj + g) & 15), t, C)] = al[jj];
+              sf[Cf::F_T6 + Cf::T6_A + tk_off(col0 + ((jj + g) & 15), t, C)] = al[jj];
           }
         }
       }
@@ -789,7 +821,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
       // V^T (rows i, K = t) for G6: lanes cover 8 rows x 4 steps of one core matrix
       for (int e = tid; e < 64 * C; e += NT) {
         const int i = ((e >> 5) & 7) * 8 + ((e >> 2) & 7), t = (e >> 8) * 4 + (e & 3);
-        sf[Cf::F_T6 + Cf::T6T + tk_off(i, t, C)] = to_f32(vb[t * 64 + i]);
+        sf[Cf::F_T6 + Cf::T6_V + tk_off(i, t, C)] = to_f32(vb[t * 64 + i]);
       }
     }
     // ---------------- G5: [S alpha ; S phi(q) | alpha.alpha ; phi(q).alpha] = [alpha; phi(q)] [S; alpha]^T
@@ -797,29 +829,21 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
       const MmaPass ps[1] = {{Cf::F_AL, Cf::F_S, 128, 128, 0, false}};
       if (!mma_run(ps, 1, 64)) { failed = true; break; }
     }
-    if (row >= 64) {   // warp-uniform: quadrants 2, 3 (rows 64 + t)
+    if (row >= 64) {   // warp-uniform: quadrants 2, 3 (rows 64 + t); S phi(q_t) stays in TMEM for G6
+      // aq[t][t'] = phi(q_t) . alpha_t', t' <= t -> tril(aq) rows t of T6 (16-column pieces by half)
       float v[16];
       const int t = row - 64;
-      if (half == 0) {   // Y_t[i] = (S phi(q_t))[i] -> staging in P
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          tld(16 * cc, v);
+      for (int cc = half; cc < (C + 15) / 16; cc += 2) {
+        tld(64 + 16 * cc, v);
+        if (t < C) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) sf[Cf::F_P + t * YLD + 16 * cc + j] = v[j];
-        }
-      } else {           // aq[t][t'] = phi(q_t) . alpha_t', t' <= t -> tril(aq) rows t of T6
+          for (int j = 0; j < 16; j += 4) {
+            const int tp = 16 * cc + j;
+            float x[4];
 #pragma unroll
-        for (int cc = 0; cc < (C + 15) / 16; ++cc) {
-          tld(64 + 16 * cc, v);
-          if (t < C) {
-#pragma unroll
-            for (int j = 0; j < 16; j += 4) {
-              const int tp = 16 * cc + j;
-              float x[4];
-#pragma unroll
-              for (int m = 0; m < 4; ++m) x[m] = (tp + m <= t && t < c) ? v[j + m] : 0.f;
-              if (tp < C) st4(Cf::F_T6 + tk_off(t, tp, C), x[0], x[1], x[2], x[3]);
-            }
+            for (int m = 0; m < 4; ++m) x[m] = (tp + m <= t && t < c) ? v[j + m] : 0.f;
+            if (tp < C) st4(Cf::F_T6 + Cf::T6_Q + tk_off(t, tp, C), x[0], x[1], x[2], x[3]);
           }
         }
       }
@@ -957,48 +981,51 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
         for (int e = tid; e < 64 * C; e += NT) {
           const int r = e / C, k = e - r * C;
           const float is = misc[Cf::M_IS + k];
-          sf[Cf::F_T6 + tk_off(r, k, C)] *= is;
-          sf[Cf::F_T6 + 2 * Cf::T6T + tk_off(r, k, C)] *= is;
+          sf[Cf::F_T6 + Cf::T6_Q + tk_off(r, k, C)] *= is;
+          sf[Cf::F_T6 + Cf::T6_A + tk_off(r, k, C)] *= is;
         }
       }
     }
-    // ---------------- G6: [tril(aq) V ; V^T alpha] = [tril(aq); V^T] [V^T; alpha^T]^T  (M 128, N 128, K C)
+    // ---------------- G6: X = [V^T; tril(aq)] (M 128, K C); Y = V^T accumulates tril(aq) V onto
+    // S phi(q_t) (rows 64 + t, columns 0..63); Y = alpha^T gives V^T alpha (rows i, columns 128..191)
     {
-      const MmaPass ps[1] = {{Cf::F_T6, Cf::F_T6 + Cf::T6T, 128, 128, 0, false}};
-      if (!mma_run(ps, 1, C)) { failed = true; break; }
+      const MmaPass ps[2] = {{Cf::F_T6, Cf::F_T6 + Cf::T6_V, 128, 64, 0, true},
+                             {Cf::F_T6, Cf::F_T6 + Cf::T6_A, 128, 64, 128, false}};
+      if (!mma_run(ps, 2, C)) { failed = true; break; }
     }
     {
       float v[16];
-      if (row < 64 && half == 0) {   // outputs of step t (warp-uniform)
-        const int t = row;
+      if (row >= 64) {   // outputs of step t, columns 32 half .. 32 half + 31 (warp-uniform)
+        const int t = row - 64;
         const float sgt = misc[Cf::M_SG + t], rd = misc[Cf::M_RDEN + t];
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          tld(16 * cc, v);
+        for (int cc = 0; cc < 2; ++cc) {
+          const int col0 = 32 * half + 16 * cc;
+          tld(col0, v);
           if (t < c) {
             uint32_t pk[8];
 #pragma unroll
             for (int j = 0; j < 16; j += 2) {
-              const float o0 = sgt * (sf[Cf::F_P + t * YLD + 16 * cc + j] + v[j]) * rd;
-              const float o1 = sgt * (sf[Cf::F_P + t * YLD + 16 * cc + j + 1] + v[j + 1]) * rd;
+              const float o0 = sgt * v[j] * rd, o1 = sgt * v[j + 1] * rd;
               if (!isfinite(o0) || !isfinite(o1)) flags |= kStatusNonfinite;
               const __nv_bfloat162 b2 = __floats2bfloat162_rn(o0, o1);
               pk[j / 2] = *reinterpret_cast<const uint32_t*>(&b2);
             }
-            uint4* dst = reinterpret_cast<uint4*>(go + (pos + t) * D + 16 * cc);
+            uint4* dst = reinterpret_cast<uint4*>(go + (pos + t) * D + col0);
             dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
           }
         }
-      } else if (row >= 64 && half == 1) {   // S_1 = sigma (S + V^T alpha)
-        const int i = row - 64;
+      } else {           // S_1 = sigma (S + V^T alpha), rows i, columns 32 half .. 32 half + 31
+        const int i = row;
         const float sgl = misc[Cf::M_SG + c - 1];
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          tld(64 + 16 * cc, v);
+        for (int cc = 0; cc < 2; ++cc) {
+          const int col0 = 32 * half + 16 * cc;
+          tld(128 + col0, v);
 #pragma unroll
           for (int j = 0; j < 16; j += 4) {
-            float4* sp = reinterpret_cast<float4*>(sf + Cf::F_S + tk_off(i, 16 * cc + j, 64));
+            float4* sp = reinterpret_cast<float4*>(sf + Cf::F_S + tk_off(i, col0 + j, 64));
             float4 x = *sp;
             x.x = sgl * (x.x + v[j]);
             x.y = sgl * (x.y + v[j + 1]);
@@ -1028,7 +1055,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     flags |= kStatusTimeout;
     if (loaded + 1 < ntiles) (void)mbar_wait_bounded(in_bar, (uint32_t)((loaded + 1) & 1));
   }
-  if (warp == 0) tc::tmem_dealloc(tmem, 128);
+  if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
   if (flags) atomicOr(&a.status->flags, flags);
   if (tid == 0) {
     if (guard_cnt) atomicAdd(&a.status->guard_count, guard_cnt);
