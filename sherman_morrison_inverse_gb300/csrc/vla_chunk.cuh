@@ -222,6 +222,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
   const int q4 = warp & 3, half = warp >> 2;
   const int row = 32 * q4 + lane;   // row of an M = 128 result held by this thread
   auto tld = [&](int col, float (&v)[16]) { tc::tmem_ld16(tmem + ((uint32_t)(32 * q4) << 16) + (uint32_t)col, v); };
+  auto tld32 = [&](int col, float (&v)[32]) { tc::tmem_ld32(tmem + ((uint32_t)(32 * q4) << 16) + (uint32_t)col, v); };
   auto st4 = [&](int off, float x0, float x1, float x2, float x3) {
     *reinterpret_cast<float4*>(sf + off) = make_float4(x0, x1, x2, x3);
   };
@@ -435,12 +436,13 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
       if (!mma_run(ps, 2, 64)) { failed = true; break; }
     }
     {
-      float v[16];
+      float v32[32];
       const int g = (lane >> 2) & 7;
+      tld32(32 * half, v32);
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {   // [W^T; Q^T] -> Q tiles (X of G2); W (rows i) fp32 -> R tile 0
         const int col0 = 32 * half + 16 * cc;
-        tld(col0, v);
+        float (&v)[16] = *reinterpret_cast<float(*)[16]>(v32 + 16 * cc);
 #pragma unroll
         for (int j = 0; j < 16; j += 4) st4(Cf::F_Q + tk_off(row, col0 + j, 64), v[j], v[j + 1], v[j + 2], v[j + 3]);
         if (row < 64) {   // W[i][a] = W^T[a][i], a = row (warp-uniform)
@@ -457,11 +459,12 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     }
     float* Gs = sf + Cf::F_P;   // [64][GLD]: G, then L (strict lower) in place
     {
-      float v[16];
+      float v32[32];
+      tld32(32 * half, v32);
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int col0 = 32 * half + 16 * cc;
-        tld(col0, v);
+        float (&v)[16] = *reinterpret_cast<float(*)[16]>(v32 + 16 * cc);
         if (row < 64) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) Gs[row * GLD + col0 + j] = v[j] + ((row == col0 + j) ? 1.f : 0.f);
@@ -477,7 +480,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     // ---------------- LDL^T of G and X = L^{-1} in 16 x 16 blocks (fp32)
     // Right-looking block LDL^T with the inverse carried along as a forward
     // elimination of the identity.  For block column k:
-    //   [a] one warp factors the diagonal block G'_kk = L_kk D_k L_kk^T in registers;
+    //   [a] one warp factors the diagonal block G'_kk = L_kk D_k L_kk^T (2 x 2 blocks of 8);
     //   [b] 64 independent forward substitutions with L_kk, one per thread: the columns
     //       of X_kk = L_kk^{-1}, the panel rows (L D)_r = L_kk^{-1} G'_rk (i > k) and the
     //       columns of X_kj = L_kk^{-1} B_kj (j < k);
@@ -487,6 +490,23 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     // block itself and factors it while the other warps update the remaining blocks.
     // L D (the panel before D^{-1}) is kept, transposed, in the unused upper blocks of the staging.
     float* XB = sf + Cf::F_Q;   // packed blocks: B, then X = L^{-1}
+    // in-register LDL^T of an 8 x 8 symmetric block (lower triangle of a): a -> L (strict
+    // lower), dd = D, idd = 1 / D
+    auto ldl8 = [](float (&a)[8][8], float (&dd)[8], float (&idd)[8]) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        dd[j] = a[j][j];
+        idd[j] = __fdividef(1.f, dd[j]);
+#pragma unroll
+        for (int i = j + 1; i < 8; ++i) {
+          const float lij = a[i][j] * idd[j];
+#pragma unroll
+          for (int m = j + 1; m <= i; ++m) a[i][m] = fmaf(-lij, a[m][j], a[i][m]);   // a[m][j] = L[m][j] D_j
+        }
+#pragma unroll
+        for (int i = j + 1; i < 8; ++i) a[i][j] *= idd[j];
+      }
+    };
     // a 2 x 4 tile of [c] for step kc: block blk in the order (trailing blocks, B blocks),
     // rows 2 rr, 2 rr + 1 and columns 4 cc .. 4 cc + 3 of the block
     auto trail_tile = [&](int kc, int blk, int rr, int cc) {
@@ -546,29 +566,65 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
           trail_tile(k - 1, 0, lane >> 2, lane & 3);
           __syncwarp();
         }
-        // [a]: lane i (both half-warps) holds row i of G'_kk
-        const int i = lane & 15;
-        float g[16];
+        // [a]: G'_kk as 2 x 2 blocks of 8: B00 = L00 D0 L00^T in every lane's registers, the rows
+        // of L10 by lanes 0..7, the Schur complement B11 - L10 D0 L10^T by all lanes, then its
+        // LDL^T again in every lane (no shuffles; L10 D0 goes, transposed, into the block's
+        // upper half, which nothing reads afterwards)
+        const int b0 = 16 * k;
+        float a8[8][8], d0[8], id0[8];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) g[j] = Gs[(16 * k + i) * GLD + 16 * k + j];
-        float dmy = 1.f, idmy = 1.f;
+        for (int r = 0; r < 8; ++r)
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float dj = __shfl_sync(0xffffffffu, g[j], j);
-          const float rj = __fdividef(1.f, dj);
-          if (i == j) { dmy = dj; idmy = rj; }
-          const float lij = (i > j) ? g[j] * rj : 0.f;
+          for (int cl = 0; cl <= r; ++cl) a8[r][cl] = Gs[(b0 + r) * GLD + b0 + cl];
+        ldl8(a8, d0, id0);
+        if (lane < 8) {   // row 8 + lane: L10 D0 = B10 L00^{-T}
+          const int r = b0 + 8 + lane;
+          float y[8];
 #pragma unroll
-          for (int m = j + 1; m < 16; ++m)   // G'[j][m] = L[m][j] D_j (the block stays symmetric)
-            g[m] = fmaf(-lij, __shfl_sync(0xffffffffu, g[m], j), g[m]);
-          if (i > j) g[j] = lij;
+          for (int cl = 0; cl < 8; ++cl) y[cl] = Gs[r * GLD + b0 + cl];
+#pragma unroll
+          for (int cl = 1; cl < 8; ++cl)
+#pragma unroll
+            for (int m = 0; m < cl; ++m) y[cl] = fmaf(-a8[cl][m], y[m], y[cl]);
+#pragma unroll
+          for (int cl = 0; cl < 8; ++cl) {
+            Gs[(b0 + cl) * GLD + r] = y[cl];               // L10 D0, transposed
+            Gs[r * GLD + b0 + cl] = y[cl] * id0[cl];       // L10
+          }
         }
-        if (lane < 16) {
-          misc[Cf::M_D + 16 * k + i] = dmy;
-          misc[Cf::M_ID + 16 * k + i] = idmy;
+        __syncwarp();
+        for (int e = lane; e < 36; e += 32) {   // Schur complement, lower triangle (row i, column m)
+          int i = 0, m = e;
 #pragma unroll
-          for (int j = 0; j < 15; ++j)
-            if (j < i) Gs[(16 * k + i) * GLD + 16 * k + j] = g[j];
+          for (int q = 0; q < 8; ++q)
+            if (m > i) { m -= i + 1; ++i; }
+          const int gr = b0 + 8 + i;
+          float acc = Gs[gr * GLD + b0 + 8 + m];
+#pragma unroll
+          for (int cl = 0; cl < 8; ++cl) acc = fmaf(-Gs[gr * GLD + b0 + cl], Gs[(b0 + cl) * GLD + b0 + 8 + m], acc);
+          Gs[gr * GLD + b0 + 8 + m] = acc;
+        }
+        __syncwarp();
+        float a1[8][8], d1[8], id1[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+#pragma unroll
+          for (int cl = 0; cl <= r; ++cl) a1[r][cl] = Gs[(b0 + 8 + r) * GLD + b0 + 8 + cl];
+        ldl8(a1, d1, id1);
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            misc[Cf::M_D + b0 + r] = d0[r];
+            misc[Cf::M_ID + b0 + r] = id0[r];
+            misc[Cf::M_D + b0 + 8 + r] = d1[r];
+            misc[Cf::M_ID + b0 + 8 + r] = id1[r];
+#pragma unroll
+            for (int cl = 0; cl < r; ++cl) {
+              Gs[(b0 + r) * GLD + b0 + cl] = a8[r][cl];
+              Gs[(b0 + 8 + r) * GLD + b0 + 8 + cl] = a1[r][cl];
+            }
+          }
         }
       } else if (k > 0 && warp != 4) {   // the rest of step k-1's [c]; warp 4 leaves warp 0's
                                          // sub-partition to it
@@ -729,11 +785,12 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
       if (!mma_run(ps, 3, 64)) { failed = true; break; }
     }
     {
-      float v[16];
+      float v32[32];
+      tld32(32 * half, v32);
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int col0 = 32 * half + 16 * cc;
-        tld(col0, v);
+        float (&v)[16] = *reinterpret_cast<float(*)[16]>(v32 + 16 * cc);
 #pragma unroll
         for (int j = 0; j < 16; j += 4) {
           const int l = col0 + j;
@@ -761,12 +818,13 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
       if (!mma_run(ps, 3, 64)) { failed = true; break; }
     }
     {
-      float v[16];
+      float v32[32];
       float an = 0.f;
+      tld32(32 * half, v32);
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int col0 = 32 * half + 16 * cc;
-        tld(col0, v);
+        float (&v)[16] = *reinterpret_cast<float(*)[16]>(v32 + 16 * cc);
         if (row < 64) {   // A_1 = A_0 - Z D^{-1} Z^T (+ eps_n I at a nudge)
 #pragma unroll
           for (int j = 0; j < 16; j += 4) {
@@ -830,19 +888,18 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
       if (!mma_run(ps, 1, 64)) { failed = true; break; }
     }
     if (row >= 64) {   // warp-uniform: quadrants 2, 3 (rows 64 + t); S phi(q_t) stays in TMEM for G6
-      // aq[t][t'] = phi(q_t) . alpha_t', t' <= t -> tril(aq) rows t of T6 (16-column pieces by half)
-      float v[16];
+      // aq[t][t'] = phi(q_t) . alpha_t', t' <= t -> tril(aq) rows t of T6 (half h: t' = 32 h .. 32 h + 31)
       const int t = row - 64;
-#pragma unroll
-      for (int cc = half; cc < (C + 15) / 16; cc += 2) {
-        tld(64 + 16 * cc, v);
+      if (32 * half < C) {
+        float v32[32];
+        tld32(64 + 32 * half, v32);
         if (t < C) {
 #pragma unroll
-          for (int j = 0; j < 16; j += 4) {
-            const int tp = 16 * cc + j;
+          for (int j = 0; j < 32; j += 4) {
+            const int tp = 32 * half + j;
             float x[4];
 #pragma unroll
-            for (int m = 0; m < 4; ++m) x[m] = (tp + m <= t && t < c) ? v[j + m] : 0.f;
+            for (int m = 0; m < 4; ++m) x[m] = (tp + m <= t && t < c) ? v32[j + m] : 0.f;
             if (tp < C) st4(Cf::F_T6 + Cf::T6_Q + tk_off(t, tp, C), x[0], x[1], x[2], x[3]);
           }
         }
@@ -994,14 +1051,15 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
       if (!mma_run(ps, 2, C)) { failed = true; break; }
     }
     {
-      float v[16];
+      float v32[32];
       if (row >= 64) {   // outputs of step t, columns 32 half .. 32 half + 31 (warp-uniform)
         const int t = row - 64;
         const float sgt = misc[Cf::M_SG + t], rd = misc[Cf::M_RDEN + t];
+        tld32(32 * half, v32);
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           const int col0 = 32 * half + 16 * cc;
-          tld(col0, v);
+          float (&v)[16] = *reinterpret_cast<float(*)[16]>(v32 + 16 * cc);
           if (t < c) {
             uint32_t pk[8];
 #pragma unroll
@@ -1019,10 +1077,11 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
       } else {           // S_1 = sigma (S + V^T alpha), rows i, columns 32 half .. 32 half + 31
         const int i = row;
         const float sgl = misc[Cf::M_SG + c - 1];
+        tld32(128 + 32 * half, v32);
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           const int col0 = 32 * half + 16 * cc;
-          tld(128 + col0, v);
+          float (&v)[16] = *reinterpret_cast<float(*)[16]>(v32 + 16 * cc);
 #pragma unroll
           for (int j = 0; j < 16; j += 4) {
             float4* sp = reinterpret_cast<float4*>(sf + Cf::F_S + tk_off(i, col0 + j, 64));
