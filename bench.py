@@ -163,6 +163,11 @@ def barrier(dist):
         dist.barrier()
 
 
+def job_value(units_per_rank: int, world: int, ms_max: float) -> float:
+    """Whole-job throughput: the units every rank processed over the slowest rank's time."""
+    return units_per_rank * world / (ms_max / 1e3)
+
+
 class OracleLeg:
     """The float64 oracle, as it stands, timed on the host cores on a bounded
     sample of the workload: every pair, the first `steps` steps."""
@@ -296,8 +301,7 @@ def main():
     ms = ev0.elapsed_time(ev1)
     ms_max = max_over_ranks(ms, dist, dev)
     st = h.status()
-    units = B * H * T * args.steps * world
-    value = units / (ms_max / 1e3)
+    value = job_value(B * H * T * args.steps, world, ms_max)
     ms_per_step = ms_max / args.steps
 
     # ---- end to end: pinned host buffers -> device, scan, result back, every step
@@ -329,7 +333,7 @@ def main():
     torch.cuda.synchronize(dev)
     barrier(dist)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
-    e2e_value = B * H * T * e2e_steps * world / (e2e_ms / 1e3)
+    e2e_value = job_value(B * H * T * e2e_steps, world, e2e_ms)
     st_e2e = h.status()
 
     # ---- roofline of the (only) kernel: FP32 CUDA-core arithmetic binds
