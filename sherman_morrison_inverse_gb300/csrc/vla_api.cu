@@ -8,15 +8,16 @@
 #include <string>
 
 namespace vla {
-cudaError_t launch_seq_block_d16(int r, bool bf16, const ScanArgs& a, cudaStream_t s, bool* built);
-cudaError_t launch_seq_block_d64(int r, bool bf16, const ScanArgs& a, cudaStream_t s, bool* built);
-cudaError_t launch_seq_block_d128(int r, bool bf16, const ScanArgs& a, cudaStream_t s, bool* built);
+cudaError_t launch_seq_block_d16(int r, bool bf16, bool cluster, const ScanArgs& a, cudaStream_t s, bool* built);
+cudaError_t launch_seq_block_d64(int r, bool bf16, bool cluster, const ScanArgs& a, cudaStream_t s, bool* built);
+cudaError_t launch_seq_block_d128(int r, bool bf16, bool cluster, const ScanArgs& a, cudaStream_t s, bool* built);
 
-cudaError_t launch_seq(int d, int r, bool bf16, const ScanArgs& a, cudaStream_t s, bool* built) {
+cudaError_t launch_seq(int d, int r, bool bf16, int ctas, const ScanArgs& a, cudaStream_t s, bool* built) {
+  const bool cluster = ctas == 2;
   switch (d) {
-    case 16: return launch_seq_block_d16(r, bf16, a, s, built);
-    case 64: return launch_seq_block_d64(r, bf16, a, s, built);
-    case 128: return launch_seq_block_d128(r, bf16, a, s, built);
+    case 16: return launch_seq_block_d16(r, bf16, cluster, a, s, built);
+    case 64: return launch_seq_block_d64(r, bf16, cluster, a, s, built);
+    case 128: return launch_seq_block_d128(r, bf16, cluster, a, s, built);
     default: *built = false; return cudaSuccess;
   }
 }
@@ -30,6 +31,7 @@ void vla::set_thread_error(const char* msg) { g_create_error = msg ? msg : ""; }
 
 struct vla_handle_s {
   int device = 0;
+  int sm_count = 0;
   vla::DevStatus* status = nullptr;
   std::string last_error;
 };
@@ -81,7 +83,9 @@ vla_err_t vla_create(vla_handle_t* h, int device) {
   if (!hh) return fail(nullptr, VLA_ERR_NOMEM, "vla_create: out of host memory");
   hh->device = device;
   e = on_device(device, [&]() -> cudaError_t {
-    cudaError_t r = cudaMalloc(&hh->status, sizeof(vla::DevStatus));
+    cudaError_t r = cudaDeviceGetAttribute(&hh->sm_count, cudaDevAttrMultiProcessorCount, device);
+    if (r != cudaSuccess) return r;
+    r = cudaMalloc(&hh->status, sizeof(vla::DevStatus));
     if (r != cudaSuccess) return r;
     return cudaMemset(hh->status, 0, sizeof(vla::DevStatus));
   });
@@ -133,15 +137,27 @@ vla_err_t vla_scan_fwd(vla_handle_t h, const void* q, const void* k, const void*
   const bool bf16 = io_dtype == VLA_BF16;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   bool built = false;
-  cudaError_t e = on_device(h->device, [&]() -> cudaError_t {
-    if (mode == VLA_SEQUENTIAL) return vla::launch_seq(d, r, bf16, a, s, &built);
-    return vla::launch_chunked(d, r, bf16, chunk, a, s, &built);
-  });
+  // sequential mode: CTAs per pair.  By default a cluster of two for d = 128 while 2 B H
+  // CTAs fit on the SMs (one CTA of 4 d threads would be capped at 128 registers a thread
+  // and spill); one otherwise (at d <= 64 the hand-off between two SMs costs more than
+  // the issue slots it frees).
+  const int ctas = (mode != VLA_SEQUENTIAL) ? 0
+                   : (chunk != 0 ? chunk : ((d == 128 && 2 * pairs <= h->sm_count) ? 2 : 1));
+  cudaError_t e = cudaSuccess;
+  if (mode == VLA_SEQUENTIAL && ctas != 1 && ctas != 2) {
+    built = false;
+  } else {
+    e = on_device(h->device, [&]() -> cudaError_t {
+      if (mode == VLA_SEQUENTIAL) return vla::launch_seq(d, r, bf16, ctas, a, s, &built);
+      return vla::launch_chunked(d, r, bf16, chunk, a, s, &built);
+    });
+  }
   if (!built) {
     char buf[256];
     std::snprintf(buf, sizeof buf,
                   "vla_scan_fwd: not built for d=%d dv=%d r=%d dtype=%s mode=%s chunk=%d "
-                  "(sequential: d=dv in {16,64,128}, r in {1,4}; chunked: d=dv=64, bf16, r=1 chunk 64 or r=4 chunk 16, 0 = default)",
+                  "(sequential: d=dv in {16,64,128}, r in {1,4}, chunk = CTAs per pair 1 or 2, 0 = default; "
+                  "chunked: d=dv=64, bf16, r=1 chunk 64 or r=4 chunk 16, 0 = default)",
                   d, dv, r, bf16 ? "bf16" : "f32", mode == VLA_SEQUENTIAL ? "sequential" : "chunked", chunk);
     return fail(h, VLA_ERR_UNSUPPORTED, buf);
   }

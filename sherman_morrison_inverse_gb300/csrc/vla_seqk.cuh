@@ -136,7 +136,7 @@ struct Cfg {
   static constexpr int F_END = F_INFO + 16;
   static constexpr size_t raw_bytes = (size_t)Gm::NSTAGE * STAGE;
   static constexpr size_t bar_off = raw_bytes + sizeof(float) * (size_t)F_END;
-  static constexpr size_t bytes = bar_off + 16 * Gm::NSTAGE + 16;
+  static constexpr size_t bytes = bar_off + 16 * Gm::NSTAGE + 16 + 32;   // + FULL[2], EMPTY[2] (cluster mode)
   static_assert(QB % 16 == 0 && UB % 16 == 0 && REC % 4 == 0, "alignment");
   static_assert(TS % KS == 0, "chunks must tile a tile");
   static_assert(bytes <= 227 * 1024, "shared memory");
@@ -171,13 +171,21 @@ __device__ __forceinline__ void reduce_scatter(float (&v)[N], int lanebits) {
 
 // PS = false: status accumulates into a.status (one block per call);
 // PS = true:  into a.pair_status[pair] (one record per pair).
-template <int D, int R, int KS, typename TIO, bool PS = false>
-__global__ void __launch_bounds__(blk::Geom<D>::NT, 1) seq_block_kernel(ScanArgs a) {
+// CL = false: one CTA per pair holds both warp groups;
+// CL = true:  a cluster of two CTAs per pair: CTA 0 runs the A group, CTA 1 the S
+//             group, each on its own SM.  Both CTAs stream and convert the inputs;
+//             alpha and the round record go from CTA 0 into CTA 1's shared memory
+//             (distributed shared memory), and the FULL / EMPTY hand-off becomes a
+//             pair of cluster-scope mbarriers per parity (every thread of the
+//             producing group arrives with release semantics; waits are bounded).
+template <int D, int R, int KS, typename TIO, bool PS = false, bool CL = false>
+__global__ void __launch_bounds__(CL ? blk::Geom<D>::GT : blk::Geom<D>::NT, 1) seq_block_kernel(ScanArgs a) {
   using namespace blk;
   using Gm = Geom<D>;
   using C = Cfg<D, R, KS, TIO>;
   constexpr int RPT = Gm::RPT, LPR = Gm::LPR, NCH = Gm::NCH, NCP = Gm::NCP, GT = Gm::GT, GW = Gm::GW;
-  constexpr int NT = Gm::NT, TS = C::TS, NSTAGE = Gm::NSTAGE;
+  constexpr int NT = CL ? Gm::GT : Gm::NT, TS = C::TS, NSTAGE = Gm::NSTAGE;
+  static_assert(!(PS && CL), "the per-pair status entry point runs one CTA per pair");
   constexpr int M = C::M, REC = C::REC;
   constexpr float kInvSqrtD = (float)(D == 16 ? 0.25 : D == 64 ? 0.125 : 0.08838834764831845);
 
@@ -187,14 +195,16 @@ __global__ void __launch_bounds__(blk::Geom<D>::NT, 1) seq_block_kernel(ScanArgs
   int* info = reinterpret_cast<int*>(sf + C::F_INFO);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::bar_off);
   volatile int* flag = reinterpret_cast<volatile int*>(smem + C::bar_off + 16 * NSTAGE);
+  uint64_t* hb = reinterpret_cast<uint64_t*>(smem + C::bar_off + 16 * NSTAGE + 16);   // FULL[2], EMPTY[2]
 
   const int tid = threadIdx.x;
-  const bool isA = tid < GT;
-  const int gid = isA ? tid : tid - GT;          // thread index within its group
+  const uint32_t crank = CL ? cluster_ctarank() : 0u;
+  const bool isA = CL ? (crank == 0) : (tid < GT);
+  const int gid = CL ? tid : (isA ? tid : tid - GT);   // thread index within its group
   const int lane = tid & 31, gw = gid >> 5;      // warp within the group
   const int g = gid / LPR, c = gid % LPR;        // row group, lane within it
   const int row0 = g * RPT;
-  const long long pair = blockIdx.x;
+  const long long pair = CL ? (long long)(blockIdx.x >> 1) : (long long)blockIdx.x;
   const long long T = a.T;
 
   const TIO* gq = static_cast<const TIO*>(a.q) + pair * T * D;
@@ -211,10 +221,18 @@ __global__ void __launch_bounds__(blk::Geom<D>::NT, 1) seq_block_kernel(ScanArgs
   for (int e = tid; e < REC; e += NT) sf[C::F_ZERO + e] = (e == C::OFF_SC) ? 1.f : 0.f;
   if (tid == 0) {
     for (int s = 0; s < NSTAGE; ++s) mbar_init(&bars[s], 1);
+    if constexpr (CL) {
+      for (int p = 0; p < 4; ++p) mbar_init(&hb[p], GT);   // every thread of the producing group arrives
+    }
     fence_mbar_init();
     *flag = 0;
   }
   __syncthreads();
+  if constexpr (CL) cluster_sync_all();   // the peer's barriers are initialised before any arrival
+  // cluster hand-off: FULL[p] lives in CTA 1 (A arrives, S waits), EMPTY[p] in CTA 0
+  // (S arrives, A waits); alpha and the round record are stored into CTA 1
+  const uint32_t peer = crank ^ 1u;
+  auto remote = [&](const void* local) -> uint32_t { return mapa_shared(smem_u32(local), peer); };
 
   const int ntiles = (int)((T + TS - 1) / TS);
   auto issue = [&](int tile) {  // thread 0 only
@@ -234,6 +252,87 @@ __global__ void __launch_bounds__(blk::Geom<D>::NT, 1) seq_block_kernel(ScanArgs
     for (int j = 0; j < NSTAGE && j < ntiles; ++j) issue(j);
   }
 
+  // per-tile prologue (the A group's, and in cluster mode also the S group's on its
+  // own CTA): float32 records, 1/den_t, |v_t|
+  auto prologue = [&](int tile, float& n_i, int gbar) -> bool {
+    const int stage = tile % NSTAGE;
+    if (gid == 0) {
+      if (!mbar_wait_bounded(&bars[stage], (uint32_t)((tile / NSTAGE) & 1))) *flag = 1;
+    }
+    bar_sync(gbar, GT);
+    if (*flag) return false;
+    const long long t_start = (long long)tile * TS;
+    const int nst = (int)min((long long)TS, T - t_start);
+    const TIO* rq = reinterpret_cast<const TIO*>(raw + stage * C::STAGE);
+    const TIO* rk = reinterpret_cast<const TIO*>(raw + stage * C::STAGE + C::QB);
+    const TIO* rv = reinterpret_cast<const TIO*>(raw + stage * C::STAGE + 2 * C::QB);
+    const TIO* ru = reinterpret_cast<const TIO*>(raw + stage * C::STAGE + 3 * C::QB);
+    float* pre = sf + C::F_PRE + (tile & 1) * TS * REC;
+    float* prod = sf + C::F_PROD;
+    for (int e4 = gid; e4 < nst * R * D / 4; e4 += GT) {
+      const int e = 4 * e4, t = e / (R * D), off = e - t * (R * D);
+      const float4 x = make_float4(to_f32(ru[e]), to_f32(ru[e + 1]), to_f32(ru[e + 2]), to_f32(ru[e + 3]));
+      *reinterpret_cast<float4*>(pre + t * REC + C::OFF_U + off) = x;
+    }
+    for (int e4 = gid; e4 < nst * D / 4; e4 += GT) {
+      const int e = 4 * e4, t = e / D, i = e - t * D;
+      float* rec = pre + t * REC;
+      float kx[4], qx[4], vx[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        kx[j] = phi_elu1(to_f32(rk[e + j]));
+        qx[j] = phi_elu1(to_f32(rq[e + j]));
+        vx[j] = to_f32(rv[e + j]);
+      }
+      *reinterpret_cast<float4*>(rec + C::OFF_S + i) =
+          make_float4(kx[0] * kInvSqrtD, kx[1] * kInvSqrtD, kx[2] * kInvSqrtD, kx[3] * kInvSqrtD);
+      *reinterpret_cast<float4*>(rec + C::OFF_Q + i) = make_float4(qx[0], qx[1], qx[2], qx[3]);
+      *reinterpret_cast<float4*>(rec + C::OFF_V + i) = make_float4(vx[0], vx[1], vx[2], vx[3]);
+      *reinterpret_cast<float4*>(prod + e) = make_float4(kx[0], kx[1], kx[2], kx[3]);
+    }
+    bar_sync(gbar, GT);
+    if (gid < D) {   // n_t = n_{t-1} + phi(k_t); products n_t[i] phi(q_t)[i] in place of phi(k)
+      for (int t = 0; t < nst; ++t) {
+        n_i += prod[t * D + gid];
+        prod[t * D + gid] = n_i * pre[t * REC + C::OFF_Q + gid];
+      }
+    }
+    bar_sync(gbar, GT);
+    {  // 1/den_t and |v_t|: TPS threads per step
+      constexpr int TPS = GT / TS >= 1 ? GT / TS : 1;
+      constexpr int EPT = D / TPS;
+      static_assert(EPT % 4 == 0 && TPS <= 32, "den reduction layout");
+      const int t = gid / TPS, part = gid - t * TPS;
+      float dn = 0.f, vv = 0.f;
+      if (t < nst) {
+#pragma unroll
+        for (int j = 0; j < EPT; j += 4) {
+          const float4 p = *reinterpret_cast<const float4*>(prod + t * D + part * EPT + j);
+          const float4 w = *reinterpret_cast<const float4*>(pre + t * REC + C::OFF_V + part * EPT + j);
+          dn += (p.x + p.y) + (p.z + p.w);
+          vv = fmaf(w.x, w.x, fmaf(w.y, w.y, fmaf(w.z, w.z, fmaf(w.w, w.w, vv))));
+        }
+      }
+      // every lane of the warp takes part in the shuffles (a ragged tile leaves
+      // some lanes without a step)
+#pragma unroll
+      for (int m = TPS / 2; m >= 1; m >>= 1) {
+        dn += __shfl_xor_sync(0xffffffffu, dn, m);
+        vv += __shfl_xor_sync(0xffffffffu, vv, m);
+      }
+      if (t < nst && part == 0) {
+        pre[t * REC + C::OFF_SC] = __frcp_rn(dn + kReadoutEps);
+        pre[t * REC + C::OFF_SC + 1] = sqrtf(vv);
+      }
+    }
+    bar_sync(gbar, GT);
+    if (gid == 0 && tile + NSTAGE < ntiles) {
+      fence_proxy_async_smem();
+      issue(tile + NSTAGE);
+    }
+    return true;
+  };
+
   unsigned int flags = 0;
 
   if (isA) {
@@ -251,86 +350,6 @@ __global__ void __launch_bounds__(blk::Geom<D>::NT, 1) seq_block_kernel(ScanArgs
       }
     float n_i = (gid < D) ? gn[gid] : 0.f;
 
-    // per-tile prologue (A group only): float32 records, 1/den_t, |v_t|
-    auto prologue = [&](int tile) -> bool {
-      const int stage = tile % NSTAGE;
-      if (gid == 0) {
-        if (!mbar_wait_bounded(&bars[stage], (uint32_t)((tile / NSTAGE) & 1))) *flag = 1;
-      }
-      bar_sync(BAR_A, GT);
-      if (*flag) return false;
-      const long long t_start = (long long)tile * TS;
-      const int nst = (int)min((long long)TS, T - t_start);
-      const TIO* rq = reinterpret_cast<const TIO*>(raw + stage * C::STAGE);
-      const TIO* rk = reinterpret_cast<const TIO*>(raw + stage * C::STAGE + C::QB);
-      const TIO* rv = reinterpret_cast<const TIO*>(raw + stage * C::STAGE + 2 * C::QB);
-      const TIO* ru = reinterpret_cast<const TIO*>(raw + stage * C::STAGE + 3 * C::QB);
-      float* pre = sf + C::F_PRE + (tile & 1) * TS * REC;
-      float* prod = sf + C::F_PROD;
-      for (int e4 = gid; e4 < nst * R * D / 4; e4 += GT) {
-        const int e = 4 * e4, t = e / (R * D), off = e - t * (R * D);
-        const float4 x = make_float4(to_f32(ru[e]), to_f32(ru[e + 1]), to_f32(ru[e + 2]), to_f32(ru[e + 3]));
-        *reinterpret_cast<float4*>(pre + t * REC + C::OFF_U + off) = x;
-      }
-      for (int e4 = gid; e4 < nst * D / 4; e4 += GT) {
-        const int e = 4 * e4, t = e / D, i = e - t * D;
-        float* rec = pre + t * REC;
-        float kx[4], qx[4], vx[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          kx[j] = phi_elu1(to_f32(rk[e + j]));
-          qx[j] = phi_elu1(to_f32(rq[e + j]));
-          vx[j] = to_f32(rv[e + j]);
-        }
-        *reinterpret_cast<float4*>(rec + C::OFF_S + i) =
-            make_float4(kx[0] * kInvSqrtD, kx[1] * kInvSqrtD, kx[2] * kInvSqrtD, kx[3] * kInvSqrtD);
-        *reinterpret_cast<float4*>(rec + C::OFF_Q + i) = make_float4(qx[0], qx[1], qx[2], qx[3]);
-        *reinterpret_cast<float4*>(rec + C::OFF_V + i) = make_float4(vx[0], vx[1], vx[2], vx[3]);
-        *reinterpret_cast<float4*>(prod + e) = make_float4(kx[0], kx[1], kx[2], kx[3]);
-      }
-      bar_sync(BAR_A, GT);
-      if (gid < D) {   // n_t = n_{t-1} + phi(k_t); products n_t[i] phi(q_t)[i] in place of phi(k)
-        for (int t = 0; t < nst; ++t) {
-          n_i += prod[t * D + gid];
-          prod[t * D + gid] = n_i * pre[t * REC + C::OFF_Q + gid];
-        }
-      }
-      bar_sync(BAR_A, GT);
-      {  // 1/den_t and |v_t|: TPS threads per step
-        constexpr int TPS = GT / TS >= 1 ? GT / TS : 1;
-        constexpr int EPT = D / TPS;
-        static_assert(EPT % 4 == 0 && TPS <= 32, "den reduction layout");
-        const int t = gid / TPS, part = gid - t * TPS;
-        float dn = 0.f, vv = 0.f;
-        if (t < nst) {
-#pragma unroll
-          for (int j = 0; j < EPT; j += 4) {
-            const float4 p = *reinterpret_cast<const float4*>(prod + t * D + part * EPT + j);
-            const float4 w = *reinterpret_cast<const float4*>(pre + t * REC + C::OFF_V + part * EPT + j);
-            dn += (p.x + p.y) + (p.z + p.w);
-            vv = fmaf(w.x, w.x, fmaf(w.y, w.y, fmaf(w.z, w.z, fmaf(w.w, w.w, vv))));
-          }
-        }
-        // every lane of the warp takes part in the shuffles (a ragged tile leaves
-        // some lanes without a step)
-#pragma unroll
-        for (int m = TPS / 2; m >= 1; m >>= 1) {
-          dn += __shfl_xor_sync(0xffffffffu, dn, m);
-          vv += __shfl_xor_sync(0xffffffffu, vv, m);
-        }
-        if (t < nst && part == 0) {
-          pre[t * REC + C::OFF_SC] = __frcp_rn(dn + kReadoutEps);
-          pre[t * REC + C::OFF_SC + 1] = sqrtf(vv);
-        }
-      }
-      bar_sync(BAR_A, GT);
-      if (gid == 0 && tile + NSTAGE < ntiles) {
-        fence_proxy_async_smem();
-        issue(tile + NSTAGE);
-      }
-      return true;
-    };
-
     long long pos = 0;
     bool replay = false;
     long long rep_pos = 0;
@@ -340,7 +359,16 @@ __global__ void __launch_bounds__(blk::Geom<D>::NT, 1) seq_block_kernel(ScanArgs
     int par = 0;
     int rnd = 0;
     while (true) {
-      if (rnd >= 2) bar_sync(BAR_EMPTY0 + (rnd & 1), NT);   // S is done with round rnd-2
+      if (rnd >= 2) {   // S is done with round rnd-2
+        if constexpr (CL) {
+          if (!mbar_wait_cluster_bounded(&hb[2 + (rnd & 1)], (uint32_t)(((rnd - 2) >> 1) & 1))) {
+            flags |= kStatusTimeout;
+            *flag = 1;
+          }
+        } else {
+          bar_sync(BAR_EMPTY0 + (rnd & 1), NT);
+        }
+      }
       // ---------------- schedule this round's chunk
       int cA = 0, rep_j = 0;
       bool rep_completes = false, nudgeA = false, haveA = false;
@@ -366,11 +394,11 @@ __global__ void __launch_bounds__(blk::Geom<D>::NT, 1) seq_block_kernel(ScanArgs
         a_step = pos;
         haveA = true;
       }
-      bool stop = !haveA;
+      bool stop = !haveA || (CL && *flag != 0);
       if (haveA) {
         const int tile = (int)(a_step / TS);
         if (tile != loaded) {
-          if (!prologue(tile)) {
+          if (!prologue(tile, n_i, BAR_A)) {
             stop = true;
             flags |= kStatusTimeout;
           }
@@ -380,9 +408,15 @@ __global__ void __launch_bounds__(blk::Geom<D>::NT, 1) seq_block_kernel(ScanArgs
       if (stop) {   // publish the end of the sequence to the S group
         if (gid == 0) {
           int* inf = info + (rnd & 1) * 8;
-          inf[0] = 0; inf[1] = 0; inf[2] = 0; inf[3] = 0; inf[4] = 1;
+          if constexpr (CL) {
+            for (int q = 0; q < 4; ++q) st_cluster_s32(remote(inf + q), 0);
+            st_cluster_s32(remote(inf + 4), 1);
+          } else {
+            inf[0] = 0; inf[1] = 0; inf[2] = 0; inf[3] = 0; inf[4] = 1;
+          }
         }
-        bar_arrive(BAR_FULL0 + (rnd & 1), NT);
+        if constexpr (CL) mbar_arrive_remote(remote(&hb[rnd & 1]));
+        else bar_arrive(BAR_FULL0 + (rnd & 1), NT);
         ++rnd;
         break;
       }
@@ -635,18 +669,21 @@ __global__ void __launch_bounds__(blk::Geom<D>::NT, 1) seq_block_kernel(ScanArgs
               const float sadd = (guard ? kGuardEps : 0.f) + ((nudgeA && last) ? a.eps_n : 0.f);
               if (sadd != 0.f) al = fmaf(sadd, sf[rs + C::OFF_S + i], al);
             }
-            sf[abuf + tt * D + i] = al;
+            if constexpr (CL) st_cluster_f32(remote(sf + abuf + tt * D + i), al);
+            else sf[abuf + tt * D + i] = al;
           }
         }
         if (gid == 0) {
           int* inf = info + (rnd & 1) * 8;
-          inf[0] = apply ? cA : 0;
-          inf[1] = recA(0);
-          inf[2] = (int)(gA0 & 0x7fffffff);
-          inf[3] = (int)(gA0 >> 31);
-          inf[4] = 0;
+          const int iv[5] = {apply ? cA : 0, recA(0), (int)(gA0 & 0x7fffffff), (int)(gA0 >> 31), 0};
+#pragma unroll
+          for (int q = 0; q < 5; ++q) {
+            if constexpr (CL) st_cluster_s32(remote(inf + q), iv[q]);
+            else inf[q] = iv[q];
+          }
         }
-        bar_arrive(BAR_FULL0 + (rnd & 1), NT);
+        if constexpr (CL) mbar_arrive_remote(remote(&hb[rnd & 1]));
+        else bar_arrive(BAR_FULL0 + (rnd & 1), NT);
         // ---------------- bookkeeping
         if (replay && apply) {
           ++rep_col;
@@ -664,7 +701,15 @@ __global__ void __launch_bounds__(blk::Geom<D>::NT, 1) seq_block_kernel(ScanArgs
     // rnd rounds were published, the last one the end marker.  S arrived on
     // EMPTY after each real round 0 .. rnd-2; the syncs at the top of the loop
     // matched rounds 0 .. rnd-3, so round rnd-2 is still to be matched.
-    if (rnd >= 2) bar_sync(BAR_EMPTY0 + ((rnd - 2) & 1), NT);
+    if (rnd >= 2) {
+      if constexpr (CL) {
+        // S's last remote access to this CTA is its EMPTY arrival for round rnd-2
+        if (!mbar_wait_cluster_bounded(&hb[2 + ((rnd - 2) & 1)], (uint32_t)(((rnd - 2) >> 1) & 1)))
+          flags |= kStatusTimeout;
+      } else {
+        bar_sync(BAR_EMPTY0 + ((rnd - 2) & 1), NT);
+      }
+    }
     if (!(flags & kStatusTimeout)) {
 #pragma unroll
       for (int r = 0; r < RPT; ++r)
@@ -704,12 +749,33 @@ __global__ void __launch_bounds__(blk::Geom<D>::NT, 1) seq_block_kernel(ScanArgs
     unsigned long long renorm_cnt = 0;
     int par = 0;
     bool timed_out = false;
+    [[maybe_unused]] float n_s = (gid < D) ? gn[gid] : 0.f;   // cluster mode: the S CTA's own records
+    [[maybe_unused]] int loaded_s = -1;
     for (int rnd = 0;; ++rnd) {
-      bar_sync(BAR_FULL0 + (rnd & 1), NT);
+      if constexpr (CL) {
+        if (!mbar_wait_cluster_bounded(&hb[rnd & 1], (uint32_t)((rnd >> 1) & 1))) {
+          timed_out = true;
+          flags |= kStatusTimeout;
+          break;
+        }
+      } else {
+        bar_sync(BAR_FULL0 + (rnd & 1), NT);
+      }
       const int* inf = info + (rnd & 1) * 8;
       const int cS = inf[0], baseS = inf[1];
       const long long gS0 = (long long)inf[2] | ((long long)inf[3] << 31);
-      if (inf[4]) { timed_out = (*flag != 0); break; }
+      if (inf[4]) { timed_out = timed_out || (*flag != 0); break; }
+      if constexpr (CL) {   // this CTA's copy of the round's tile
+        const int tile_s = (int)(gS0 / TS);
+        if (cS > 0 && tile_s != loaded_s) {
+          if (!prologue(tile_s, n_s, BAR_S)) {
+            timed_out = true;
+            flags |= kStatusTimeout;
+            break;
+          }
+          loaded_s = tile_s;
+        }
+      }
       if (cS > 0) {
         auto recS = [&](int t) -> int { return (t < cS) ? baseS + t * REC : C::F_ZERO; };
         const int ybuf = C::F_Y + par * KS * D;
@@ -965,7 +1031,8 @@ __global__ void __launch_bounds__(blk::Geom<D>::NT, 1) seq_block_kernel(ScanArgs
           }
         }
       }
-      bar_arrive(BAR_EMPTY0 + (rnd & 1), NT);
+      if constexpr (CL) mbar_arrive_remote(remote(&hb[2 + (rnd & 1)]));
+      else bar_arrive(BAR_EMPTY0 + (rnd & 1), NT);
       par ^= 1;
     }
     if (!timed_out) {
@@ -977,6 +1044,12 @@ __global__ void __launch_bounds__(blk::Geom<D>::NT, 1) seq_block_kernel(ScanArgs
               make_float4(sigma * S2[r][2 * kk].x, sigma * S2[r][2 * kk].y, sigma * S2[r][2 * kk + 1].x,
                           sigma * S2[r][2 * kk + 1].y);
         }
+    }
+    if constexpr (CL) {
+      if (timed_out && gid == 0) {
+        for (int j = loaded_s + 1; j < ntiles && j <= loaded_s + NSTAGE; ++j)
+          (void)mbar_wait_bounded(&bars[j % NSTAGE], (uint32_t)((j / NSTAGE) & 1));
+      }
     }
     if (gid == 0 && renorm_cnt) {
       if constexpr (PS) atomicAdd(&a.pair_status[pair].renorm_count, (unsigned int)renorm_cnt);
@@ -992,10 +1065,34 @@ __global__ void __launch_bounds__(blk::Geom<D>::NT, 1) seq_block_kernel(ScanArgs
 template <int D, int R, int KS, typename TIO, bool PS = false>
 cudaError_t launch_seq_block_t(const ScanArgs& a, cudaStream_t s) {
   using C = blk::Cfg<D, R, KS, TIO>;
-  auto kern = seq_block_kernel<D, R, KS, TIO, PS>;
+  auto kern = seq_block_kernel<D, R, KS, TIO, PS, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::bytes);
   if (e != cudaSuccess) return e;
   kern<<<a.pairs, blk::Geom<D>::NT, C::bytes, s>>>(a);
+  return cudaGetLastError();
+}
+
+// Cluster mode: two CTAs (A group, S group) per pair.
+template <int D, int R, int KS, typename TIO>
+cudaError_t launch_seq_cluster_t(const ScanArgs& a, cudaStream_t s) {
+  using C = blk::Cfg<D, R, KS, TIO>;
+  auto kern = seq_block_kernel<D, R, KS, TIO, false, true>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::bytes);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2u * (unsigned)a.pairs, 1, 1);
+  cfg.blockDim = dim3(blk::Geom<D>::GT, 1, 1);
+  cfg.dynamicSmemBytes = C::bytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

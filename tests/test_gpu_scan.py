@@ -145,7 +145,7 @@ def _raw_call(h, t, **over):
     lib = h.lib
     args = dict(q=t["q"].data_ptr(), k=t["k"].data_ptr(), v=t["v"].data_ptr(), u=t["u"].data_ptr(),
                 A=t["A"].data_ptr(), S=t["S"].data_ptr(), n=t["n"].data_ptr(), o=t["o"].data_ptr(),
-                B=1, H=2, T=8, d=64, dv=64, r=1, P=4, eps=1e-6, tau=1e4, t0=0, dtype=0, mode=0, chunk=16)
+                B=1, H=2, T=8, d=64, dv=64, r=1, P=4, eps=1e-6, tau=1e4, t0=0, dtype=0, mode=0, chunk=0)
     args.update(over)
     return lib.vla_scan_fwd(h.ptr, args["q"], args["k"], args["v"], args["u"], args["A"], args["S"],
                             args["n"], args["o"], args["B"], args["H"], args["T"], args["d"], args["dv"],
