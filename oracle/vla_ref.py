@@ -33,6 +33,15 @@ Reading adopted where the pages are loose (each is listed in the design notes):
 * Readout: o_t = S_t phi(q_t) / (n_t . phi(q_t) + 1e-6) with n_t = n_{t-1} + phi(k_t).
 * phi(x) = x + 1 for x > 0, exp(x) otherwise (ELU with alpha = 1, plus one).
 
+The delta-rule variant (``rule="delta"``) follows the gist.science summary
+§2.3 ("Recursive Update Rule"): the same tracking of A, then
+alpha_hat_t = A_t k_hat_t / |A_t k_hat_t| and S_t = S_{t-1} + (v_t - S_{t-1} k_hat_t)
+alpha_hat_t^T, with both vectors of unit length.  Readings: k_hat_t is the
+feature-mapped key phi(k_t) normalised (the summary calls it "the normalized
+key" and uses the ELU+1 features for the output); unit length is x / max(|x|,
+1e-12), the convention of u's normalisation; the normaliser n, the
+renormalisation and the readout are the additive path's.
+
 The loop runs over t; independent (batch, head) pairs are stacked on a leading
 axis and advanced together with numpy (no reordering of any step).
 """
@@ -41,6 +50,7 @@ from __future__ import annotations
 import numpy as np
 
 GUARD_EPS = 1e-6     # singularity threshold and injected diagonal (Mathematical Primitives §2)
+NORM_EPS = 1e-12     # floor of the norms in unit-length vectors (delta-rule variant)
 READOUT_EPS = 1e-6   # readout denominator offset (spec reading of the README's calibrated readout)
 
 
@@ -57,7 +67,7 @@ def _f64(x):
 
 
 def scan(q, k, v, u, A0, S0, n0, *, P: int, eps_n: float, tau: float, t0: int = 0,
-         trace: bool = False, keep_A: bool = False):
+         trace: bool = False, keep_A: bool = False, rule: str = "additive"):
     """Run the recurrence over T steps for N independent (batch, head) pairs.
 
     Shapes: q, k [N, T, d]; v [N, T, dv]; u [N, T, r, d]; A0 [N, d, d];
@@ -67,8 +77,10 @@ def scan(q, k, v, u, A0, S0, n0, *, P: int, eps_n: float, tau: float, t0: int = 
     Returns ``(o, A, S, n)`` with o [N, T, dv] and the final state, plus a trace
     dict when ``trace``: delta [N, T, r], guard [N, T, r] (bool), renorm [N, T]
     (bool), snorm_pre [N, T] (||S_t||_F before renormalisation), and A_t [N, T, d, d]
-    when ``keep_A``.
+    when ``keep_A``.  ``rule`` = "additive" (S += v alpha^T) or "delta" (the
+    delta-rule variant in the module docstring).
     """
+    assert rule in ("additive", "delta")
     q, k, v, u = _f64(q), _f64(k), _f64(v), _f64(u)
     A, S, n = _f64(A0), _f64(S0), _f64(n0)
     N, T, d = q.shape
@@ -103,12 +115,22 @@ def scan(q, k, v, u, A0, S0, n0, *, P: int, eps_n: float, tau: float, t0: int = 
             # --- periodic spectrum stabilisation (Primitives §2, last item)
             if P > 0 and g % P == 0:
                 A = A + eps_n * eye
-            # --- coefficient alpha_t = A_t s_t (Primitives §4)
             phk = phi(k[:, t, :])
-            s = phk * inv_sqrt_d
-            alpha = np.matmul(A, s[:, :, None])[:, :, 0]
-            # --- state update and normaliser (Primitives §5, README v3 item 5)
-            S = S + v[:, t, :, None] * alpha[:, None, :]
+            if rule == "delta":
+                # --- unit key, unit gate alpha_hat = A k_hat / |A k_hat|, residual write
+                #     (gist.science summary §2.3)
+                kh = phk / np.maximum(np.linalg.norm(phk, axis=1, keepdims=True), NORM_EPS)
+                ak = np.matmul(A, kh[:, :, None])[:, :, 0]
+                gate = ak / np.maximum(np.linalg.norm(ak, axis=1, keepdims=True), NORM_EPS)
+                resid = v[:, t, :] - np.matmul(S, kh[:, :, None])[:, :, 0]
+                S = S + resid[:, :, None] * gate[:, None, :]
+            else:
+                # --- coefficient alpha_t = A_t s_t (Primitives §4)
+                s = phk * inv_sqrt_d
+                alpha = np.matmul(A, s[:, :, None])[:, :, 0]
+                # --- state update (Primitives §5)
+                S = S + v[:, t, :, None] * alpha[:, None, :]
+            # --- normaliser (README v3 item 5)
             n = n + phk
             # --- dynamic renormalisation (Primitives §5)
             nrm = np.sqrt(np.sum(S * S, axis=(1, 2)))

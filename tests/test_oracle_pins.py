@@ -342,10 +342,77 @@ def check_phi(mod):
     assert mod.phi(np.array([0.0]))[0] == 1.0
 
 
+# ---- the delta-rule variant (gist.science summary §2.3)
+
+def check_delta_d1_overwrite(mod):
+    """d = 1: k_hat = 1 and alpha_hat = 1 (A > 0), so S_t = v_t exactly; the readout
+    is the additive path's ratio with that S."""
+    g = rng(31)
+    T, dv = 30, 3
+    q = g.normal(size=(1, T, 1)); k = g.normal(size=(1, T, 1)); v = g.normal(size=(1, T, dv))
+    u = 0.5 * np.where(g.random(size=(1, T, 1, 1)) < 0.5, -1.0, 1.0)
+    S0 = g.normal(size=(1, dv, 1))
+    o, A, S, n = run(mod, q, k, v, u, np.ones((1, 1, 1)), S0, np.zeros((1, 1)), P=0, eps_n=0.0,
+                     tau=1e30, rule="delta")
+    nx = 0.0
+    for t in range(T):
+        fk = phi_torch(k[0, t, 0]); fq = phi_torch(q[0, t, 0])
+        nx = nx + fk
+        assert rel(o[0, t], v[0, t] * fq / (nx * fq + 1e-6)) < 1e-12
+    assert rel(S[0, :, 0], v[0, T - 1]) < 1e-14
+
+
+def _delta_steps(mod, seed, d=6, dv=4, N=3, T=10):
+    """Run the delta rule one step per call; yields (t, S_prev, S_next, A_next, k_hat, v_t)."""
+    q, k, v, u, A0, M0, S0, n0 = rand_case(seed, N, T, d, dv, 1, spd_A0=True)
+    S0 = rng(seed + 1).normal(size=(N, dv, d))
+    A, S, n = A0, S0, n0
+    for t in range(T):
+        _, A1, S1, n1 = run(mod, q[:, t:t + 1], k[:, t:t + 1], v[:, t:t + 1], u[:, t:t + 1], A, S, n,
+                            P=0, eps_n=0.0, tau=1e30, t0=t, rule="delta")
+        fk = phi_torch(k[:, t])
+        kh = fk / np.linalg.norm(fk, axis=1, keepdims=True)
+        yield t, S, S1, A1, kh, v[:, t]
+        A, S, n = A1, S1, n1
+
+
+def check_delta_residual_contraction(mod):
+    """The residual at the written key shrinks by exactly (1 - alpha_hat . k_hat):
+    v - S_t k_hat = (1 - c)(v - S_{t-1} k_hat), c = (A_t k_hat / |A_t k_hat|) . k_hat."""
+    for t, S0, S1, A1, kh, vt in _delta_steps(mod, 41):
+        ak = np.einsum("pij,pj->pi", A1, kh)
+        c = np.sum(ak * kh, axis=1) / np.linalg.norm(ak, axis=1)
+        r0 = vt - np.einsum("pij,pj->pi", S0, kh)
+        r1 = vt - np.einsum("pij,pj->pi", S1, kh)
+        assert rel(r1, (1.0 - c)[:, None] * r0) < 1e-10
+
+
+def check_delta_orthogonal_untouched(mod):
+    """Directions orthogonal to alpha_hat = A_t k_hat / |A_t k_hat| keep their image:
+    S_t w = S_{t-1} w for w . alpha_hat = 0."""
+    g = rng(43)
+    for t, S0, S1, A1, kh, vt in _delta_steps(mod, 42):
+        ah = np.einsum("pij,pj->pi", A1, kh)
+        ah = ah / np.linalg.norm(ah, axis=1, keepdims=True)
+        w = g.normal(size=kh.shape)
+        w = w - np.sum(w * ah, axis=1, keepdims=True) * ah
+        assert rel(np.einsum("pij,pj->pi", S1, w), np.einsum("pij,pj->pi", S0, w)) < 1e-10
+
+
+def check_delta_tracks_the_same_A(mod):
+    """The variant changes the state write only: A, n and the guard are the additive path's."""
+    q, k, v, u, A0, M0, S0, n0 = rand_case(44, 2, 25, 5, 3, 2, spd_A0=True)
+    kw = dict(P=7, eps_n=1e-3, tau=3.0)
+    _, Aa, _, na = run(mod, q, k, v, u, A0, S0, n0, **kw)
+    _, Ad, _, nd = run(mod, q, k, v, u, A0, S0, n0, rule="delta", **kw)
+    assert np.array_equal(Aa, Ad) and np.array_equal(na, nd)
+
+
 CHECKS = [check_golden_worked, check_exact_rational, check_gauss_jordan, check_d1_closed_form,
           check_basis_cycling, check_woodbury_rank_r, check_ldl_pivots, check_alpha_least_squares,
           check_invariants, check_guard, check_renorm, check_split_calls,
-          check_readout_bruteforce, check_phi]
+          check_readout_bruteforce, check_phi, check_delta_d1_overwrite, check_delta_residual_contraction,
+          check_delta_orthogonal_untouched, check_delta_tracks_the_same_A]
 
 
 @pytest.mark.parametrize("check", CHECKS, ids=lambda c: c.__name__)
@@ -443,6 +510,18 @@ MUTATIONS = {
     "alpha_before_nudge": ("            if P > 0 and g % P == 0:\n                A = A + eps_n * eye\n",
                            ""),
     "readout_before_renorm": ("            S = S * scale[:, None, None]\n", ""),
+    # delta-rule variant
+    "delta_gate_unnormalised": ("gate = ak / np.maximum(np.linalg.norm(ak, axis=1, keepdims=True), NORM_EPS)",
+                                "gate = ak"),
+    "delta_key_unnormalised": ("kh = phk / np.maximum(np.linalg.norm(phk, axis=1, keepdims=True), NORM_EPS)",
+                               "kh = phk"),
+    "delta_residual_sign": ("resid = v[:, t, :] - np.matmul(S, kh[:, :, None])[:, :, 0]",
+                            "resid = v[:, t, :] + np.matmul(S, kh[:, :, None])[:, :, 0]"),
+    "delta_no_residual": ("resid = v[:, t, :] - np.matmul(S, kh[:, :, None])[:, :, 0]", "resid = v[:, t, :]"),
+    "delta_gate_from_raw_key": ("ak = np.matmul(A, kh[:, :, None])[:, :, 0]",
+                                "ak = np.matmul(A, k[:, t, :, None])[:, :, 0]"),
+    "delta_outer_transposed": ("S = S + resid[:, :, None] * gate[:, None, :]",
+                               "S = S + (gate[:, :, None] * resid[:, None, :]).reshape(S.shape)"),
 }
 
 
