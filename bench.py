@@ -43,10 +43,11 @@ FP32_LANES_PER_SM = 128
 SM_MAX_MHZ_NOMINAL = 2070.0
 
 
-def flops_per_token_head(d: int, dv: int, r: int) -> int:
+def flops_per_token_head(d: int, dv: int, r: int, mode: str = "sequential") -> int:
     """Algorithmic flops of one step of one pair (FMA = 2): r (A u: 2d^2, u.z: 2d,
-    rank-1 update: 2d^2) + alpha = A s (2d^2) + S += v alpha^T (2 d dv) + S phi(q) (2 d dv)."""
-    return r * (4 * d * d + 2 * d) + 2 * d * d + 4 * d * dv
+    rank-1 update: 2d^2) + alpha = A s (2d^2) + S += v alpha^T (2 d dv) + S phi(q) (2 d dv);
+    the delta-rule variant adds S k_hat (2 d dv)."""
+    return r * (4 * d * d + 2 * d) + 2 * d * d + (6 if mode == "delta" else 4) * d * dv
 
 
 def flops_per_token_head_short(d: int, dv: int, r: int) -> int:
@@ -72,7 +73,7 @@ TRAFFIC = {
 }
 
 # arithmetic type of each mode's path
-MODE_DTYPE = {"sequential": "f32", "chunked": "tf32"}
+MODE_DTYPE = {"sequential": "f32", "chunked": "tf32", "delta": "f32"}
 
 
 def fp32_peak_tflops(peaks: dict) -> tuple[float, str]:
@@ -240,9 +241,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="2", help="index or name of the workload")
-    ap.add_argument("--mode", choices=["auto", "sequential", "chunked"], default="auto",
+    ap.add_argument("--mode", choices=["auto", "sequential", "chunked", "delta"], default="auto",
                     help="auto: the chunked tensor-core kernel where it is built (d = d_v = 64, bf16 I/O, "
-                         "r = 1 or 4), else the sequential one")
+                         "r = 1 or 4), else the sequential one; delta: the delta-rule variant")
     ap.add_argument("--chunk", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=None)
@@ -339,7 +340,7 @@ def main():
     # ---- roofline of the (only) kernel: FP32 CUDA-core arithmetic binds
     peaks = load_peaks()
     peak_tf, peak_how = fp32_peak_tflops(peaks)
-    F = flops_per_token_head(w.d, w.dv, w.r)
+    F = flops_per_token_head(w.d, w.dv, w.r, args.mode)
     achieved_tf = B * H * T * F / (ms_per_step / 1e3) / 1e12
     bytes_step = B * H * T * streamed_bytes_per_token_head(w)
     traffic = TRAFFIC.get((w.name, args.mode), (None, "no capture for this workload"))
@@ -352,8 +353,9 @@ def main():
         "vs_baseline": None, "dtype": MODE_DTYPE[args.mode], "data": "synthetic",
         "config": {"workload": w.name, "B": B, "H": H, "T": T, "d": w.d, "dv": w.dv, "r": w.r,
                    "io": w.io, "state": "f32", "mode": args.mode,
-                   "precision": ("fp32 CUDA-core arithmetic" if args.mode == "sequential" else
-                                 "tcgen05 kind::tf32, 3xTF32 on the products that carry A; fp32 state"),
+                   "precision": ("tcgen05 kind::tf32, 3xTF32 on the products that carry A; fp32 state"
+                                 if args.mode == "chunked" else "fp32 CUDA-core arithmetic"),
+                   "rule": "delta (gist.science summary §2.3)" if args.mode == "delta" else "additive",
                    "l2": f"inputs {bytes_step / 1e9:.2f} GB per step > 129 MB L2 (no flush)",
                    "parallelism": f"replicas x{world}, one CTA per (b,h) pair"},
         "roofline": {"bound": "alu", "achieved": achieved_tf, "peak": peak_tf, "unit": "TFLOP/s",

@@ -63,7 +63,11 @@ typedef enum { VLA_F32 = 0, VLA_BF16 = 1 } vla_dtype_t;        /* dtype of q, k,
 
 typedef enum {
   VLA_SEQUENTIAL = 0,   /* one step after another (the pages' recurrence) */
-  VLA_CHUNKED = 1       /* `chunk` steps at a time in exact Woodbury / LDL^T form */
+  VLA_CHUNKED = 1,      /* `chunk` steps at a time in exact Woodbury / LDL^T form */
+  VLA_DELTA = 2         /* the delta-rule variant (gist.science summary §2.3, "Recursive
+                           Update Rule"): A tracked as above, then alpha_hat = A k_hat / |A k_hat|
+                           with k_hat = phi(k) / |phi(k)|, S += (v - S k_hat) alpha_hat^T; n,
+                           renormalisation and readout unchanged; one step at a time */
 } vla_mode_t;
 
 /* Status flags, ORed over all pairs since the last vla_status() call. */
@@ -100,7 +104,8 @@ vla_err_t vla_create(vla_handle_t* h, int device);
  *   mode      VLA_SEQUENTIAL (every built shape) or VLA_CHUNKED (d == 64 only;
  *             `chunk` = steps per chunk, see the built list in the library's
  *             error message).  Both compute the same recurrence; they differ in
- *             rounding only.
+ *             rounding only.  VLA_DELTA computes the delta-rule variant (every
+ *             built shape; `chunk` must be 0).
  *   chunk     VLA_CHUNKED: steps per chunk (0 = the built default).
  *             VLA_SEQUENTIAL: CTAs per (batch, head) pair: 1 = one CTA holds
  *             both halves of the step; 2 = a cluster of two CTAs on two SMs, one

@@ -21,10 +21,10 @@ import threading
 import torch
 
 __all__ = ["scan_fwd", "Handle", "VlaError", "library_path", "load_library",
-           "STATUS_NONFINITE", "STATUS_TIMEOUT", "SEQUENTIAL", "CHUNKED"]
+           "STATUS_NONFINITE", "STATUS_TIMEOUT", "SEQUENTIAL", "CHUNKED", "DELTA"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-SEQUENTIAL, CHUNKED = 0, 1
+SEQUENTIAL, CHUNKED, DELTA = 0, 1, 2
 F32, BF16 = 0, 1
 STATUS_NONFINITE, STATUS_TIMEOUT = 1, 2
 ERR_NAMES = {0: "VLA_OK", 1: "VLA_ERR_INVALID_ARG", 2: "VLA_ERR_UNSUPPORTED", 3: "VLA_ERR_CUDA",
@@ -158,7 +158,7 @@ class Handle:
                 raise ValueError(f"{name} is on {t.device}, the handle is on {self.device}")
             if not t.is_contiguous():
                 raise ValueError(f"{name} must be contiguous")
-        mode_i = {"sequential": SEQUENTIAL, "chunked": CHUNKED}[mode]
+        mode_i = {"sequential": SEQUENTIAL, "chunked": CHUNKED, "delta": DELTA}[mode]
         code = self.lib.vla_scan_fwd(
             self._h, q.data_ptr(), k.data_ptr(), v.data_ptr(), u.data_ptr(),
             A.data_ptr(), S.data_ptr(), n.data_ptr(), o.data_ptr(),

@@ -114,7 +114,7 @@ vla_err_t vla_scan_fwd(vla_handle_t h, const void* q, const void* k, const void*
   if (!std::isfinite(eps_n)) return fail(h, VLA_ERR_INVALID_ARG, "vla_scan_fwd: eps_n must be finite");
   if (io_dtype != VLA_F32 && io_dtype != VLA_BF16)
     return fail(h, VLA_ERR_INVALID_ARG, "vla_scan_fwd: unknown io_dtype");
-  if (mode != VLA_SEQUENTIAL && mode != VLA_CHUNKED)
+  if (mode != VLA_SEQUENTIAL && mode != VLA_CHUNKED && mode != VLA_DELTA)
     return fail(h, VLA_ERR_INVALID_ARG, "vla_scan_fwd: unknown mode");
   const long long pairs = (long long)B * H;
   if (pairs > 0x7fffffffLL) return fail(h, VLA_ERR_INVALID_ARG, "vla_scan_fwd: B*H too large");
@@ -144,21 +144,23 @@ vla_err_t vla_scan_fwd(vla_handle_t h, const void* q, const void* k, const void*
   const int ctas = (mode != VLA_SEQUENTIAL) ? 0
                    : (chunk != 0 ? chunk : ((d == 128 && 2 * pairs <= h->sm_count) ? 2 : 1));
   cudaError_t e = cudaSuccess;
-  if (mode == VLA_SEQUENTIAL && ctas != 1 && ctas != 2) {
+  if ((mode == VLA_SEQUENTIAL && ctas != 1 && ctas != 2) || (mode == VLA_DELTA && chunk != 0)) {
     built = false;
   } else {
     e = on_device(h->device, [&]() -> cudaError_t {
       if (mode == VLA_SEQUENTIAL) return vla::launch_seq(d, r, bf16, ctas, a, s, &built);
+      if (mode == VLA_DELTA) return vla::launch_delta(d, r, bf16, a, s, &built);
       return vla::launch_chunked(d, r, bf16, chunk, a, s, &built);
     });
   }
   if (!built) {
-    char buf[256];
+    char buf[384];
     std::snprintf(buf, sizeof buf,
                   "vla_scan_fwd: not built for d=%d dv=%d r=%d dtype=%s mode=%s chunk=%d "
                   "(sequential: d=dv in {16,64,128}, r in {1,4}, chunk = CTAs per pair 1 or 2, 0 = default; "
-                  "chunked: d=dv=64, bf16, r=1 chunk 64 or r=4 chunk 16, 0 = default)",
-                  d, dv, r, bf16 ? "bf16" : "f32", mode == VLA_SEQUENTIAL ? "sequential" : "chunked", chunk);
+                  "chunked: d=dv=64, bf16, r=1 chunk 64 or r=4 chunk 16, 0 = default; "
+                  "delta: d=dv in {16,64,128}, r in {1,4}, chunk 0)",
+                  d, dv, r, bf16 ? "bf16" : "f32", mode == VLA_SEQUENTIAL ? "sequential" : mode == VLA_DELTA ? "delta" : "chunked", chunk);
     return fail(h, VLA_ERR_UNSUPPORTED, buf);
   }
   if (e != cudaSuccess) return fail(h, VLA_ERR_CUDA, cuda_msg("vla_scan_fwd: launch", e));
