@@ -12,5 +12,5 @@ Modules
               Woodbury / LDL^T form (the design the chunked GPU kernel follows),
               checked against ``vla_ref`` by the tests.
 """
-from .vla_ref import GUARD_EPS, READOUT_EPS, phi, scan, errors  # noqa: F401
+from .vla_ref import GUARD_EPS, READOUT_EPS, phi, scan, errors, project_u  # noqa: F401
 from .woodbury import scan_chunked, ldl_unit  # noqa: F401

@@ -152,6 +152,18 @@ def scan(q, k, v, u, A0, S0, n0, *, P: int, eps_n: float, tau: float, t0: int = 
     return o, A, S, n
 
 
+def project_u(k_raw, W_u):
+    """u_{t,i} = W_u[i] k_t / max(|W_u[i] k_t|_2, 1e-12): the learned penalty directions
+    "u_t = normalize(W_u k_t^raw)" (README "VLA v3" item 2).
+
+    k_raw [N, d] (any leading dims flattened by the caller), W_u [r, d, d] with
+    W_u[i][j][m] the weight of input m in output j; returns u [N, r, d] in float64.
+    """
+    k_raw, W_u = _f64(k_raw), _f64(W_u)
+    x = np.einsum("ijm,nm->nij", W_u, k_raw)
+    return x / np.maximum(np.linalg.norm(x, axis=-1, keepdims=True), NORM_EPS)
+
+
 def errors(o, A, S, n, o_ref, A_ref, S_ref, n_ref):
     """Scale-aware errors used by the parity gates.
 

@@ -408,11 +408,36 @@ def check_delta_tracks_the_same_A(mod):
     assert np.array_equal(Aa, Ad) and np.array_equal(na, nd)
 
 
+# ---- the direction projection u = normalize(W_u k_raw) (README "VLA v3" item 2)
+
+def check_project_u_closed_forms(mod):
+    g = rng(51)
+    d, N = 7, 9
+    k = g.normal(size=(N, d))
+    # identity: the keys' own directions
+    u = mod.project_u(k, np.eye(d)[None])
+    assert rel(u[:, 0], k / np.linalg.norm(k, axis=1, keepdims=True)) < 1e-15
+    # a permutation permutes the unit vector; a positive scale changes nothing
+    perm = g.permutation(d)
+    Pm = np.eye(d)[perm]
+    u2 = mod.project_u(k, np.stack([Pm, 3.5 * Pm]))
+    want = (k / np.linalg.norm(k, axis=1, keepdims=True))[:, perm]
+    assert rel(u2[:, 0], want) < 1e-15 and rel(u2[:, 1], want) < 1e-15
+    # a zero key gives a zero direction (the 1e-12 floor), not NaN
+    z = mod.project_u(np.zeros((1, d)), np.eye(d)[None])
+    assert np.array_equal(z, np.zeros((1, 1, d)))
+    # rank-one W: every output is +-w / |w| according to the sign of a.k
+    a, w = g.normal(size=d), g.normal(size=d)
+    u3 = mod.project_u(k, np.outer(w, a)[None])[:, 0]
+    sgn = np.sign(k @ a)[:, None]
+    assert rel(u3, sgn * w / np.linalg.norm(w)) < 1e-14
+
+
 CHECKS = [check_golden_worked, check_exact_rational, check_gauss_jordan, check_d1_closed_form,
           check_basis_cycling, check_woodbury_rank_r, check_ldl_pivots, check_alpha_least_squares,
           check_invariants, check_guard, check_renorm, check_split_calls,
           check_readout_bruteforce, check_phi, check_delta_d1_overwrite, check_delta_residual_contraction,
-          check_delta_orthogonal_untouched, check_delta_tracks_the_same_A]
+          check_delta_orthogonal_untouched, check_delta_tracks_the_same_A, check_project_u_closed_forms]
 
 
 @pytest.mark.parametrize("check", CHECKS, ids=lambda c: c.__name__)
@@ -522,6 +547,10 @@ MUTATIONS = {
                                 "ak = np.matmul(A, k[:, t, :, None])[:, :, 0]"),
     "delta_outer_transposed": ("S = S + resid[:, :, None] * gate[:, None, :]",
                                "S = S + (gate[:, :, None] * resid[:, None, :]).reshape(S.shape)"),
+    # direction projection
+    "project_transposed_W": ('x = np.einsum("ijm,nm->nij", W_u, k_raw)', 'x = np.einsum("imj,nm->nij", W_u, k_raw)'),
+    "project_no_normalise": ("return x / np.maximum(np.linalg.norm(x, axis=-1, keepdims=True), NORM_EPS)",
+                             "return x"),
 }
 
 
