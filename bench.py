@@ -234,6 +234,46 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
+def run_project_u(args, w):
+    """Time vla_project_u (u = normalize(W_u k_raw)) over the workload's B H T keys."""
+    import sherman_morrison_inverse_gb300 as vla
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    x = workloads.make_inputs(w, pairs=[0], T=w.T)
+    n = w.B * w.H * w.T
+    k = x["k"][0].to(dev).repeat(w.B * w.H, 1).contiguous()          # [B H T, d] keys (pair 0's, repeated)
+    W = x["Wu"].to(dev)
+    u = torch.empty((n, w.r, w.d), dtype=k.dtype, device=dev)
+    h = vla.Handle(0)
+    for _ in range(args.warmup):
+        h.project_u(k, W, u)
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(0)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        h.project_u(k, W, u)
+    e1.record()
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    peaks = load_peaks()
+    peak_tf, peak_how = fp32_peak_tflops(peaks)
+    flops = 2 * w.r * w.d * w.d * n
+    nbytes = n * (w.d + w.r * w.d) * k.element_size()
+    line = {"metric": "u projection tokens/s (normalize(W_u k_raw))", "value": n / (ms / 1e3), "unit": "tokens/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "tokens": n, "d": w.d, "r": w.r, "io": w.io, "op": "project_u"},
+            "roofline": {"bound": "alu", "achieved": flops / (ms / 1e3) / 1e12, "peak": peak_tf, "unit": "TFLOP/s",
+                         "frac": flops / (ms / 1e3) / 1e12 / peak_tf, "traffic": None, "peak_how": peak_how,
+                         "hbm_gbs": nbytes / (ms / 1e3) / 1e9,
+                         "hbm_frac": nbytes / (ms / 1e3) / 1e9 / float(peaks["hbm_gbs"])},
+            "clocks": clk, "gpu_launches": args.steps}
+    print(json.dumps(line), flush=True)
+    h.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -245,6 +285,8 @@ def main():
                     help="auto: the chunked tensor-core kernel where it is built (d = d_v = 64, bf16 I/O, "
                          "r = 1 or 4), else the sequential one; delta: the delta-rule variant")
     ap.add_argument("--chunk", type=int, default=0)
+    ap.add_argument("--op", choices=["scan", "project_u"], default="scan",
+                    help="project_u: time the direction projection u = normalize(W_u k_raw) instead")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--T", type=int, default=None,
@@ -259,6 +301,9 @@ def main():
         args.mode = "chunked" if (w.d == 64 and w.dv == 64 and w.io == "bf16" and w.r in (1, 4)) else "sequential"
     if args.impl == "reference":
         run_reference(args, w)
+        return
+    if args.op == "project_u":
+        run_project_u(args, w)
         return
 
     import sherman_morrison_inverse_gb300 as vla

@@ -127,6 +127,22 @@ vla_err_t vla_scan_fwd(vla_handle_t h,
                        vla_dtype_t io_dtype, vla_mode_t mode, int chunk,
                        void* stream);
 
+/* The learned penalty directions before the scan: for every token t < n_tokens and
+ * rank i < r,  u[t][i] = W_u[i] k_raw[t] / max(|W_u[i] k_raw[t]|_2, 1e-12)  (README
+ * "VLA v3" item 2, "u_t = normalize(W_u k_t^raw)"), in float32 arithmetic.
+ *
+ *   k_raw     [n_tokens, d] in io_dtype: the keys before the feature map (for the scan's
+ *             layout, n_tokens = B H T and k_raw is the [B, H, T, d] tensor).
+ *   W_u       [r, d, d] float32 on the device, row-major: W_u[i][j][m] weighs input m
+ *             in output j; one set of weights for every token.
+ *   u         [n_tokens, r, d] in io_dtype, written: exactly the scan's u input.
+ *   d         16, 64 or 128;  r  1..8.
+ * Asynchronous on `stream`; the caller owns every buffer.  Errors (before any launch):
+ * INVALID_ARG for a NULL handle or pointer, n_tokens < 0, r outside 1..8; UNSUPPORTED
+ * for other d; CUDA if the launch fails. */
+vla_err_t vla_project_u(vla_handle_t h, const void* k_raw, const float* W_u, void* u, long long n_tokens,
+                        int d, int r, vla_dtype_t io_dtype, void* stream);
+
 /* Synchronise `stream`, copy the accumulated status into *out and reset it.
  * Errors: INVALID_ARG (NULL argument), CUDA. */
 vla_err_t vla_status(vla_handle_t h, void* stream, vla_status_t* out);

@@ -20,7 +20,7 @@ import threading
 
 import torch
 
-__all__ = ["scan_fwd", "Handle", "VlaError", "library_path", "load_library",
+__all__ = ["scan_fwd", "project_u", "Handle", "VlaError", "library_path", "load_library",
            "STATUS_NONFINITE", "STATUS_TIMEOUT", "SEQUENTIAL", "CHUNKED", "DELTA"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -81,6 +81,8 @@ def load_library():
         lib.vla_scan_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, cll, ci, ci, ci,
                                              ci, cf, cf, cll, ci, vp, vp]
         lib.vla_scan_fwd_noalloc.restype = ci
+        lib.vla_project_u.argtypes = [vp, vp, vp, vp, cll, ci, ci, ci, vp]
+        lib.vla_project_u.restype = ci
         _lib = lib
         return lib
 
@@ -133,6 +135,31 @@ class Handle:
                     timeout=bool(st.flags & STATUS_TIMEOUT), guard_count=st.guard_count,
                     renorm_count=st.renorm_count, chunk_fallbacks=st.chunk_fallbacks)
 
+    def project_u(self, k_raw, W_u, u=None, stream=None):
+        """u[..., i, :] = normalize(W_u[i] k_raw[...]) (README "VLA v3" item 2); k_raw [..., d]
+        float32 or bfloat16, W_u [r, d, d] float32; returns u [..., r, d] in k_raw's dtype."""
+        d = k_raw.shape[-1]
+        if W_u.dim() != 3 or tuple(W_u.shape[1:]) != (d, d) or W_u.dtype != torch.float32:
+            raise ValueError("W_u must be float32 [r, d, d]")
+        if k_raw.dtype not in (torch.float32, torch.bfloat16):
+            raise ValueError("k_raw must be float32 or bfloat16")
+        r = W_u.shape[0]
+        if u is None:
+            u = torch.empty((*k_raw.shape[:-1], r, d), dtype=k_raw.dtype, device=k_raw.device)
+        for name, t in (("k_raw", k_raw), ("W_u", W_u), ("u", u)):
+            if t.device != self.device:
+                raise ValueError(f"{name} is on {t.device}, the handle is on {self.device}")
+            if not t.is_contiguous():
+                raise ValueError(f"{name} must be contiguous")
+        if tuple(u.shape) != (*k_raw.shape[:-1], r, d) or u.dtype != k_raw.dtype:
+            raise ValueError("u must be [..., r, d] in k_raw's dtype")
+        n = k_raw.numel() // d
+        code = self.lib.vla_project_u(self._h, k_raw.data_ptr(), W_u.data_ptr(), u.data_ptr(), n, d, r,
+                                      F32 if k_raw.dtype == torch.float32 else BF16,
+                                      _stream_ptr(stream, self.device))
+        _check(self.lib, self._h, code)
+        return u
+
     def scan_fwd(self, q, k, v, u, A, S, n, o=None, *, P: int, eps_n: float, tau: float, t0: int = 0,
                  mode: str = "sequential", chunk: int = 0, stream=None):
         if q.dim() != 4:
@@ -179,6 +206,12 @@ def default_handle(device=None) -> Handle:
     if h is None:
         h = _default_handles[idx] = Handle(idx)
     return h
+
+
+def project_u(k_raw, W_u, u=None, *, stream=None, handle: Handle | None = None):
+    """u = normalize(W_u k_raw) on k_raw's device (see Handle.project_u)."""
+    h = handle if handle is not None else default_handle(k_raw.device)
+    return h.project_u(k_raw, W_u, u, stream=stream)
 
 
 def scan_fwd(q, k, v, u, A, S, n, o=None, *, P: int, eps_n: float, tau: float, t0: int = 0,

@@ -167,6 +167,26 @@ vla_err_t vla_scan_fwd(vla_handle_t h, const void* q, const void* k, const void*
   return VLA_OK;
 }
 
+vla_err_t vla_project_u(vla_handle_t h, const void* k_raw, const float* W_u, void* u, long long n_tokens,
+                        int d, int r, vla_dtype_t io_dtype, void* stream) {
+  if (!h) return fail(nullptr, VLA_ERR_INVALID_ARG, "vla_project_u: handle is NULL");
+  h->last_error.clear();
+  if (n_tokens < 0) return fail(h, VLA_ERR_INVALID_ARG, "vla_project_u: n_tokens < 0");
+  if (r < 1 || r > 8) return fail(h, VLA_ERR_INVALID_ARG, "vla_project_u: r must be 1..8");
+  if (io_dtype != VLA_F32 && io_dtype != VLA_BF16)
+    return fail(h, VLA_ERR_INVALID_ARG, "vla_project_u: unknown io_dtype");
+  if (n_tokens == 0) return VLA_OK;
+  if (!k_raw || !W_u || !u) return fail(h, VLA_ERR_INVALID_ARG, "vla_project_u: NULL pointer");
+  bool built = false;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = on_device(h->device, [&]() -> cudaError_t {
+    return vla::launch_project_u(d, io_dtype == VLA_BF16, k_raw, W_u, u, n_tokens, r, h->sm_count, s, &built);
+  });
+  if (!built) return fail(h, VLA_ERR_UNSUPPORTED, "vla_project_u: built for d in {16, 64, 128}");
+  if (e != cudaSuccess) return fail(h, VLA_ERR_CUDA, cuda_msg("vla_project_u: launch", e));
+  return VLA_OK;
+}
+
 vla_err_t vla_status(vla_handle_t h, void* stream, vla_status_t* out) {
   if (!h || !out) return fail(h, VLA_ERR_INVALID_ARG, "vla_status: NULL argument");
   vla::DevStatus st{};

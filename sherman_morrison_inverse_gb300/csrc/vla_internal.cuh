@@ -53,6 +53,8 @@ cudaError_t launch_seq(int d, int r, bool bf16, int ctas, const ScanArgs& a, cud
 cudaError_t launch_chunked(int d, int r, bool bf16, int chunk, const ScanArgs& a, cudaStream_t s,
                            bool* built);
 cudaError_t launch_delta(int d, int r, bool bf16, const ScanArgs& a, cudaStream_t s, bool* built);
+cudaError_t launch_project_u(int d, bool bf16, const void* k, const float* W, void* u, long long n, int r,
+                             int sm_count, cudaStream_t s, bool* built);
 
 // Message returned by vla_last_error(NULL) on the calling thread.
 void set_thread_error(const char* msg);

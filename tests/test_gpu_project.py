@@ -1,0 +1,82 @@
+"""GPU parity of the direction projection u = normalize(W_u k_raw) (vla_project_u).
+
+README "VLA v3" item 2 forms the scan's directions as u_t = normalize(W_u k_t^raw).
+The kernel computes it in float32; the float64 oracle (oracle.project_u, pinned by
+closed forms) on the same rounded keys and float32 weights, rounded to the I/O
+dtype, is the reference.  The tolerance follows from the arithmetic: a float32 dot
+product of length d errs by at most about d * 2^-24 times the sum of its terms' sizes,
+i.e. a few 1e-6 in absolute terms on a unit vector, and a bfloat16 result may round
+to the neighbour of the rounded float64 value (one unit in the last place).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from _util import ensure_built
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    ensure_built()
+    import sherman_morrison_inverse_gb300 as vla
+    vla.load_library()
+
+
+def _ref(k, W, dtype):
+    u = oracle.project_u(k.reshape(-1, k.shape[-1]), W)
+    return torch.from_numpy(u).to(dtype).double().numpy().reshape(*k.shape[:-1], W.shape[0], k.shape[-1])
+
+
+def _check(got, ref, dtype):
+    d = got.shape[-1]
+    fp32 = d * 2.0 ** -24 * 4        # the float32 summation bound on a unit vector (|W|, |k| of order 1)
+    diff = np.abs(got - ref)
+    if dtype == torch.bfloat16:   # plus one bf16 ulp of the reference value
+        bound = np.abs(ref) * 2.0 ** -7 + fp32
+    else:
+        bound = np.full_like(ref, fp32)
+    assert np.all(diff <= bound), float(np.max(diff / bound))
+
+
+@pytest.mark.parametrize("d,r,dtype,n", [(16, 1, torch.float32, 300), (64, 1, torch.bfloat16, 1000),
+                                         (64, 4, torch.float32, 257), (128, 1, torch.bfloat16, 129),
+                                         (128, 4, torch.float32, 77)])
+def test_projection_matches_oracle(d, r, dtype, n):
+    import sherman_morrison_inverse_gb300 as vla
+    g = np.random.default_rng([d, r, n])
+    k = torch.from_numpy(g.normal(size=(n, d))).to(dtype)
+    W = torch.from_numpy(g.normal(size=(r, d, d)) / np.sqrt(d)).float()
+    u = vla.project_u(k.cuda(), W.cuda()).double().cpu().numpy()
+    _check(u, _ref(k.double().numpy(), W.double().numpy(), dtype), dtype)
+
+
+def test_projection_of_the_recall_workload_keys():
+    """The recall workload's keys and W_u ([B, H, T, d] keys, B H T tokens), all tokens."""
+    import sherman_morrison_inverse_gb300 as vla
+    w = workloads.get(2)
+    x = workloads.make_inputs(w, pairs=[0, 1, 2], T=4096)
+    k = x["k"]   # [3, T, d] bf16
+    u = vla.project_u(k.cuda(), x["Wu"].cuda()).double().cpu().numpy()
+    _check(u, _ref(k.double().numpy(), x["Wu"].double().numpy(), torch.bfloat16), torch.bfloat16)
+
+
+def test_zero_keys_give_zero_directions_and_n0_is_a_no_op():
+    import sherman_morrison_inverse_gb300 as vla
+    k = torch.zeros((5, 64), device="cuda")
+    W = torch.eye(64, device="cuda")[None]
+    assert torch.count_nonzero(vla.project_u(k, W)) == 0
+    empty = torch.empty((0, 64), device="cuda")
+    assert vla.project_u(empty, W).shape == (0, 1, 64)
+
+
+def test_projection_rejects_unbuilt_width():
+    import sherman_morrison_inverse_gb300 as vla
+    with pytest.raises(vla.VlaError, match="UNSUPPORTED"):
+        vla.project_u(torch.zeros((4, 32), device="cuda"), torch.zeros((1, 32, 32), device="cuda"))

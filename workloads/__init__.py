@@ -159,7 +159,8 @@ def make_inputs(w: Workload | int | str, pairs: Sequence[int] | None = None,
 
     Returns a dict with q, k [N, T, d], v [N, T, dv], u [N, T, r, d] in the I/O
     dtype (N = number of selected pairs, in the order given) and A0 [N, d, d],
-    S0 [N, dv, d], n0 [N, d] in float32, plus ``pairs`` and ``workload``.
+    S0 [N, dv, d], n0 [N, d] in float32, Wu [r, d, d] (the shared projection
+    weights, float32), plus ``pairs`` and ``workload``.
     ``T`` truncates the sequence (the first T steps; identical prefix values).
     """
     w = get(w)
@@ -186,7 +187,8 @@ def make_inputs(w: Workload | int | str, pairs: Sequence[int] | None = None,
     A0 = torch.eye(w.d, dtype=torch.float32).expand(N, w.d, w.d).contiguous()
     S0 = torch.zeros((N, w.dv, w.d), dtype=torch.float32)
     n0 = torch.zeros((N, w.d), dtype=torch.float32)
-    return dict(q=q, k=k, v=v, u=u, A0=A0, S0=S0, n0=n0, pairs=pairs, workload=w)
+    Wu_f32 = torch.from_numpy(np.ascontiguousarray(Wu)).float()   # [r, d, d], the shared projection weights
+    return dict(q=q, k=k, v=v, u=u, A0=A0, S0=S0, n0=n0, Wu=Wu_f32, pairs=pairs, workload=w)
 
 
 def gaussian_inputs(N: int, T: int, d: int, dv: int, r: int, io: str, seed: int,
