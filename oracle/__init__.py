@@ -7,7 +7,9 @@ the CUDA path; the two meet only in the seeded inputs of ``workloads``.
 
 Modules
 -------
-``vla_ref``   the sequential recurrence, step by step, as the pages state it.
+``vla_ref``   the sequential recurrence, step by step, as the pages state it
+              (additive state write, and the delta-rule variant with
+              ``rule="delta"``), and the direction projection ``project_u``.
 ``woodbury``  the same recurrence taken a chunk of steps at a time in exact
               Woodbury / LDL^T form (the design the chunked GPU kernel follows),
               checked against ``vla_ref`` by the tests.

@@ -51,7 +51,7 @@ import numpy as np
 
 GUARD_EPS = 1e-6     # singularity threshold and injected diagonal (Mathematical Primitives §2)
 NORM_EPS = 1e-12     # floor of the norms in unit-length vectors (delta-rule variant)
-READOUT_EPS = 1e-6   # readout denominator offset (spec reading of the README's calibrated readout)
+READOUT_EPS = 1e-6   # readout denominator offset (the reading adopted for the README's calibrated readout)
 
 
 def phi(x):
