@@ -289,6 +289,8 @@ def main():
                     help="project_u: time the direction projection u = normalize(W_u k_raw) instead")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--seg", type=int, default=0,
+                    help="steps per window of the host-buffer (e2e) path; 0 = the library's choice")
     ap.add_argument("--T", type=int, default=None,
                     help="truncate the sequence (profiling a smaller case; not a bench number)")
     args = ap.parse_args()
@@ -350,34 +352,36 @@ def main():
     value = job_value(B * H * T * args.steps, world, ms_max)
     ms_per_step = ms_max / args.steps
 
-    # ---- end to end: pinned host buffers -> device, scan, result back, every step
+    # ---- end to end through the host-buffer entry point: every step copies q, k, v, u and
+    # the state in from page-locked host memory and o and the state back, pipelined with
+    # the scan window by window inside the library
     e2e_steps = args.e2e_steps or max(3, args.steps // 4)
     host = {k: x[k].reshape(B, H, *x[k].shape[1:]).contiguous().pin_memory() for k in ("q", "k", "v", "u")}
     host_state = {"A": x["A0"].reshape(B, H, w.d, w.d).contiguous().pin_memory(),
                   "S": x["S0"].reshape(B, H, w.dv, w.d).contiguous().pin_memory(),
                   "n": x["n0"].reshape(B, H, w.d).contiguous().pin_memory()}
     host_o = torch.empty_like(o, device="cpu").pin_memory()
-    host_out_state = {k: torch.empty_like(v).pin_memory() for k, v in host_state.items()}
     h2d = sum(t.numel() * t.element_size() for t in list(host.values()) + list(host_state.values()))
     d2h = host_o.numel() * host_o.element_size() + sum(t.numel() * t.element_size()
-                                                       for t in host_out_state.values())
-    dev_state = {"A": A, "S": S, "n": n}
+                                                       for t in host_state.values())
+    hkw = dict(kw, seg=args.seg, stream=stream, wait=False)
+    h.scan_fwd_host(host["q"], host["k"], host["v"], host["u"], host_state["A"], host_state["S"],
+                    host_state["n"], host_o, t0=0, **hkw)   # warm-up: allocates the workspace
+    torch.cuda.synchronize(dev)
+    h.status()
     barrier(dist)
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
+    te = T
     for _ in range(e2e_steps):
-        for k2 in g:
-            g[k2].copy_(host[k2], non_blocking=True)
-        for k2 in dev_state:
-            dev_state[k2].copy_(host_state[k2], non_blocking=True)
-        h.scan_fwd(g["q"], g["k"], g["v"], g["u"], A, S, n, o, t0=0, **kw)
-        host_o.copy_(o, non_blocking=True)
-        for k2 in dev_state:
-            host_out_state[k2].copy_(dev_state[k2], non_blocking=True)
+        h.scan_fwd_host(host["q"], host["k"], host["v"], host["u"], host_state["A"], host_state["S"],
+                        host_state["n"], host_o, t0=te, **hkw)
+        te += T
     e1.record(stream)
     torch.cuda.synchronize(dev)
     barrier(dist)
+    host_info = h.host_path_info()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
     e2e_value = job_value(B * H * T * e2e_steps, world, e2e_ms)
     st_e2e = h.status()
@@ -415,7 +419,11 @@ def main():
         "clocks": clk,
         "gpu_launches": args.steps,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps},
+                "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps,
+                "api": "scan_fwd_host: windows of the sequence copied in, scanned and copied out "
+                       "in a pipeline", "seg": host_info["seg"],
+                "copy_in": "SM gather from mapped page-locked memory" if host_info["gathered"] == 1
+                           else "copy engines (cudaMemcpy2DAsync)"},
         "status": {"warmup": st_warm, "timed": st, "e2e": st_e2e},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -127,6 +127,56 @@ vla_err_t vla_scan_fwd(vla_handle_t h,
                        vla_dtype_t io_dtype, vla_mode_t mode, int chunk,
                        void* stream);
 
+/* The same scan as vla_scan_fwd with every buffer in HOST memory: q, k, v, u are
+ * read from the host, o is written there, and A, S, n are read at the start and
+ * written back at the end.  All arguments but `seg` mean what they mean for
+ * vla_scan_fwd, with the same layouts; nothing needs any alignment.
+ *
+ * The sequence is cut into windows of `seg` steps (0 = the library's choice: the
+ * whole sequence up to 2048 steps, else about 16 windows of a multiple of 64 steps
+ * and at least 1024, larger for the copy engines; see below).  Each window of
+ * q, k, v, u is copied in on a copy stream of the handle, scanned on `stream`, and
+ * its o copied out on a second copy stream, so that the copies of one window
+ * overlap the scan of its neighbours.  The state stays
+ * on the device between windows and `t0` advances window by window, so the result is
+ * that of vla_scan_fwd called once per window.
+ *
+ * Copy-in.  When each of q, k, v, u lies inside one page-locked host allocation
+ * that CUDA maps into the device's address space (cudaHostAlloc, or cudaHostRegister
+ * with mapping, which unified addressing gives every page-locked buffer) and starts
+ * on a 16-byte boundary, a small gather kernel on the copy stream reads each window
+ * through that mapping, on the SMs the scan leaves idle.  Otherwise the copy engines
+ * move each window (cudaMemcpy2DAsync), and the default window grows to rows of at
+ * least 512 KB: the engines lose about half their rate on narrower rows of several
+ * tensors.  Copies from or to pageable memory are correct but do not overlap the
+ * scan.  o and the state always go through the copy engines.  The call is
+ * asynchronous on `stream`: it returns once every copy and launch is enqueued;
+ * o, A, S and n are final, and the host buffers may be reused, once `stream` has
+ * reached that point (cudaStreamSynchronize).  Work the caller put on `stream`
+ * before the call, and any earlier call of this entry point on the handle, finish
+ * before the first copy starts.
+ *
+ * The handle keeps a device workspace of the state plus three windows of
+ * q, k, v, u and o (reallocated, after the previous call has finished, when a larger
+ * one is needed; freed by vla_destroy), two streams and a few events.
+ *
+ * Errors: as for vla_scan_fwd (except alignment), and INVALID_ARG for seg < 0;
+ * NOMEM when the workspace cannot be allocated (a smaller `seg` needs less);
+ * CUDA when a copy or launch cannot be enqueued.  After a CUDA error part of the
+ * work may be enqueued: synchronise `stream` before touching the buffers. */
+vla_err_t vla_scan_fwd_host(vla_handle_t h,
+                            const void* q, const void* k, const void* v, const void* u,
+                            float* A, float* S, float* n, void* o,
+                            int B, int H, long long T, int d, int dv, int r,
+                            int P, float eps_n, float tau, long long t0,
+                            vla_dtype_t io_dtype, vla_mode_t mode, int chunk, long long seg,
+                            void* stream);
+
+/* How the last vla_scan_fwd_host call on the handle moved its inputs: *gathered = 1
+ * for the SM gather, 0 for the copy engines, -1 before any such call; *seg = the
+ * window it used (steps).  Errors: INVALID_ARG for a NULL argument. */
+vla_err_t vla_host_path_info(vla_handle_t h, int* gathered, long long* seg);
+
 /* The learned penalty directions before the scan: for every token t < n_tokens and
  * rank i < r,  u[t][i] = W_u[i] k_raw[t] / max(|W_u[i] k_raw[t]|_2, 1e-12)  (README
  * "VLA v3" item 2, "u_t = normalize(W_u k_t^raw)"), in float32 arithmetic.
@@ -153,7 +203,8 @@ vla_err_t vla_status(vla_handle_t h, void* stream, vla_status_t* out);
  * vla_scan_fwd_noalloc on this thread. */
 const char* vla_last_error(vla_handle_t h);
 
-/* Free the handle and its status block (synchronises its device first).
+/* Free the handle, its status block and the workspace of vla_scan_fwd_host
+ * (synchronises its device first).
  * h == NULL is a no-op that returns VLA_OK. */
 vla_err_t vla_destroy(vla_handle_t h);
 

@@ -11,6 +11,11 @@ kernels.  There is no fallback: without the built library every call raises.
 q, k [B, H, T, d] and v [B, H, T, d_v] and u [B, H, T, r, d] are CUDA tensors of
 one dtype (float32 or bfloat16); A [B, H, d, d], S [B, H, d_v, d], n [B, H, d]
 are float32 CUDA tensors updated in place; o [B, H, T, d_v] is returned.
+
+    o = scan_fwd_host(q, k, v, u, A, S, n, P=1024, eps_n=1e-6, tau=1e4)
+
+takes the same tensors in (page-locked) host memory and pipelines the copies in
+and out with the scan, window by window of the sequence.
 """
 from __future__ import annotations
 
@@ -20,7 +25,7 @@ import threading
 
 import torch
 
-__all__ = ["scan_fwd", "project_u", "Handle", "VlaError", "library_path", "load_library",
+__all__ = ["scan_fwd", "scan_fwd_host", "project_u", "Handle", "VlaError", "library_path", "load_library",
            "STATUS_NONFINITE", "STATUS_TIMEOUT", "SEQUENTIAL", "CHUNKED", "DELTA"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -81,6 +86,11 @@ def load_library():
         lib.vla_scan_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, cll, ci, ci, ci,
                                              ci, cf, cf, cll, ci, vp, vp]
         lib.vla_scan_fwd_noalloc.restype = ci
+        lib.vla_scan_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, cll, ci, ci, ci,
+                                          ci, cf, cf, cll, ci, ci, ci, cll, vp]
+        lib.vla_scan_fwd_host.restype = ci
+        lib.vla_host_path_info.argtypes = [vp, ctypes.POINTER(ci), ctypes.POINTER(cll)]
+        lib.vla_host_path_info.restype = ci
         lib.vla_project_u.argtypes = [vp, vp, vp, vp, cll, ci, ci, ci, vp]
         lib.vla_project_u.restype = ci
         _lib = lib
@@ -160,8 +170,9 @@ class Handle:
         _check(self.lib, self._h, code)
         return u
 
-    def scan_fwd(self, q, k, v, u, A, S, n, o=None, *, P: int, eps_n: float, tau: float, t0: int = 0,
-                 mode: str = "sequential", chunk: int = 0, stream=None):
+    @staticmethod
+    def _scan_shapes(q, k, v, u, A, S, n, o, device, pin: bool):
+        """Check the scan's tensors against the C layouts; allocate o (on `device`) if None."""
         if q.dim() != 4:
             raise ValueError("q must be [B, H, T, d]")
         B, H, T, d = q.shape
@@ -174,24 +185,58 @@ class Handle:
                 "u": (u, (B, H, T, r, d), io), "A": (A, (B, H, d, d), torch.float32),
                 "S": (S, (B, H, dv, d), torch.float32), "n": (n, (B, H, d), torch.float32)}
         if o is None:
-            o = torch.empty((B, H, T, dv), dtype=io, device=q.device)
+            o = torch.empty((B, H, T, dv), dtype=io, device=device, pin_memory=pin)
         want["o"] = (o, (B, H, T, dv), io)
         for name, (t, shape, dt) in want.items():
             if tuple(t.shape) != tuple(shape):
                 raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
             if t.dtype != dt:
                 raise ValueError(f"{name} has dtype {t.dtype}, expected {dt}")
-            if t.device != self.device:
-                raise ValueError(f"{name} is on {t.device}, the handle is on {self.device}")
+            if t.device != device:
+                raise ValueError(f"{name} is on {t.device}, expected {device}")
             if not t.is_contiguous():
                 raise ValueError(f"{name} must be contiguous")
+        return (B, H, T, d, dv, r, F32 if io == torch.float32 else BF16), o
+
+    def scan_fwd(self, q, k, v, u, A, S, n, o=None, *, P: int, eps_n: float, tau: float, t0: int = 0,
+                 mode: str = "sequential", chunk: int = 0, stream=None):
+        """The scan on device tensors (asynchronous on `stream`); A, S, n are updated in place."""
+        (B, H, T, d, dv, r, io), o = self._scan_shapes(q, k, v, u, A, S, n, o, self.device, False)
         mode_i = {"sequential": SEQUENTIAL, "chunked": CHUNKED, "delta": DELTA}[mode]
         code = self.lib.vla_scan_fwd(
             self._h, q.data_ptr(), k.data_ptr(), v.data_ptr(), u.data_ptr(),
             A.data_ptr(), S.data_ptr(), n.data_ptr(), o.data_ptr(),
             B, H, T, d, dv, r, int(P), float(eps_n), float(tau), int(t0),
-            F32 if io == torch.float32 else BF16, mode_i, int(chunk), _stream_ptr(stream, self.device))
+            io, mode_i, int(chunk), _stream_ptr(stream, self.device))
         _check(self.lib, self._h, code)
+        return o
+
+    def host_path_info(self) -> dict:
+        """How the last scan_fwd_host call moved its inputs: {"gathered": 1 (SM gather),
+        0 (copy engines) or -1 (no call yet), "seg": window in steps}."""
+        g, sg = ctypes.c_int(), ctypes.c_longlong()
+        _check(self.lib, self._h, self.lib.vla_host_path_info(self._h, ctypes.byref(g), ctypes.byref(sg)))
+        return {"gathered": g.value, "seg": sg.value}
+
+    def scan_fwd_host(self, q, k, v, u, A, S, n, o=None, *, P: int, eps_n: float, tau: float, t0: int = 0,
+                      mode: str = "sequential", chunk: int = 0, seg: int = 0, stream=None, wait: bool = True):
+        """The scan on CPU tensors (page-locked ones let the copies overlap the scan): windows
+        of `seg` steps are copied in, scanned and copied out in a pipeline on the handle's
+        device.  A, S, n are updated in place; o (page-locked if allocated here) is returned.
+        With wait=False the call returns once the work is enqueued on `stream`, and the
+        results are final after that stream is synchronised."""
+        cpu = torch.device("cpu")
+        (B, H, T, d, dv, r, io), o = self._scan_shapes(q, k, v, u, A, S, n, o, cpu, True)
+        mode_i = {"sequential": SEQUENTIAL, "chunked": CHUNKED, "delta": DELTA}[mode]
+        st = _stream_ptr(stream, self.device)
+        code = self.lib.vla_scan_fwd_host(
+            self._h, q.data_ptr(), k.data_ptr(), v.data_ptr(), u.data_ptr(),
+            A.data_ptr(), S.data_ptr(), n.data_ptr(), o.data_ptr(),
+            B, H, T, d, dv, r, int(P), float(eps_n), float(tau), int(t0),
+            io, mode_i, int(chunk), int(seg), st)
+        _check(self.lib, self._h, code)
+        if wait:
+            (stream or torch.cuda.current_stream(self.device)).synchronize()
         return o
 
 
@@ -220,3 +265,12 @@ def scan_fwd(q, k, v, u, A, S, n, o=None, *, P: int, eps_n: float, tau: float, t
     h = handle if handle is not None else default_handle(q.device)
     return h.scan_fwd(q, k, v, u, A, S, n, o, P=P, eps_n=eps_n, tau=tau, t0=t0, mode=mode, chunk=chunk,
                       stream=stream)
+
+
+def scan_fwd_host(q, k, v, u, A, S, n, o=None, *, P: int, eps_n: float, tau: float, t0: int = 0,
+                  mode: str = "sequential", chunk: int = 0, seg: int = 0, stream=None, wait: bool = True,
+                  device=None, handle: Handle | None = None):
+    """Run the scan on host tensors through the device `device` (see Handle.scan_fwd_host)."""
+    h = handle if handle is not None else default_handle(device)
+    return h.scan_fwd_host(q, k, v, u, A, S, n, o, P=P, eps_n=eps_n, tau=tau, t0=t0, mode=mode,
+                           chunk=chunk, seg=seg, stream=stream, wait=wait)

@@ -55,6 +55,13 @@ cudaError_t launch_chunked(int d, int r, bool bf16, int chunk, const ScanArgs& a
 cudaError_t launch_delta(int d, int r, bool bf16, const ScanArgs& a, cudaStream_t s, bool* built);
 cudaError_t launch_project_u(int d, bool bf16, const void* k, const float* W, void* u, long long n, int r,
                              int sm_count, cudaStream_t s, bool* built);
+// Gather the window [off, off + tj) of four [pairs, T, w_bytes[i]] host tensors (read
+// through the device addresses src[i] of page-locked host memory) into dense
+// [pairs, tj, w_bytes[i]] device buffers dst[i]; w_bytes[i] and all pointers 16-byte
+// aligned.  `ctas` CTAs of 1024 threads.
+cudaError_t launch_gather_window(const void* const src[4], void* const dst[4], const long long w_bytes[4],
+                                 long long pairs, long long T, long long off, long long tj, int ctas,
+                                 cudaStream_t s);
 
 // Message returned by vla_last_error(NULL) on the calling thread.
 void set_thread_error(const char* msg);
