@@ -109,9 +109,11 @@ vla_err_t vla_create(vla_handle_t* h, int device);
  *   chunk     VLA_CHUNKED: steps per chunk (0 = the built default).
  *             VLA_SEQUENTIAL: CTAs per (batch, head) pair: 1 = one CTA holds
  *             both halves of the step; 2 = a cluster of two CTAs on two SMs, one
- *             tracking A, the other S (same arithmetic, the same results bit for
- *             bit); 0 = two for d == 128 while 2 B H CTAs fit on the device's
- *             SMs, else one.
+ *             tracking A, the other S (the same arithmetic and the same results
+ *             bit for bit, except at d == 128, r == 1, where the cluster takes 4
+ *             steps per reduction round and one CTA 2: equal up to rounding);
+ *             0 = two for d == 128 while 2 B H CTAs fit on the device's SMs, else
+ *             one.
  *   stream    cudaStream_t as void*.
  *
  * Errors (returned before any launch, nothing is written): INVALID_ARG for a

@@ -2,11 +2,14 @@
 
 With `chunk` = 2 in sequential mode each (batch, head) pair runs on a cluster of
 two CTAs: one tracks A, the other S, and alpha crosses between their shared
-memories.  It is the same arithmetic as the one-CTA kernel (`chunk` = 1), so
-every output and state element must agree bit for bit; the cluster path is also
-checked against the float64 oracle on the long-context d = 128 workload and on
-the edge cases (ragged tiles, nudges with a t0 phase, renormalisation that fires,
-the singularity guard and its replay, split calls).
+memories.  Where both variants take the same steps per reduction round (d <= 64,
+and r = 4) it is the same arithmetic as the one-CTA kernel (`chunk` = 1), so every
+output and state element must agree bit for bit.  At d = 128, r = 1 the cluster
+takes 4-step rounds and the single CTA 2-step ones: the two then agree to the
+float32 gate.  The cluster path is also checked against the float64 oracle on the
+long-context d = 128 workload and on the edge cases (ragged tiles, nudges with a
+t0 phase, renormalisation that fires, the singularity guard and its replay, split
+calls).
 """
 from __future__ import annotations
 
@@ -43,20 +46,37 @@ CASES = [
     (4, 517, 64, 1, "bf16", 1024, 8.0, 0),     # renormalisation fires
     (3, 129, 64, 4, "f32", 40, 1e4, 3),
     (2, 300, 128, 1, "f32", 64, 1e3, 0),
+    (2, 301, 128, 1, "bf16", 60, 6.0, 9),      # 4-step rounds: ragged tail, nudges, renormalisation
     (2, 77, 128, 4, "bf16", 16, 3.0, 1),
 ]
 
 
+def _same_rounds(d, r):
+    """True where the cluster and the single CTA take the same steps per round."""
+    return not (d == 128 and r == 1)
+
+
+def _close(a, b, tol, label):
+    import oracle
+    e = oracle.errors(*a[:4], *b[:4])
+    assert max(e.values()) <= tol, (label, e)
+    assert a[4]["flags"] == b[4]["flags"] == 0, (label, a[4], b[4])
+
+
 @pytest.mark.parametrize("N,T,d,r,io,P,tau,t0", CASES)
-def test_cluster_matches_one_cta_bit_for_bit(N, T, d, r, io, P, tau, t0):
+def test_cluster_matches_one_cta(N, T, d, r, io, P, tau, t0):
     x = workloads.gaussian_inputs(N, T, d, d, r, io, seed=900 + d + r + T)
     kw = dict(P=P, eps_n=1e-3, tau=tau, t0=t0)
     one = gpu_scan(x, 1, N, chunk=1, **kw)
     two = gpu_scan(x, 1, N, chunk=2, **kw)
-    _same(one, two, f"N{N} T{T} d{d} r{r} {io}")
+    tol = 1e-4 if io == "f32" else 2e-2
+    if _same_rounds(d, r):
+        _same(one, two, f"N{N} T{T} d{d} r{r} {io}")
+    else:
+        _close(one, two, tol, f"N{N} T{T} d{d} r{r} {io}")
     ref = oracle_scan(x, **kw)
     e = errs(two, ref)
-    assert max(e.values()) <= (1e-4 if io == "f32" else 2e-2), e
+    assert max(e.values()) <= tol, e
 
 
 def test_cluster_guard_and_replay():
@@ -86,7 +106,7 @@ def test_cluster_long_context_workload_sampled():
     e = errs(got, ref, idx=[0, 11])
     assert max(e.values()) <= 1e-3, e
     one = gpu_scan(x, w.B, w.H, chunk=1, **kw)
-    _same(one, got, "workload 3 prefix")
+    _close(one, got, 1e-3, "workload 3 prefix")     # 2-step against 4-step rounds
 
 
 def test_cluster_split_calls_continue_the_state():
