@@ -24,10 +24,12 @@
 // layout, free of bank conflicts.  The one transposed operand (alpha^T) is
 // written with a per-lane register rotation that spreads the lanes over all banks.
 //
-// LDL^T and L^{-1} run in 16 x 16 blocks: one warp factors a diagonal block in
-// registers (shuffles, no barriers) and inverts its unit-lower factor, all 256
-// threads form the panel and the trailing update, and the off-diagonal blocks of
-// L^{-1} follow from (L^{-1})_ij = -L_ii^{-1} sum_m L_im (L^{-1})_mj by block diagonals.
+// LDL^T and L^{-1} run in 16 x 16 blocks, right-looking, with L^{-1} carried along
+// as the forward elimination of the identity: one warp factors a diagonal block as
+// 2 x 2 blocks of 8 in registers and inverts its unit-lower factor there, 192
+// threads multiply that inverse into the panel and the eliminated identity's
+// blocks, and the trailing update of one block column runs beside the factoring of
+// the next diagonal block.
 //
 // Renormalisation: ||S_t||^2 = ||S||^2 + 2 sum v_t'^T S alpha_t' + sum (v.v)(alpha.alpha) from the
 // products above; the bound ||S|| + sum |v_t||alpha_t| decides that no step can
@@ -480,10 +482,10 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     // ---------------- LDL^T of G and X = L^{-1} in 16 x 16 blocks (fp32)
     // Right-looking block LDL^T with the inverse carried along as a forward
     // elimination of the identity.  For block column k:
-    //   [a] one warp factors the diagonal block G'_kk = L_kk D_k L_kk^T (2 x 2 blocks of 8);
-    //   [b] 64 independent forward substitutions with L_kk, one per thread: the columns
-    //       of X_kk = L_kk^{-1}, the panel rows (L D)_r = L_kk^{-1} G'_rk (i > k) and the
-    //       columns of X_kj = L_kk^{-1} B_kj (j < k);
+    //   [a] one warp factors the diagonal block G'_kk = L_kk D_k L_kk^T (2 x 2 blocks of 8)
+    //       and forms X_kk = L_kk^{-1} from the factors in its registers;
+    //   [b] the product of X_kk with 48 columns, 4 lanes a column: the panel rows
+    //       (L D)_r = X_kk G'_rk (i > k) and the columns of X_kj = X_kk B_kj (j < k);
     //   [c] trailing G'_ij -= L_ik D_k L_jk^T (k < j <= i) and B_ij -= L_ik X_kj (j <= k < i),
     // where B is the identity being eliminated (B_ij = 0 for i != j at the start).
     // [c] of step k runs beside [a] of step k + 1: warp 0 updates the next diagonal
@@ -611,7 +613,37 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
 #pragma unroll
           for (int cl = 0; cl <= r; ++cl) a1[r][cl] = Gs[(b0 + 8 + r) * GLD + b0 + 8 + cl];
         ldl8(a1, d1, id1);
-        __syncwarp();
+        // X_kk = L_kk^{-1}, column c = lane & 15 (lanes 16..31 repeat 0..15 and do not
+        // store): x_top = L00^{-1} e_c[0..7], x_bot = L11^{-1} (e_c[8..15] - L10 x_top), with
+        // L00, L11 in registers and L10 in the staging; entries above the diagonal stay 0
+        {
+          const int c = lane & 15;
+          float xt[8], xb[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            xt[i] = (i == c) ? 1.f : 0.f;
+            xb[i] = (i + 8 == c) ? 1.f : 0.f;
+          }
+#pragma unroll
+          for (int i = 1; i < 8; ++i)
+#pragma unroll
+            for (int m = 0; m < i; ++m) xt[i] = fmaf(-a8[i][m], xt[m], xt[i]);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int m = 0; m < 8; ++m) xb[i] = fmaf(-Gs[(b0 + 8 + i) * GLD + b0 + m], xt[m], xb[i]);
+#pragma unroll
+          for (int i = 1; i < 8; ++i)
+#pragma unroll
+            for (int m = 0; m < i; ++m) xb[i] = fmaf(-a1[i][m], xb[m], xb[i]);
+          if (lane < 16) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              XB[pblk(k, k) + i * 17 + c] = xt[i];
+              XB[pblk(k, k) + (8 + i) * 17 + c] = xb[i];
+            }
+          }
+        }
         if (lane == 0) {
 #pragma unroll
           for (int r = 0; r < 8; ++r) {
@@ -619,11 +651,6 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
             misc[Cf::M_ID + b0 + r] = id0[r];
             misc[Cf::M_D + b0 + 8 + r] = d1[r];
             misc[Cf::M_ID + b0 + 8 + r] = id1[r];
-#pragma unroll
-            for (int cl = 0; cl < r; ++cl) {
-              Gs[(b0 + r) * GLD + b0 + cl] = a8[r][cl];
-              Gs[(b0 + 8 + r) * GLD + b0 + 8 + cl] = a1[r][cl];
-            }
           }
         }
       } else if (k > 0 && warp != 4) {   // the rest of step k-1's [c]; warp 4 leaves warp 0's
@@ -635,40 +662,46 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
           trail_tile(kc, 1 + (q >> 5), (q >> 2) & 7, q & 3);
       }
       __syncthreads();
-      if (tid < 64) {   // [b]: chain q = tid
+      if (warp < 6) {   // [b]: Y = X_kk R for the 48 right-hand columns R, 4 lanes a column
+        // columns 0 .. npan-1: panel rows r = 16 (k+1) + col (Y = (L D)_r, stored transposed in
+        // the upper block and, times D^{-1}, as L_r); the rest: columns of B_kj, j < k (Y = X_kj)
         const int npan = 48 - 16 * k;
-        float y[16];
-        if (tid < 16) {                        // column tid of X_kk
-#pragma unroll
-          for (int m = 0; m < 16; ++m) y[m] = (m == tid) ? 1.f : 0.f;
-        } else if (tid < 16 + npan) {          // panel row r
-          const int r = 16 * (k + 1) + (tid - 16);
-#pragma unroll
-          for (int m = 0; m < 16; ++m) y[m] = Gs[r * GLD + 16 * k + m];
-        } else {                               // column of B_kj, j < k
-          const int idx = tid - 16 - npan, bj = idx >> 4, cl = idx & 15;
-#pragma unroll
-          for (int m = 0; m < 16; ++m) y[m] = XB[pblk(k, bj) + m * 17 + cl];
+        const int col = 8 * warp + (lane >> 2), g = lane & 3;   // rows 4 g .. 4 g + 3 of Y
+        float* rp;      // column col of R: element m at rp[m * rs]
+        int rs;
+        int r = 0;
+        if (col < npan) {
+          r = 16 * (k + 1) + col;
+          rp = Gs + r * GLD + 16 * k;
+          rs = 1;
+        } else {
+          const int idx = col - npan, bj = idx >> 4, cl = idx & 15;
+          rp = XB + pblk(k, bj) + cl;
+          rs = 17;
         }
-        // y <- L_kk^{-1} y (unit lower, L_kk strict lower part in the staging)
+        float rv[16];
 #pragma unroll
-        for (int m = 0; m < 15; ++m)
+        for (int m = 0; m < 16; ++m) rv[m] = rp[m * rs];
+        const float* xr = XB + pblk(k, k) + 4 * g * 17;
+        float y[4];
 #pragma unroll
-          for (int ii = m + 1; ii < 16; ++ii) y[ii] = fmaf(-Gs[(16 * k + ii) * GLD + 16 * k + m], y[m], y[ii]);
-        if (tid < 16) {
+        for (int j = 0; j < 4; ++j) {
+          float acc = 0.f;
 #pragma unroll
-          for (int m = 0; m < 16; ++m) XB[pblk(k, k) + m * 17 + tid] = y[m];
-        } else if (tid < 16 + npan) {
-          const int r = 16 * (k + 1) + (tid - 16);
+          for (int m = 0; m < 16; ++m) acc = fmaf(xr[j * 17 + m], rv[m], acc);
+          y[j] = acc;
+        }
+        __syncwarp();   // the column's 4 lanes are in this warp: all read R before any writes it
+        if (col < npan) {
 #pragma unroll
-          for (int m = 0; m < 16; ++m) {
-            Gs[(16 * k + m) * GLD + r] = y[m];                               // L D, transposed (upper block)
-            Gs[r * GLD + 16 * k + m] = y[m] * misc[Cf::M_ID + 16 * k + m];   // L
+          for (int j = 0; j < 4; ++j) {
+            const int i = 4 * g + j;
+            Gs[(16 * k + i) * GLD + r] = y[j];                             // L D, transposed (upper block)
+            rp[i] = y[j] * misc[Cf::M_ID + 16 * k + i];                    // L
           }
         } else {
-          const int idx = tid - 16 - npan, bj = idx >> 4, cl = idx & 15;
 #pragma unroll
-          for (int m = 0; m < 16; ++m) XB[pblk(k, bj) + m * 17 + cl] = y[m];
+          for (int j = 0; j < 4; ++j) rp[(4 * g + j) * 17] = y[j];
         }
       }
       __syncthreads();
