@@ -189,9 +189,10 @@ vla_err_t vla_host_path_info(vla_handle_t h, int* gathered, long long* seg);
  *             in output j; one set of weights for every token.
  *   u         [n_tokens, r, d] in io_dtype, written: exactly the scan's u input.
  *   d         16, 64 or 128;  r  1..8.
+ * k_raw, W_u and u start on 16-byte boundaries (rows move as 16-byte vectors).
  * Asynchronous on `stream`; the caller owns every buffer.  Errors (before any launch):
- * INVALID_ARG for a NULL handle or pointer, n_tokens < 0, r outside 1..8; UNSUPPORTED
- * for other d; CUDA if the launch fails. */
+ * INVALID_ARG for a NULL handle or pointer, a misaligned pointer, n_tokens < 0, r
+ * outside 1..8; UNSUPPORTED for other d; CUDA if the launch fails. */
 vla_err_t vla_project_u(vla_handle_t h, const void* k_raw, const float* W_u, void* u, long long n_tokens,
                         int d, int r, vla_dtype_t io_dtype, void* stream);
 

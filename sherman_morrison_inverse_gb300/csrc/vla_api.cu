@@ -460,6 +460,8 @@ vla_err_t vla_project_u(vla_handle_t h, const void* k_raw, const float* W_u, voi
     return fail(h, VLA_ERR_INVALID_ARG, "vla_project_u: unknown io_dtype");
   if (n_tokens == 0) return VLA_OK;
   if (!k_raw || !W_u || !u) return fail(h, VLA_ERR_INVALID_ARG, "vla_project_u: NULL pointer");
+  if (!aligned16(k_raw) || !aligned16(W_u) || !aligned16(u))
+    return fail(h, VLA_ERR_INVALID_ARG, "vla_project_u: k_raw, W_u and u must be 16-byte aligned");
   bool built = false;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = on_device(h->device, [&]() -> cudaError_t {

@@ -80,3 +80,26 @@ def test_projection_rejects_unbuilt_width():
     import sherman_morrison_inverse_gb300 as vla
     with pytest.raises(vla.VlaError, match="UNSUPPORTED"):
         vla.project_u(torch.zeros((4, 32), device="cuda"), torch.zeros((1, 32, 32), device="cuda"))
+
+
+def test_projection_rejects_misaligned_pointers():
+    """Rows move as 16-byte vectors: a key tensor that starts 2 bytes into its buffer is refused."""
+    import sherman_morrison_inverse_gb300 as vla
+    buf = torch.zeros(4 * 64 + 8, dtype=torch.bfloat16, device="cuda")
+    k = buf[1:1 + 4 * 64].view(4, 64)
+    assert k.data_ptr() % 16 != 0
+    with pytest.raises(vla.VlaError, match="INVALID_ARG"):
+        vla.project_u(k, torch.eye(64, device="cuda")[None])
+
+
+def test_projection_grid_stride_covers_every_token():
+    """More tokens than one pass of the grid (4 CTAs of 128 threads per SM): every row is
+    written, including the ragged end."""
+    import sherman_morrison_inverse_gb300 as vla
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    n = 4 * 128 * sms * 2 + 37
+    g = np.random.default_rng(5)
+    k = torch.from_numpy(g.normal(size=(n, 16))).float()
+    W = torch.from_numpy(g.normal(size=(2, 16, 16)) / 4.0).float()
+    u = vla.project_u(k.cuda(), W.cuda()).double().cpu().numpy()
+    _check(u, _ref(k.double().numpy(), W.double().numpy(), torch.float32), torch.float32)
