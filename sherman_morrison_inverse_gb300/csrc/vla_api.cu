@@ -147,15 +147,17 @@ cudaError_t dispatch(const vla::ScanArgs& a, int d, int r, bool bf16, vla_mode_t
 }
 
 // Steps per window of the host-buffer path, a multiple of 64 (whole chunks in VLA_CHUNKED
-// mode).  Gathered by the SMs: the whole sequence up to 2048 steps, else about 16 windows
-// of at least 1024 steps, so that the copy-in of one window overlaps the scan of the one
-// before and the pipeline fills and drains in a sixteenth of the sequence.  Copied by the
-// copy engines: rows of at least 512 KB (`step_bytes` = bytes a step of the narrowest
-// input takes), below which the engines lose rate when rows of four tensors alternate.
+// mode).  Gathered by the SMs: the whole sequence up to 2048 steps, else about 32 windows
+// of at least 512 steps, so that the copy-in of one window overlaps the scan of the one
+// before and the pipeline fills and drains in a thirty-second of the sequence (windows of
+// 384 to 768 steps give the same end-to-end time at T = 16384, 1024 steps 2 % more).
+// Copied by the copy engines: rows of at least 512 KB (`step_bytes` = bytes a step of the
+// narrowest input takes), below which the engines lose rate when rows of four tensors
+// alternate.
 long long default_segment(long long T, bool gathered, long long step_bytes) {
   if (T <= 2048) return T;
-  long long seg = ((T + 15) / 16 + 63) / 64 * 64;
-  if (seg < 1024) seg = 1024;
+  long long seg = ((T + 31) / 32 + 63) / 64 * 64;
+  if (seg < 512) seg = 512;
   if (!gathered) {
     const long long rows = ((512 * 1024 + step_bytes - 1) / step_bytes + 63) / 64 * 64;
     if (seg < rows) seg = rows;

@@ -111,8 +111,8 @@ def test_host_path_full_length_recall_workload():
     x = workloads.make_inputs(w, pairs=[0, 1, 2, 77])
     kw = dict(P=w.P, eps_n=w.eps_n, tau=w.tau, mode="chunked")
     got = _run_host(h, x, 1, 4, 0, **kw)
-    assert h.host_path_info() == {"gathered": 1, "seg": 1024}   # the default window at T = 16384
-    ref_dev = _device_windows(h, x, 1, 4, 1024, **kw)
+    assert h.host_path_info() == {"gathered": 1, "seg": 512}   # the default window at T = 16384
+    ref_dev = _device_windows(h, x, 1, 4, 512, **kw)
     _same(got, ref_dev, "host vs device windows, recall workload")
     ref = oracle_scan(x, idx=[0, 3], P=w.P, eps_n=w.eps_n, tau=w.tau)
     f = lambda t: t.reshape(4, *t.shape[2:]).double().numpy()
