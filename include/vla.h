@@ -67,7 +67,10 @@ typedef enum {
   VLA_DELTA = 2         /* the delta-rule variant (gist.science summary §2.3, "Recursive
                            Update Rule"): A tracked as above, then alpha_hat = A k_hat / |A k_hat|
                            with k_hat = phi(k) / |phi(k)|, S += (v - S k_hat) alpha_hat^T; n,
-                           renormalisation and readout unchanged; one step at a time */
+                           renormalisation and readout unchanged; computed in rounds of
+                           several steps like VLA_SEQUENTIAL (CTAs per pair chosen as its
+                           default), so splitting a sequence into calls gives the same bits
+                           only at multiples of the tile (32 steps at d = 64) */
 } vla_mode_t;
 
 /* Status flags, ORed over all pairs since the last vla_status() call. */

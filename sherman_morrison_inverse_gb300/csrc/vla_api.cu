@@ -99,10 +99,10 @@ bool shape_built(int d, int dv, int r, bool bf16, vla_mode_t mode, int chunk, in
 }
 
 // Argument checks shared by the device and host entry points; sets *ctas (sequential
-// mode: CTAs per pair).  By default a cluster of two for d = 128 while 2 B H CTAs fit on
-// the SMs (one CTA of 4 d threads would be capped at 128 registers a thread and spill);
-// one otherwise (at d <= 64 the hand-off between two SMs costs more than the issue slots
-// it frees).
+// and delta modes: CTAs per pair).  By default a cluster of two for d = 128 while 2 B H
+// CTAs fit on the SMs (one CTA of 4 d threads would be capped at 128 registers a thread
+// and spill); one otherwise (at d <= 64 the hand-off between two SMs costs more than the
+// issue slots it frees).
 vla_err_t check_scan(vla_handle_t h, const char* fn, int B, int H, long long T, int d, int dv, int r, int P,
                      float eps_n, float tau, long long t0, vla_dtype_t io_dtype, vla_mode_t mode, int chunk,
                      int* ctas) {
@@ -119,8 +119,8 @@ vla_err_t check_scan(vla_handle_t h, const char* fn, int B, int H, long long T, 
   const long long pairs = (long long)B * H;
   if (pairs > 0x7fffffffLL) return fail(h, VLA_ERR_INVALID_ARG, f + ": B*H too large");
   if (d != dv) return fail(h, VLA_ERR_UNSUPPORTED, f + ": built only for d == dv");
-  *ctas = (mode != VLA_SEQUENTIAL) ? 0
-          : (chunk != 0 ? chunk : ((d == 128 && 2 * pairs <= h->sm_count) ? 2 : 1));
+  const int auto_ctas = (d == 128 && 2 * pairs <= h->sm_count) ? 2 : 1;
+  *ctas = mode == VLA_SEQUENTIAL ? (chunk != 0 ? chunk : auto_ctas) : mode == VLA_DELTA ? auto_ctas : 0;
   const bool bf16 = io_dtype == VLA_BF16;
   if (!shape_built(d, dv, r, bf16, mode, chunk, *ctas)) {
     char buf[400];
@@ -141,7 +141,7 @@ cudaError_t dispatch(const vla::ScanArgs& a, int d, int r, bool bf16, vla_mode_t
                      cudaStream_t s) {
   bool built = false;
   cudaError_t e = mode == VLA_SEQUENTIAL ? vla::launch_seq(d, r, bf16, ctas, a, s, &built)
-                  : mode == VLA_DELTA    ? vla::launch_delta(d, r, bf16, a, s, &built)
+                  : mode == VLA_DELTA    ? vla::launch_delta(d, r, bf16, ctas, a, s, &built)
                                          : vla::launch_chunked(d, r, bf16, chunk, a, s, &built);
   return built ? e : cudaErrorNotSupported;
 }

@@ -1,19 +1,21 @@
-// Instantiations of the delta-rule scan kernel: d = d_v in {16, 64, 128}, r in {1, 4},
-// float32 or bfloat16 I/O.
-#include "vla_delta.cuh"
+// Dispatch of the delta-rule variant (mode VLA_DELTA) to the blocked scan kernel's
+// instantiations, one translation unit per head width.
+#include "vla_internal.cuh"
 
 namespace vla {
 
-cudaError_t launch_delta(int d, int r, bool bf16, const ScanArgs& a, cudaStream_t s, bool* built) {
-  *built = true;
-  if (d == 16 && r == 1) return bf16 ? launch_delta_t<16, 1, __nv_bfloat16>(a, s) : launch_delta_t<16, 1, float>(a, s);
-  if (d == 16 && r == 4) return bf16 ? launch_delta_t<16, 4, __nv_bfloat16>(a, s) : launch_delta_t<16, 4, float>(a, s);
-  if (d == 64 && r == 1) return bf16 ? launch_delta_t<64, 1, __nv_bfloat16>(a, s) : launch_delta_t<64, 1, float>(a, s);
-  if (d == 64 && r == 4) return bf16 ? launch_delta_t<64, 4, __nv_bfloat16>(a, s) : launch_delta_t<64, 4, float>(a, s);
-  if (d == 128 && r == 1) return bf16 ? launch_delta_t<128, 1, __nv_bfloat16>(a, s) : launch_delta_t<128, 1, float>(a, s);
-  if (d == 128 && r == 4) return bf16 ? launch_delta_t<128, 4, __nv_bfloat16>(a, s) : launch_delta_t<128, 4, float>(a, s);
-  *built = false;
-  return cudaSuccess;
+cudaError_t launch_seq_delta_d16(int r, bool bf16, bool cluster, const ScanArgs& a, cudaStream_t s, bool* built);
+cudaError_t launch_seq_delta_d64(int r, bool bf16, bool cluster, const ScanArgs& a, cudaStream_t s, bool* built);
+cudaError_t launch_seq_delta_d128(int r, bool bf16, bool cluster, const ScanArgs& a, cudaStream_t s, bool* built);
+
+cudaError_t launch_delta(int d, int r, bool bf16, int ctas, const ScanArgs& a, cudaStream_t s, bool* built) {
+  const bool cluster = ctas == 2;
+  switch (d) {
+    case 16: return launch_seq_delta_d16(r, bf16, cluster, a, s, built);
+    case 64: return launch_seq_delta_d64(r, bf16, cluster, a, s, built);
+    case 128: return launch_seq_delta_d128(r, bf16, cluster, a, s, built);
+    default: *built = false; return cudaSuccess;
+  }
 }
 
 }  // namespace vla

@@ -52,7 +52,7 @@ struct ScanArgs {
 cudaError_t launch_seq(int d, int r, bool bf16, int ctas, const ScanArgs& a, cudaStream_t s, bool* built);
 cudaError_t launch_chunked(int d, int r, bool bf16, int chunk, const ScanArgs& a, cudaStream_t s,
                            bool* built);
-cudaError_t launch_delta(int d, int r, bool bf16, const ScanArgs& a, cudaStream_t s, bool* built);
+cudaError_t launch_delta(int d, int r, bool bf16, int ctas, const ScanArgs& a, cudaStream_t s, bool* built);
 cudaError_t launch_project_u(int d, bool bf16, const void* k, const float* W, void* u, long long n, int r,
                              int sm_count, cudaStream_t s, bool* built);
 // Gather the window [off, off + tj) of four [pairs, T, w_bytes[i]] host tensors (read

@@ -34,6 +34,10 @@
 // delta itself and the guard (A += 1e-6 I instead of the update) is taken as the
 // pages state it.
 //
+// Delta-rule variant (DL = true; gist.science summary §2.3): the same A group; the S
+// group also forms X_t = S_reg s_t and the scalars alpha_t' . s_t, solves the round's
+// residuals w_t = v_t - S_{t-1} k_hat_t row by row, and writes S += w alpha_hat^T.
+//
 // Renormalisation: S = sigma * S_reg (lazy scale).  Each round reduces ||S_reg||^2
 // exactly; with |alpha_t| and |v_t| the bound ||S_t|| <= ||S_0|| + sum |v||alpha| shows
 // that no step of the chunk can exceed tau.  Otherwise an extra reduction gives the
@@ -51,6 +55,7 @@ namespace blk {
 
 constexpr float kGuardEps = 1e-6f;
 constexpr float kReadoutEps = 1e-6f;
+constexpr float kNormEps = 1e-12f;   // floor of |alpha| and |s| in the delta rule's unit vectors
 // named barriers (0 is __syncthreads)
 constexpr int BAR_A = 1, BAR_S = 2, BAR_FULL0 = 3, BAR_EMPTY0 = 5;
 
@@ -92,13 +97,14 @@ __host__ __device__ constexpr int pick_ts() {
          : smem_bytes_for<D, R, KS, TIO>(16) <= 200 * 1024 ? 16 : 8;
 }
 
-template <int D, int R, int KS, typename TIO>
+template <int D, int R, int KS, typename TIO, bool DL = false>
 struct Cfg {
   using Gm = Geom<D>;
   static constexpr int TS = pick_ts<D, R, KS, TIO>();   // steps per tile
   static constexpr int M = KS * R;                      // directions per round
   static constexpr int NVA = up2(M + KS);               // A-group vectors (P, Q, zero padding)
-  static constexpr int NVS = up2(KS);                   // S-group vectors (Y, zero padding)
+  static constexpr int NVY = DL ? 2 * KS : KS;          // S-group products: Y (and X = S_reg s_t, delta rule)
+  static constexpr int NVS = up2(NVY);                  // S-group vectors (zero padding)
   static constexpr int KVA = Gm::RPT * NVA / Gm::LPR;   // values a lane keeps after the reduce-scatter
   static constexpr int KVS = Gm::RPT * NVS / Gm::LPR;
   static_assert((Gm::RPT * NVA) % Gm::LPR == 0 && (Gm::RPT * NVS) % Gm::LPR == 0, "even split");
@@ -107,13 +113,19 @@ struct Cfg {
   static constexpr int NJH = R * KS * (KS + 1) / 2;     // u_a . Q_t, a <= e_t
   static constexpr int NJA = NJG + NJH;
   static constexpr int NJQ = KS * (KS + 1) / 2;         // alpha_t' . phi(q_t), t' <= t
-  static constexpr int NJS = NJQ + KS;                  // + alpha_t . alpha_t
+  static constexpr int NJS = NJQ + KS + (DL ? NJQ : 0); // + alpha_t . alpha_t (+ alpha_t' . s_t, t' <= t)
   static constexpr int NSA = pow2_ceil((NJA + Gm::GW - 1) / Gm::GW);   // job slots per A warp
   static constexpr int NSS = pow2_ceil((NJS + Gm::GW - 1) / Gm::GW);
   static_assert(NSA <= 32 && NSS <= 32, "one pass of job slots");
-  static constexpr int NMINI = KS + KS * (KS + 1);      // exact-norm scalars
+  // exact-norm scalars.  Additive: v_t^T S alpha_t, alpha_t . alpha_t', v_t . v_t' (t' <= t).
+  // Delta rule: v_m^T S alpha_t, X_m^T S alpha_t (all m, t), v_m . X_m' (all), v_m . v_m',
+  // X_m . X_m', alpha_t . alpha_t' (m' <= m, t' <= t).
+  static constexpr int NTRI = KS * (KS + 1) / 2;
+  static constexpr int NMINI = DL ? 3 * KS * KS + 3 * NTRI : KS + KS * (KS + 1);
+  static constexpr int MI_VSA = 0, MI_XSA = KS * KS, MI_VX = 2 * KS * KS, MI_VV = 3 * KS * KS,
+                       MI_XX = 3 * KS * KS + NTRI, MI_AA = 3 * KS * KS + 2 * NTRI;
   static constexpr int MSTR = up4(NMINI);
-  // step record (floats): u[R][D] | s[D] | phi(q)[D] | v[D] | 1/den, |v|, 0, 0
+  // step record (floats): u[R][D] | s[D] | phi(q)[D] | v[D] | 1/den, |v|, |s|, 0
   static constexpr int OFF_U = 0, OFF_S = R * D, OFF_Q = (R + 1) * D, OFF_V = (R + 2) * D;
   static constexpr int OFF_SC = (R + 3) * D;
   static constexpr int REC = (R + 3) * D + 4;
@@ -126,8 +138,8 @@ struct Cfg {
   static constexpr int F_PROD = F_ZERO + REC;              // [TS][D] prologue scratch
   static constexpr int F_P = F_PROD + TS * D;              // [2][M][D]
   static constexpr int F_Q = F_P + 2 * M * D;              // [2][KS][D]
-  static constexpr int F_Y = F_Q + 2 * KS * D;             // [2][KS][D]
-  static constexpr int F_AL = F_Y + 2 * KS * D;            // [2][KS][D]
+  static constexpr int F_Y = F_Q + 2 * KS * D;             // [2][NVY][D]
+  static constexpr int F_AL = F_Y + 2 * NVY * D;           // [2][KS][D]
   static constexpr int F_RA = F_AL + 2 * KS * D;           // [NJA]
   static constexpr int F_RS = F_RA + up4(NJA);             // [NJS]
   static constexpr int F_WP = F_RS + up4(NJS);             // [2][GW]
@@ -178,11 +190,11 @@ __device__ __forceinline__ void reduce_scatter(float (&v)[N], int lanebits) {
 //             (distributed shared memory), and the FULL / EMPTY hand-off becomes a
 //             pair of cluster-scope mbarriers per parity (every thread of the
 //             producing group arrives with release semantics; waits are bounded).
-template <int D, int R, int KS, typename TIO, bool PS = false, bool CL = false>
+template <int D, int R, int KS, typename TIO, bool PS = false, bool CL = false, bool DL = false>
 __global__ void __launch_bounds__(CL ? blk::Geom<D>::GT : blk::Geom<D>::NT, 1) seq_block_kernel(ScanArgs a) {
   using namespace blk;
   using Gm = Geom<D>;
-  using C = Cfg<D, R, KS, TIO>;
+  using C = Cfg<D, R, KS, TIO, DL>;
   constexpr int RPT = Gm::RPT, LPR = Gm::LPR, NCH = Gm::NCH, NCP = Gm::NCP, GT = Gm::GT, GW = Gm::GW;
   constexpr int NT = CL ? Gm::GT : Gm::NT, TS = C::TS, NSTAGE = Gm::NSTAGE;
   static_assert(!(PS && CL), "the per-pair status entry point runs one CTA per pair");
@@ -303,7 +315,7 @@ __global__ void __launch_bounds__(CL ? blk::Geom<D>::GT : blk::Geom<D>::NT, 1) s
       constexpr int EPT = D / TPS;
       static_assert(EPT % 4 == 0 && TPS <= 32, "den reduction layout");
       const int t = gid / TPS, part = gid - t * TPS;
-      float dn = 0.f, vv = 0.f;
+      float dn = 0.f, vv = 0.f, ss = 0.f;
       if (t < nst) {
 #pragma unroll
         for (int j = 0; j < EPT; j += 4) {
@@ -311,6 +323,10 @@ __global__ void __launch_bounds__(CL ? blk::Geom<D>::GT : blk::Geom<D>::NT, 1) s
           const float4 w = *reinterpret_cast<const float4*>(pre + t * REC + C::OFF_V + part * EPT + j);
           dn += (p.x + p.y) + (p.z + p.w);
           vv = fmaf(w.x, w.x, fmaf(w.y, w.y, fmaf(w.z, w.z, fmaf(w.w, w.w, vv))));
+          if constexpr (DL) {
+            const float4 k4 = *reinterpret_cast<const float4*>(pre + t * REC + C::OFF_S + part * EPT + j);
+            ss = fmaf(k4.x, k4.x, fmaf(k4.y, k4.y, fmaf(k4.z, k4.z, fmaf(k4.w, k4.w, ss))));
+          }
         }
       }
       // every lane of the warp takes part in the shuffles (a ragged tile leaves
@@ -319,10 +335,12 @@ __global__ void __launch_bounds__(CL ? blk::Geom<D>::GT : blk::Geom<D>::NT, 1) s
       for (int m = TPS / 2; m >= 1; m >>= 1) {
         dn += __shfl_xor_sync(0xffffffffu, dn, m);
         vv += __shfl_xor_sync(0xffffffffu, vv, m);
+        if constexpr (DL) ss += __shfl_xor_sync(0xffffffffu, ss, m);
       }
       if (t < nst && part == 0) {
         pre[t * REC + C::OFF_SC] = __frcp_rn(dn + kReadoutEps);
         pre[t * REC + C::OFF_SC + 1] = sqrtf(vv);
+        if constexpr (DL) pre[t * REC + C::OFF_SC + 2] = sqrtf(ss);
       }
     }
     bar_sync(gbar, GT);
@@ -778,9 +796,9 @@ __global__ void __launch_bounds__(CL ? blk::Geom<D>::GT : blk::Geom<D>::NT, 1) s
       }
       if (cS > 0) {
         auto recS = [&](int t) -> int { return (t < cS) ? baseS + t * REC : C::F_ZERO; };
-        const int ybuf = C::F_Y + par * KS * D;
+        const int ybuf = C::F_Y + par * C::NVY * D;   // Y_t at ybuf + t D (delta rule: X_t at ybuf + (KS + t) D)
         const int abuf = C::F_AL + (rnd & 1) * KS * D;
-        // ---------------- phase P: Y_t = S_reg phi(q_t), ||S_reg||^2
+        // ---------------- phase P: Y_t = S_reg phi(q_t) (delta rule: and X_t = S_reg s_t), ||S_reg||^2
         {
           float ns;
           float vals[RPT * C::NVS];
@@ -791,8 +809,8 @@ __global__ void __launch_bounds__(CL ? blk::Geom<D>::GT : blk::Geom<D>::NT, 1) s
 #pragma unroll
               for (int v = 0; v < C::NVS; ++v) acc[r][v] = f2(0.f, 0.f);
 #pragma unroll
-            for (int v = 0; v < KS; ++v) {
-              const int base = recS(v) + C::OFF_Q;
+            for (int v = 0; v < C::NVY; ++v) {
+              const int base = (v < KS) ? recS(v) + C::OFF_Q : recS(v - KS) + C::OFF_S;
 #pragma unroll
               for (int kk = 0; kk < NCH; ++kk) {
                 const float4 x = *reinterpret_cast<const float4*>(sf + base + colof(kk, 0));
@@ -820,14 +838,14 @@ __global__ void __launch_bounds__(CL ? blk::Geom<D>::GT : blk::Geom<D>::NT, 1) s
           for (int i = 0; i < C::KVS; ++i) {
             const int slot = c * C::KVS + i;
             const int r = slot / C::NVS, v = slot - r * C::NVS;
-            if (v < KS) sf[ybuf + v * D + row0 + r] = vals[i];
+            if (v < C::NVY) sf[ybuf + v * D + row0 + r] = vals[i];
           }
 #pragma unroll
           for (int m = 16; m >= 1; m >>= 1) ns += __shfl_xor_sync(0xffffffffu, ns, m);
           if (lane == 0) sf[C::F_WP + par * GW + gw] = ns;
         }
         bar_sync(BAR_S, GT);
-        // ---------------- phase G: alpha_t' . phi(q_t) (t' <= t), |alpha_t|^2
+        // ---------------- phase G: alpha_t' . phi(q_t) (t' <= t), |alpha_t|^2 (delta rule: alpha_t' . s_t)
         {
           auto jobs = [&](auto wtag) {
             constexpr int W = decltype(wtag)::value;
@@ -844,9 +862,16 @@ __global__ void __launch_bounds__(CL ? blk::Geom<D>::GT : blk::Geom<D>::NT, 1) s
                   for (int tt = 1; tt < KS; ++tt) t += (j >= tt * (tt + 1) / 2) ? 1 : 0;
                   oa = abuf + (j - t * (t + 1) / 2) * D;
                   ob = recS(t) + C::OFF_Q;
-                } else {
+                } else if (j < C::NJQ + KS) {
                   oa = abuf + (j - C::NJQ) * D;
                   ob = oa;
+                } else {   // delta rule: alpha_t' . s_t, t' <= t
+                  const int jj = j - C::NJQ - KS;
+                  int t = 0;
+#pragma unroll
+                  for (int tt = 1; tt < KS; ++tt) t += (jj >= tt * (tt + 1) / 2) ? 1 : 0;
+                  oa = abuf + (jj - t * (t + 1) / 2) * D;
+                  ob = recS(t) + C::OFF_S;
                 }
                 if (D >= 32) {
 #pragma unroll
@@ -880,7 +905,7 @@ __global__ void __launch_bounds__(CL ? blk::Geom<D>::GT : blk::Geom<D>::NT, 1) s
         }
         bar_sync(BAR_S, GT);
         // ---------------- phase U: renormalisation, outputs, S update
-        {
+        if constexpr (!DL) {
           float rs_[C::NJS];
 #pragma unroll
           for (int j = 0; j < C::NJS; ++j) rs_[j] = sf[C::F_RS + j];
@@ -1030,6 +1055,258 @@ __global__ void __launch_bounds__(CL ? blk::Geom<D>::GT : blk::Geom<D>::NT, 1) s
             sigma = 1.f;
           }
         }
+        else {
+          // delta rule (gist.science summary §2.3): S_t = S_{t-1} + w_t alpha_hat_t^T with
+          // w_t = v_t - S_{t-1} k_hat_t, k_hat = s / |s|, alpha_hat = alpha / |alpha|.  With the
+          // lazy scale S = sigma S_reg and X_t = S_reg,0 s_t from phase P, per row:
+          //   w_t = v_t - sigma_{t-1} (X_t / |s_t| + sum_{t'<t} w_t' (alpha_hat_t'.k_hat_t) / sigma_{t'-1}),
+          //   S_reg += w_t alpha_hat_t^T / sigma_{t-1},
+          //   S_t phi(q_t) = sigma_t (Y_t + sum_{t'<=t} w_t' (alpha_t'.phi(q_t)) / (|alpha_t'| sigma_{t'-1})).
+          float rs_[C::NJS];
+#pragma unroll
+          for (int j = 0; j < C::NJS; ++j) rs_[j] = sf[C::F_RS + j];
+          float ws = 0.f;
+#pragma unroll
+          for (int w = 0; w < GW; ++w) ws += sf[C::F_WP + par * GW + w];
+          float ia[KS], isn[KS], ck[KS][KS];   // 1/|alpha_t|, 1/|s_t|, alpha_hat_t' . k_hat_t (t' <= t)
+#pragma unroll
+          for (int t = 0; t < KS; ++t) {
+            ia[t] = 1.f / fmaxf(sqrtf(rs_[C::NJQ + t]), kNormEps);
+            isn[t] = 1.f / fmaxf(sf[recS(t) + C::OFF_SC + 2], kNormEps);
+          }
+#pragma unroll
+          for (int t = 0; t < KS; ++t)
+#pragma unroll
+            for (int tp = 0; tp < KS; ++tp)
+              ck[t][tp] = (tp <= t) ? rs_[C::NJQ + KS + t * (t + 1) / 2 + tp] * ia[tp] * isn[t] : 0.f;
+          // ||S_t|| <= ||I - k_hat alpha_hat^T||_2 ||S_{t-1}|| + |v_t|, and for unit vectors with
+          // c = alpha_hat . k_hat that norm is sqrt((3 - 2c + sqrt(5 - 4c)) / 2): when the bound
+          // stays below tau no step of the round renormalises
+          float bound = sigma * sqrtf(ws);
+#pragma unroll
+          for (int t = 0; t < KS; ++t)
+            if (t < cS) {
+              const float cc = fminf(fmaxf(ck[t][t], -1.f), 1.f);
+              const float gr = sqrtf(0.5f * (3.f - 2.f * cc + sqrtf(5.f - 4.f * cc)));
+              bound = fmaf(gr, bound, sf[recS(t) + C::OFF_SC + 1]);
+            }
+          if (!isfinite(bound)) flags |= kStatusNonfinite;
+          float isg[KS], sg[KS], sgp[KS];   // 1/sigma before step t, sigma after it, sigma before it
+          const bool exact = !(bound <= a.tau * (1.f - 0x1p-12f));
+          if (!exact) {
+            const float is = __frcp_rn(sigma);
+#pragma unroll
+            for (int t = 0; t < KS; ++t) { isg[t] = is; sg[t] = sigma; sgp[t] = sigma; }
+          } else {
+            // the per-step norms from one reduction: w_t = sum_m A_tm v_m + B_tm X_m, so every
+            // product they need is a combination of v_m^T S_reg,0 alpha_t, X_m^T S_reg,0 alpha_t,
+            // the Gram matrix of {v_m, X_m} and alpha_t . alpha_t'
+            float mv[C::NMINI];
+#pragma unroll
+            for (int k2 = 0; k2 < C::NMINI; ++k2) mv[k2] = 0.f;
+            float vrow[KS][RPT], xrow[KS][RPT];
+#pragma unroll
+            for (int t = 0; t < KS; ++t)
+#pragma unroll
+              for (int r = 0; r < RPT; ++r) {
+                vrow[t][r] = sf[recS(t) + C::OFF_V + row0 + r];
+                xrow[t][r] = (t < cS) ? sf[ybuf + (KS + t) * D + row0 + r] : 0.f;
+              }
+#pragma unroll
+            for (int t = 0; t < KS; ++t) {
+              float y[RPT];
+#pragma unroll
+              for (int r = 0; r < RPT; ++r) y[r] = 0.f;
+#pragma unroll
+              for (int kk = 0; kk < NCH; ++kk) {
+                const float4 al = *reinterpret_cast<const float4*>(sf + abuf + t * D + colof(kk, 0));
+#pragma unroll
+                for (int r = 0; r < RPT; ++r) {
+                  y[r] = fmaf(S2[r][2 * kk].x, al.x, y[r]);
+                  y[r] = fmaf(S2[r][2 * kk].y, al.y, y[r]);
+                  y[r] = fmaf(S2[r][2 * kk + 1].x, al.z, y[r]);
+                  y[r] = fmaf(S2[r][2 * kk + 1].y, al.w, y[r]);
+                }
+              }
+#pragma unroll
+              for (int m = 0; m < KS; ++m)
+#pragma unroll
+                for (int r = 0; r < RPT; ++r) {
+                  mv[C::MI_VSA + m * KS + t] = fmaf(vrow[m][r], y[r], mv[C::MI_VSA + m * KS + t]);
+                  mv[C::MI_XSA + m * KS + t] = fmaf(xrow[m][r], y[r], mv[C::MI_XSA + m * KS + t]);
+                }
+            }
+            if (c == 0) {   // lane 0 of each row group covers its rows once
+#pragma unroll
+              for (int m = 0; m < KS; ++m)
+#pragma unroll
+                for (int mp = 0; mp < KS; ++mp)
+#pragma unroll
+                  for (int r = 0; r < RPT; ++r) {
+                    mv[C::MI_VX + m * KS + mp] = fmaf(vrow[m][r], xrow[mp][r], mv[C::MI_VX + m * KS + mp]);
+                    if (mp <= m) {
+                      mv[C::MI_VV + m * (m + 1) / 2 + mp] =
+                          fmaf(vrow[m][r], vrow[mp][r], mv[C::MI_VV + m * (m + 1) / 2 + mp]);
+                      mv[C::MI_XX + m * (m + 1) / 2 + mp] =
+                          fmaf(xrow[m][r], xrow[mp][r], mv[C::MI_XX + m * (m + 1) / 2 + mp]);
+                    }
+                  }
+            }
+            if (g == 0) {   // row group 0 covers every column once
+#pragma unroll
+              for (int t = 0; t < KS; ++t)
+#pragma unroll
+                for (int tp = 0; tp <= t; ++tp)
+#pragma unroll
+                  for (int kk = 0; kk < NCH; ++kk)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                      const int col = colof(kk, e);
+                      mv[C::MI_AA + t * (t + 1) / 2 + tp] =
+                          fmaf(sf[abuf + t * D + col], sf[abuf + tp * D + col], mv[C::MI_AA + t * (t + 1) / 2 + tp]);
+                    }
+            }
+#pragma unroll
+            for (int k2 = 0; k2 < C::NMINI; ++k2) {
+              float x = mv[k2];
+#pragma unroll
+              for (int m = 16; m >= 1; m >>= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
+              mv[k2] = x;
+            }
+            if (lane == 0) {
+#pragma unroll
+              for (int k2 = 0; k2 < C::NMINI; ++k2) sf[C::F_MINI + gw * C::MSTR + k2] = mv[k2];
+            }
+            bar_sync(BAR_S, GT);
+#pragma unroll
+            for (int k2 = 0; k2 < C::NMINI; ++k2) {
+              float x = 0.f;
+#pragma unroll
+              for (int w = 0; w < GW; ++w) x += sf[C::F_MINI + w * C::MSTR + k2];
+              mv[k2] = x;
+            }
+            auto vv_ = [&](int m, int mp) { return m >= mp ? mv[C::MI_VV + m * (m + 1) / 2 + mp] : mv[C::MI_VV + mp * (mp + 1) / 2 + m]; };
+            auto xx_ = [&](int m, int mp) { return m >= mp ? mv[C::MI_XX + m * (m + 1) / 2 + mp] : mv[C::MI_XX + mp * (mp + 1) / 2 + m]; };
+            float cA[KS][KS], cB[KS][KS];
+            float nreg2 = ws, sgc = sigma;
+#pragma unroll
+            for (int t = 0; t < KS; ++t) {
+              isg[t] = __frcp_rn(sgc);
+              sgp[t] = sgc;
+#pragma unroll
+              for (int m = 0; m < KS; ++m) {
+                cA[t][m] = (m == t) ? 1.f : 0.f;
+                cB[t][m] = (m == t) ? -sgc * isn[t] : 0.f;
+              }
+              if (t < cS) {
+#pragma unroll
+                for (int tp = 0; tp < t; ++tp) {
+                  const float f = sgc * isg[tp] * ck[t][tp];
+#pragma unroll
+                  for (int m = 0; m < KS; ++m) {
+                    cA[t][m] = fmaf(-f, cA[tp][m], cA[t][m]);
+                    cB[t][m] = fmaf(-f, cB[tp][m], cB[t][m]);
+                  }
+                }
+                float wsa = 0.f;   // w_t . S_reg,0 alpha_t
+#pragma unroll
+                for (int m = 0; m < KS; ++m)
+                  wsa = fmaf(cA[t][m], mv[C::MI_VSA + m * KS + t], fmaf(cB[t][m], mv[C::MI_XSA + m * KS + t], wsa));
+                float ww[KS];      // w_t . w_t'
+#pragma unroll
+                for (int tp = 0; tp <= t; ++tp) {
+                  float x = 0.f;
+#pragma unroll
+                  for (int m = 0; m < KS; ++m)
+#pragma unroll
+                    for (int mp = 0; mp < KS; ++mp) {
+                      x = fmaf(cA[t][m] * cA[tp][mp], vv_(m, mp), x);
+                      x = fmaf(cA[t][m] * cB[tp][mp], mv[C::MI_VX + m * KS + mp], x);
+                      x = fmaf(cB[t][m] * cA[tp][mp], mv[C::MI_VX + mp * KS + m], x);
+                      x = fmaf(cB[t][m] * cB[tp][mp], xx_(m, mp), x);
+                    }
+                  ww[tp] = x;
+                }
+                float cross = wsa;   // w_t . S_reg,t-1 alpha_t, then times 1/|alpha_t|
+#pragma unroll
+                for (int tp = 0; tp < t; ++tp)
+                  cross = fmaf(ww[tp] * mv[C::MI_AA + t * (t + 1) / 2 + tp], ia[tp] * isg[tp], cross);
+                cross *= ia[t];
+                nreg2 = fmaf(2.f * isg[t], cross, nreg2);
+                nreg2 = fmaf(ww[t], isg[t] * isg[t], nreg2);
+                const float npre = sgc * sqrtf(fmaxf(nreg2, 0.f));
+                if (npre > a.tau) {
+                  sgc *= a.tau / npre;
+                  ++renorm_cnt;
+                }
+                if (!isfinite(npre)) flags |= kStatusNonfinite;
+              }
+              sg[t] = sgc;
+            }
+          }
+          // w_t of row i from v, X and the earlier w's of that row
+          auto wrow = [&](int i, float (&w)[KS]) {
+#pragma unroll
+            for (int t = 0; t < KS; ++t) {
+              float x = 0.f;
+              if (t < cS) {
+                x = fmaf(-sgp[t] * isn[t], sf[ybuf + (KS + t) * D + i], sf[recS(t) + C::OFF_V + i]);
+#pragma unroll
+                for (int tp = 0; tp < t; ++tp) x = fmaf(-sgp[t] * isg[tp] * ck[t][tp], w[tp], x);
+              }
+              w[t] = x;
+            }
+          };
+          // outputs: o_t = sigma_t (Y_t + sum_{t'<=t} w_t' (alpha_t'.phi(q_t)) / (|alpha_t'| sigma_{t'-1})) / den_t
+          {
+            const int h = gid / D, i = gid - (gid / D) * D;
+            float wi[KS];
+            wrow(i, wi);
+#pragma unroll
+            for (int tt = 0; tt < KS; ++tt) {
+              if ((tt & 1) != h || tt >= cS) continue;
+              float x = sf[ybuf + tt * D + i];
+#pragma unroll
+              for (int tp = 0; tp <= tt; ++tp) x = fmaf(wi[tp] * rs_[tt * (tt + 1) / 2 + tp], ia[tp] * isg[tp], x);
+              const float o = sg[tt] * x * sf[recS(tt) + C::OFF_SC];
+              if (!isfinite(o)) flags |= kStatusNonfinite;
+              go[(gS0 + tt) * D + i] = from_f32<TIO>(o);
+            }
+          }
+          // S_reg += sum_t w_t alpha_t^T / (sigma_{t-1} |alpha_t|)
+          {
+            float wr[RPT][KS];
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) wrow(row0 + r, wr[r]);
+#pragma unroll
+            for (int t = 0; t < KS; ++t) {
+              if (t < cS) {
+                float vr[RPT];
+#pragma unroll
+                for (int r = 0; r < RPT; ++r) vr[r] = wr[r][t] * isg[t] * ia[t];
+#pragma unroll
+                for (int kk = 0; kk < NCH; ++kk) {
+                  const float4 al = *reinterpret_cast<const float4*>(sf + abuf + t * D + colof(kk, 0));
+                  const float2 a0 = f2(al.x, al.y), a1 = f2(al.z, al.w);
+#pragma unroll
+                  for (int r = 0; r < RPT; ++r) {
+                    const float2 w = f2(vr[r], vr[r]);
+                    S2[r][2 * kk] = __ffma2_rn(w, a0, S2[r][2 * kk]);
+                    S2[r][2 * kk + 1] = __ffma2_rn(w, a1, S2[r][2 * kk + 1]);
+                  }
+                }
+              }
+            }
+          }
+          sigma = sg[KS - 1];
+          if (sigma < 0x1p-16f) {
+#pragma unroll
+            for (int r = 0; r < RPT; ++r)
+#pragma unroll
+              for (int p = 0; p < NCP; ++p) { S2[r][p].x *= sigma; S2[r][p].y *= sigma; }
+            sigma = 1.f;
+          }
+        }
       }
       if constexpr (CL) mbar_arrive_remote(remote(&hb[2 + (rnd & 1)]));
       else bar_arrive(BAR_EMPTY0 + (rnd & 1), NT);
@@ -1062,10 +1339,11 @@ __global__ void __launch_bounds__(CL ? blk::Geom<D>::GT : blk::Geom<D>::NT, 1) s
   }
 }
 
-template <int D, int R, int KS, typename TIO, bool PS = false>
+// DL = true: the delta-rule variant (same A group; the S group writes S with the residual).
+template <int D, int R, int KS, typename TIO, bool PS = false, bool DL = false>
 cudaError_t launch_seq_block_t(const ScanArgs& a, cudaStream_t s) {
-  using C = blk::Cfg<D, R, KS, TIO>;
-  auto kern = seq_block_kernel<D, R, KS, TIO, PS, false>;
+  using C = blk::Cfg<D, R, KS, TIO, DL>;
+  auto kern = seq_block_kernel<D, R, KS, TIO, PS, false, DL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::bytes);
   if (e != cudaSuccess) return e;
   kern<<<a.pairs, blk::Geom<D>::NT, C::bytes, s>>>(a);
@@ -1073,10 +1351,10 @@ cudaError_t launch_seq_block_t(const ScanArgs& a, cudaStream_t s) {
 }
 
 // Cluster mode: two CTAs (A group, S group) per pair.
-template <int D, int R, int KS, typename TIO>
+template <int D, int R, int KS, typename TIO, bool DL = false>
 cudaError_t launch_seq_cluster_t(const ScanArgs& a, cudaStream_t s) {
-  using C = blk::Cfg<D, R, KS, TIO>;
-  auto kern = seq_block_kernel<D, R, KS, TIO, false, true>;
+  using C = blk::Cfg<D, R, KS, TIO, DL>;
+  auto kern = seq_block_kernel<D, R, KS, TIO, false, true, DL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::bytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};

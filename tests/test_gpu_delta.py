@@ -4,7 +4,10 @@ The variant (gist.science summary §2.3) keeps the exact tracking of A and write
 the state with a residual and unit vectors: alpha_hat = A k_hat / |A k_hat|,
 k_hat = phi(k) / |phi(k)|, S += (v - S k_hat) alpha_hat^T.  The oracle's
 ``scan(..., rule="delta")`` is pinned by its own checks (tests/test_oracle_pins.py);
-here the CUDA kernel is compared with it element by element on seeded inputs:
+here the CUDA kernel (the blocked scan kernel's delta-rule variant: rounds of
+several steps, the residuals solved within the round, renormalisation decided on
+one reduction of Gram scalars) is compared with it element by element on seeded
+inputs:
 full-length workloads (all pairs of the f32 one, sampled pairs of the bf16 one)
 and edge cases (ragged tiles, nudges with a t0 phase, renormalisation that
 fires, the singularity guard, split calls, every built head width and rank).
@@ -44,6 +47,8 @@ CASES = [
     (3, 333, 64, 1, "bf16", 1024, 1e4, 0),
     (3, 129, 64, 4, "f32", 40, 1e4, 3),
     (2, 300, 64, 1, "f32", 64, 1.5, 0),        # renormalisation fires
+    (3, 333, 64, 4, "bf16", 30, 2.0, 7),       # r = 4: renormalisation, nudges, ragged tail
+    (2, 261, 64, 1, "bf16", 1024, 0.7, 0),     # renormalisation at nearly every step
     (2, 150, 128, 1, "f32", 64, 1e3, 0),
     (2, 77, 128, 4, "bf16", 16, 1e4, 1),
 ]
@@ -93,9 +98,15 @@ def test_delta_guard():
     _check(errs(got, ref), TOL["f32"], "delta guard")
 
 
-def test_delta_split_calls_continue_the_state():
+@pytest.mark.parametrize("T1", [160, 150])
+def test_delta_split_calls_continue_the_state(T1):
+    """Two calls with t0 continue the state of one.  The blocked kernel takes rounds of up to
+    4 steps inside tiles of 32 counted from each call's start, so a split at a tile boundary
+    (160) gives the same rounds and the same bits; elsewhere (150) the rounds differ and the
+    results agree to float32 rounding."""
     import sherman_morrison_inverse_gb300 as vla
-    N, T1, T2, d = 3, 150, 97, 64
+    import oracle
+    N, T2, d = 3, 247 - T1, 64
     x = workloads.gaussian_inputs(N, T1 + T2, d, d, 1, "f32", seed=88)
     kw = dict(P=50, eps_n=1e-3, tau=1e4)
     whole = gpu_scan(x, 1, N, mode="delta", **kw)
@@ -108,8 +119,14 @@ def test_delta_split_calls_continue_the_state():
         g = [x[k][:, a:b].reshape(1, N, b - a, *x[k].shape[2:]).to(dev).contiguous() for k in ("q", "k", "v", "u")]
         outs.append(vla.scan_fwd(*g, A, S, n, t0=a, mode="delta", **kw))
     o = torch.cat(outs, dim=2).reshape(N, T1 + T2, d).double().cpu().numpy()
-    assert np.array_equal(o, whole[0])
-    assert np.array_equal(S.reshape(N, d, d).double().cpu().numpy(), whole[2])
+    got = (o, A.reshape(N, d, d).double().cpu().numpy(), S.reshape(N, d, d).double().cpu().numpy(),
+           n.reshape(N, d).double().cpu().numpy())
+    if T1 % 32 == 0:
+        for x1, x2 in zip(got, whole[:4]):
+            assert np.array_equal(x1, x2)
+    else:
+        e = oracle.errors(*got, *whole[:4])
+        assert max(e.values()) <= 1e-5, e
 
 
 def test_delta_rejects_a_chunk_size():
