@@ -258,17 +258,22 @@ def run_project_u(args, w):
     clk = clocks.stop()
     ms = e0.elapsed_time(e1) / args.steps
     peaks = load_peaks()
-    peak_tf, peak_how = fp32_peak_tflops(peaks)
     flops = 2 * w.r * w.d * w.d * n
-    nbytes = n * (w.d + w.r * w.d) * k.element_size()
+    nbytes = n * (w.d + w.r * w.d) * k.element_size()   # keys in, directions out (W: a few KB)
+    # the tensor-core form (tcgen05 kind::tf32, W as hi + lo) serves every shape but d = 128 with
+    # float32 keys; it is bound by HBM: a few flops per byte, far below the tensor ridge
+    tc = not (w.d == 128 and w.io == "f32")
+    gbs = nbytes / (ms / 1e3) / 1e9
     line = {"metric": "u projection tokens/s (normalize(W_u k_raw))", "value": n / (ms / 1e3), "unit": "tokens/s",
             "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": w.name, "tokens": n, "d": w.d, "r": w.r, "io": w.io, "op": "project_u"},
-            "roofline": {"bound": "alu", "achieved": flops / (ms / 1e3) / 1e12, "peak": peak_tf, "unit": "TFLOP/s",
-                         "frac": flops / (ms / 1e3) / 1e12 / peak_tf, "traffic": None, "peak_how": peak_how,
-                         "hbm_gbs": nbytes / (ms / 1e3) / 1e9,
-                         "hbm_frac": nbytes / (ms / 1e3) / 1e9 / float(peaks["hbm_gbs"])},
+            "scaling": "weak", "vs_baseline": None, "dtype": "tf32" if tc else "f32", "data": "synthetic",
+            "config": {"workload": w.name, "tokens": n, "d": w.d, "r": w.r, "io": w.io, "op": "project_u",
+                       "l2": "keys and directions 2 x %.0f MB > 129 MB L2 (no flush)" % (n * w.d * k.element_size() / 1e6)},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
+                         "frac": gbs / float(peaks["hbm_gbs"]), "traffic": None,
+                         "peak_how": "%s HBM copy bandwidth" % peaks["_source"],
+                         "algorithmic_bytes": nbytes, "tflops": flops / (ms / 1e3) / 1e12,
+                         "form": "tcgen05 kind::tf32, 2 passes (W hi + lo)" if tc else "CUDA cores, float32"},
             "clocks": clk, "gpu_launches": args.steps}
     print(json.dumps(line), flush=True)
     h.close()

@@ -467,7 +467,8 @@ vla_err_t vla_project_u(vla_handle_t h, const void* k_raw, const float* W_u, voi
   bool built = false;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = on_device(h->device, [&]() -> cudaError_t {
-    return vla::launch_project_u(d, io_dtype == VLA_BF16, k_raw, W_u, u, n_tokens, r, h->sm_count, s, &built);
+    return vla::launch_project_u(d, io_dtype == VLA_BF16, k_raw, W_u, u, n_tokens, r, h->sm_count, h->status, s,
+                                 &built);
   });
   if (!built) return fail(h, VLA_ERR_UNSUPPORTED, "vla_project_u: built for d in {16, 64, 128}");
   if (e != cudaSuccess) return fail(h, VLA_ERR_CUDA, cuda_msg("vla_project_u: launch", e));

@@ -54,7 +54,7 @@ cudaError_t launch_chunked(int d, int r, bool bf16, int chunk, const ScanArgs& a
                            bool* built);
 cudaError_t launch_delta(int d, int r, bool bf16, int ctas, const ScanArgs& a, cudaStream_t s, bool* built);
 cudaError_t launch_project_u(int d, bool bf16, const void* k, const float* W, void* u, long long n, int r,
-                             int sm_count, cudaStream_t s, bool* built);
+                             int sm_count, DevStatus* status, cudaStream_t s, bool* built);
 // Gather the window [off, off + tj) of four [pairs, T, w_bytes[i]] host tensors (read
 // through the device addresses src[i] of page-locked host memory) into dense
 // [pairs, tj, w_bytes[i]] device buffers dst[i]; w_bytes[i] and all pointers 16-byte

@@ -1,16 +1,17 @@
 // Direction projection u_{t,i} = W_u[i] k_t / max(|W_u[i] k_t|_2, 1e-12) for sm_103a: the
 // README "VLA v3" item 2 "u_t = normalize(W_u k_t^raw)", computed before the scan (whose u
-// input it produces, [n, r, d]).
+// input it produces, [n, r, d]).  Two forms: the tensor-core one (below, every shape whose
+// operands fit in shared memory) and a CUDA-core one (d = 128 with float32 keys).
 //
-// Each thread takes TPT consecutive tokens (4 at d = 16, 2 at d = 64, 1 at d = 128),
+// CUDA-core form: each thread takes TPT consecutive tokens (4 at d = 16, 2 at d = 64, 1 at d = 128),
 // groups taken grid-stride, the ranks one after another (W_u[i] in shared memory, d x d
 // float32).  Each thread reads its keys as 16-byte vectors (all independent loads, one
 // memory latency per group), forms x_j = W[j] . k for its tokens with W's rows broadcast
 // from shared memory, keeps x in its own padded shared-memory rows (stride d + 1,
 // conflict-free), and writes x_j / max(|x|, 1e-12) as 16-byte vectors: no barrier
-// inside the token loop.  Arithmetic in float32 (float32 or bfloat16 in
-// and out).
+// inside the token loop.  Arithmetic in float32 (float32 or bfloat16 in and out).
 #include "vla_internal.cuh"
+#include "vla_tc.cuh"
 
 namespace vla {
 namespace prj {
@@ -133,29 +134,195 @@ __global__ void __launch_bounds__(NTH) project_u_kernel(const TIO* __restrict__ 
   }
 }
 
+// ---------------------------------------------------------------------------
+// Tensor-core form: x = K W^T for a tile of 128 tokens as one tcgen05 product
+// (kind::tf32, M = 128 tokens, N = d outputs, K = d), accumulated in TMEM.  bf16 keys
+// are exact in tf32; W is split into tf32 hi + lo parts, so two passes give W to about
+// 2^-21 (float32 keys: also k hi + lo, three passes).  Operands sit in shared memory in
+// the K-major no-swizzle core-matrix layout (tc::tk_off).  Row t of the result is TMEM
+// lane t, which the epilogue thread t reads: it forms |x|, scales, converts and stores
+// its token's u row as 16-byte vectors.
+__device__ __forceinline__ float tf32_hi(float x) { return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u); }
+
+template <int D, typename TIO>
+struct TcCfg {
+  static constexpr int NP = sizeof(TIO) == 2 ? 2 : 3;        // MMA passes
+  static constexpr int F_KH = 0;                              // [128][D] keys (hi)
+  static constexpr int F_KL = F_KH + 128 * D;                 // [128][D] keys lo (float32 keys)
+  static constexpr int F_WH = F_KL + (NP == 3 ? 128 * D : 0); // [D][D] W hi
+  static constexpr int F_WL = F_WH + D * D;                   // [D][D] W lo
+  static constexpr int F_END = F_WL + D * D;
+  static constexpr size_t bytes = sizeof(float) * (size_t)F_END + 16;   // + mbarrier, TMEM slot
+  static constexpr uint32_t TCOLS = D < 32 ? 32 : D;
+};
+
+template <int D, typename TIO>
+__global__ void __launch_bounds__(NTH) project_u_tc_kernel(const TIO* __restrict__ k, const float* __restrict__ W,
+                                                           TIO* __restrict__ u, long long n, int r,
+                                                           DevStatus* __restrict__ status) {
+  using Cf = TcCfg<D, TIO>;
+  using V = Vec<TIO>;
+  using tc::tk_off;
+  constexpr int NV = D / V::N;
+  static_assert(NTH == 128, "one thread per TMEM lane of an M = 128 product");
+  extern __shared__ __align__(1024) float sm[];
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + Cf::F_END);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const uint32_t sbase = smem_u32(sm);
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tc::tmem_alloc(tslot, Cf::TCOLS);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tslot;
+  const uint32_t tlane = tmem + ((uint32_t)(32 * warp) << 16);   // this warp's lane quadrant
+  uint32_t phase = 0;
+  bool failed = false;
+  auto st4 = [&](int off, float x0, float x1, float x2, float x3) {
+    *reinterpret_cast<float4*>(sm + off) = make_float4(x0, x1, x2, x3);
+  };
+  const long long ntiles = (n + NTH - 1) / NTH;
+  for (int i = 0; i < r && !failed; ++i) {
+    // W_u[i] -> hi / lo, K-major (row j = output, K = input m)
+    for (int e4 = tid; e4 < D * D / 4; e4 += NTH) {
+      const float4 w = reinterpret_cast<const float4*>(W + (size_t)i * D * D)[e4];
+      const int j = (4 * e4) / D, m = 4 * e4 - j * D;
+      const float h0 = tf32_hi(w.x), h1 = tf32_hi(w.y), h2 = tf32_hi(w.z), h3 = tf32_hi(w.w);
+      st4(Cf::F_WH + tk_off(j, m, D), h0, h1, h2, h3);
+      st4(Cf::F_WL + tk_off(j, m, D), w.x - h0, w.y - h1, w.z - h2, w.w - h3);
+    }
+    // this thread's key row of the next tile, loaded a tile ahead so that the load
+    // overlaps the product and the epilogue of the tile before
+    uint4 kn[NV];
+    auto fetch = [&](long long tile) {
+      const long long t = tile * NTH + tid;
+      const uint4* kv = reinterpret_cast<const uint4*>(k + t * D);
+#pragma unroll
+      for (int v = 0; v < NV; ++v) kn[v] = (tile < ntiles && t < n) ? __ldg(kv + v) : make_uint4(0u, 0u, 0u, 0u);
+    };
+    fetch(blockIdx.x);
+    for (long long tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+      const long long t = tile * NTH + tid;   // this thread's token (row tid of the tile)
+      {
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+          float x[V::N];
+          V::load(kn[v], x);
+#pragma unroll
+          for (int q = 0; q < V::N; q += 4) {
+            const int m = V::N * v + q;
+            if constexpr (Cf::NP == 3) {
+              const float h0 = tf32_hi(x[q]), h1 = tf32_hi(x[q + 1]), h2 = tf32_hi(x[q + 2]), h3 = tf32_hi(x[q + 3]);
+              st4(Cf::F_KH + tk_off(tid, m, D), h0, h1, h2, h3);
+              st4(Cf::F_KL + tk_off(tid, m, D), x[q] - h0, x[q + 1] - h1, x[q + 2] - h2, x[q + 3] - h3);
+            } else {
+              st4(Cf::F_KH + tk_off(tid, m, D), x[q], x[q + 1], x[q + 2], x[q + 3]);
+            }
+          }
+        }
+      }
+      // operands written by the generic proxy -> visible to the tensor core; the previous
+      // tile's TMEM reads are done before this tile's product overwrites the accumulator
+      fence_proxy_async_smem();
+      tc::fence_before_sync();
+      __syncthreads();
+      tc::fence_after_sync();
+      if (tid == 0) {
+        constexpr uint32_t sbo = 32u * D;
+        constexpr uint32_t idesc = tc::idesc_tf32(128, D);
+        const int xs[3] = {Cf::F_KH, Cf::F_KH, Cf::F_KL}, ys[3] = {Cf::F_WH, Cf::F_WL, Cf::F_WH};
+#pragma unroll
+        for (int p = 0; p < Cf::NP; ++p)
+#pragma unroll
+          for (int kk = 0; kk < D / 8; ++kk)
+            tc::mma_tf32(tmem, tc::sdesc(sbase + 4u * xs[p] + 256u * kk, sbo),
+                         tc::sdesc(sbase + 4u * ys[p] + 256u * kk, sbo), idesc, p > 0 || kk > 0);
+        tc::mma_commit(bar);
+      }
+      fetch(tile + gridDim.x);   // the staged keys are consumed; the registers are free
+      if (tid == 0 && !mbar_wait_bounded(bar, phase)) failed = true;
+      phase ^= 1u;
+      tc::fence_before_sync();
+      failed = __syncthreads_or(failed) != 0;
+      tc::fence_after_sync();
+      if (failed) break;
+      // epilogue: |x| of this thread's row, then the scaled row
+      constexpr int CW = D < 32 ? 16 : 32;   // columns per TMEM load
+      float nrm = 0.f;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += CW) {
+        float x[CW];
+        if constexpr (CW == 32) tc::tmem_ld32(tlane + (uint32_t)c0, x);
+        else tc::tmem_ld16(tlane + (uint32_t)c0, x);
+#pragma unroll
+        for (int j = 0; j < CW; ++j) nrm = fmaf(x[j], x[j], nrm);
+      }
+      const float inv = 1.f / fmaxf(sqrtf(nrm), 1e-12f);
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += CW) {
+        float x[CW];
+        if constexpr (CW == 32) tc::tmem_ld32(tlane + (uint32_t)c0, x);
+        else tc::tmem_ld16(tlane + (uint32_t)c0, x);
+        if (t < n) {
+          uint4* uv = reinterpret_cast<uint4*>(u + (t * r + i) * D + c0);
+#pragma unroll
+          for (int v = 0; v < CW / V::N; ++v) {
+            float y[V::N];
+#pragma unroll
+            for (int m = 0; m < V::N; ++m) y[m] = x[V::N * v + m] * inv;
+            uv[v] = V::pack(y);
+          }
+        }
+      }
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 0) tc::tmem_dealloc(tmem, Cf::TCOLS);
+  if (failed && tid == 0) atomicOr(&status->flags, kStatusTimeout);
+}
+
 template <int D, typename TIO>
 cudaError_t launch_project_t(const void* k, const float* W, void* u, long long n, int r, int sm_count,
-                             cudaStream_t s) {
-  auto kern = project_u_kernel<D, TIO>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Smem<D>::bytes);
-  if (e != cudaSuccess) return e;
-  const long long nblk = (n + (long long)NTH * tpt<D>() - 1) / ((long long)NTH * tpt<D>());
-  const int grid = (int)min(nblk, (long long)(sm_count > 0 ? sm_count : 1) * 4);
-  kern<<<grid, NTH, Smem<D>::bytes, s>>>(static_cast<const TIO*>(k), W, static_cast<TIO*>(u), n, r);
-  return cudaGetLastError();
+                             DevStatus* status, cudaStream_t s) {
+  const int sms = sm_count > 0 ? sm_count : 1;
+  if constexpr (TcCfg<D, TIO>::bytes <= 227 * 1024) {   // the tensor-core form
+    auto kern = project_u_tc_kernel<D, TIO>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TcCfg<D, TIO>::bytes);
+    if (e != cudaSuccess) return e;
+    const long long ntiles = (n + NTH - 1) / NTH;
+    const int grid = (int)min(ntiles, (long long)sms * 4);
+    kern<<<grid, NTH, TcCfg<D, TIO>::bytes, s>>>(static_cast<const TIO*>(k), W, static_cast<TIO*>(u), n, r,
+                                                 status);
+    return cudaGetLastError();
+  } else {   // d = 128 float32 keys: operands beyond shared memory; CUDA cores
+    auto kern = project_u_kernel<D, TIO>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Smem<D>::bytes);
+    if (e != cudaSuccess) return e;
+    const long long nblk = (n + (long long)NTH * tpt<D>() - 1) / ((long long)NTH * tpt<D>());
+    const int grid = (int)min(nblk, (long long)sms * 4);
+    kern<<<grid, NTH, Smem<D>::bytes, s>>>(static_cast<const TIO*>(k), W, static_cast<TIO*>(u), n, r);
+    return cudaGetLastError();
+  }
 }
 
 }  // namespace prj
 
 cudaError_t launch_project_u(int d, bool bf16, const void* k, const float* W, void* u, long long n, int r,
-                             int sm_count, cudaStream_t s, bool* built) {
+                             int sm_count, DevStatus* status, cudaStream_t s, bool* built) {
   *built = true;
-  if (d == 16) return bf16 ? prj::launch_project_t<16, __nv_bfloat16>(k, W, u, n, r, sm_count, s)
-                           : prj::launch_project_t<16, float>(k, W, u, n, r, sm_count, s);
-  if (d == 64) return bf16 ? prj::launch_project_t<64, __nv_bfloat16>(k, W, u, n, r, sm_count, s)
-                           : prj::launch_project_t<64, float>(k, W, u, n, r, sm_count, s);
-  if (d == 128) return bf16 ? prj::launch_project_t<128, __nv_bfloat16>(k, W, u, n, r, sm_count, s)
-                            : prj::launch_project_t<128, float>(k, W, u, n, r, sm_count, s);
+  if (d == 16) return bf16 ? prj::launch_project_t<16, __nv_bfloat16>(k, W, u, n, r, sm_count, status, s)
+                           : prj::launch_project_t<16, float>(k, W, u, n, r, sm_count, status, s);
+  if (d == 64) return bf16 ? prj::launch_project_t<64, __nv_bfloat16>(k, W, u, n, r, sm_count, status, s)
+                           : prj::launch_project_t<64, float>(k, W, u, n, r, sm_count, status, s);
+  if (d == 128) return bf16 ? prj::launch_project_t<128, __nv_bfloat16>(k, W, u, n, r, sm_count, status, s)
+                            : prj::launch_project_t<128, float>(k, W, u, n, r, sm_count, status, s);
   *built = false;
   return cudaSuccess;
 }
