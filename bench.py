@@ -279,6 +279,32 @@ def run_project_u(args, w):
     h.close()
 
 
+def drift_trace(h, w, x, g, kw, seg, dev):
+    """max|A_t M_t - I| and the largest ||S_t||_F after every `seg` steps of one pass over
+    the sequence, with t0 carried from call to call.  M_t = A_0^{-1} + sum_{t' <= t} u u^T is
+    accumulated on the host in float64.  Nudges (A += eps_n I every P steps) make A differ
+    from M^{-1} by about eps_n ||M|| per nudge: with nudges on this is a report, not a gate."""
+    B, H, T, d = w.B, w.H, w.T, w.d
+    N = B * H
+    A = x["A0"].reshape(B, H, d, d).to(dev).contiguous()
+    S = x["S0"].reshape(B, H, w.dv, d).to(dev).contiguous()
+    n = x["n0"].reshape(B, H, d).to(dev).contiguous()
+    M = np.linalg.inv(x["A0"].double().numpy())
+    eye = np.eye(d)
+    rows = []
+    for a0 in range(0, T, seg):
+        b0 = min(T, a0 + seg)
+        sl = lambda t: t[:, :, a0:b0].contiguous()
+        h.scan_fwd(sl(g["q"]), sl(g["k"]), sl(g["v"]), sl(g["u"]), A, S, n, t0=a0, **kw)
+        Ud = x["u"][:, a0:b0].double().numpy().reshape(N, -1, d)   # the r directions of each step, in order
+        M += np.matmul(Ud.transpose(0, 2, 1), Ud)
+        Ah = A.reshape(N, d, d).double().cpu().numpy()
+        drift = float(np.abs(np.matmul(Ah, M) - eye).max())
+        sfn = float(torch.linalg.norm(S.reshape(N, -1).double(), dim=1).max().item())
+        rows.append({"t": b0, "max_abs_AM_minus_I": drift, "max_S_F": sfn})
+    return rows
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -293,6 +319,13 @@ def main():
     ap.add_argument("--op", choices=["scan", "project_u"], default="scan",
                     help="project_u: time the direction projection u = normalize(W_u k_raw) instead")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--trace", type=int, default=0,
+                    help="untimed, after the timed legs: run the sequence again in calls of this many steps "
+                         "(t0 carried) and report max|A M - I| (M = A_0^-1 + sum u u^T in float64 on the host) "
+                         "and the largest ||S||_F after each call")
+    ap.add_argument("--trace-P", type=int, default=None,
+                    help="nudge period for the trace run (default: the workload's; 0 turns nudges off, so "
+                         "that A tracks M^-1 exactly in exact arithmetic)")
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--seg", type=int, default=0,
                     help="steps per window of the host-buffer (e2e) path; 0 = the library's choice")
@@ -431,6 +464,11 @@ def main():
                            else "copy engines (cudaMemcpy2DAsync)"},
         "status": {"warmup": st_warm, "timed": st, "e2e": st_e2e},
     }
+    if args.trace > 0 and rank == 0:
+        tkw = dict(kw, P=w.P if args.trace_P is None else args.trace_P)
+        rows = drift_trace(h, w, x, g, tkw, args.trace, dev)
+        line["trace"] = {"seg": args.trace, "P": tkw["P"], "tau": w.tau, "rows": rows, "status": h.status(),
+                         "note": "untimed; M = A_0^-1 + sum u u^T in float64 on the host"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, cores, sample = oracle_leg(w)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
