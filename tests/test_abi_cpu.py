@@ -56,3 +56,16 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(vla, "library_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         vla.load_library()
+
+
+def test_host_entry_point_and_path_info_reject_a_null_handle(lib):
+    code = lib.vla_scan_fwd_host(None, None, None, None, None, None, None, None, None,
+                                 1, 1, 4, 64, 64, 1, 0, 0.0, 1.0, 0, 0, 0, 0, 0, None)
+    assert code == 1  # VLA_ERR_INVALID_ARG
+    assert b"handle" in lib.vla_last_error(None)
+    g, seg = ctypes.c_int(), ctypes.c_longlong()
+    assert lib.vla_host_path_info(None, ctypes.byref(g), ctypes.byref(seg)) == 1
+
+
+def test_projection_rejects_a_null_handle(lib):
+    assert lib.vla_project_u(None, None, None, None, 4, 64, 1, 0, None) == 1

@@ -1,0 +1,65 @@
+"""bench.py's host-side pieces that need no GPU: the work and byte counts behind its
+roofline figures, and the reference arm (the float64 oracle timed on the host),
+whose JSON line follows the same contract as the GPU arm's."""
+from __future__ import annotations
+
+import io
+import json
+import os
+import sys
+from contextlib import redirect_stdout
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+import workloads  # noqa: E402
+
+
+def test_flop_counts_per_token_head():
+    # r (A u: 2 d^2, u.z: 2 d, rank-1 update: 2 d^2) + A s (2 d^2) + S += v alpha^T and S phi(q) (2 d dv each)
+    assert bench.flops_per_token_head(64, 64, 1) == 41_088
+    assert bench.flops_per_token_head(64, 64, 4) == 90_624
+    assert bench.flops_per_token_head(128, 128, 1) == 4 * 128 * 128 + 2 * 128 + 2 * 128 * 128 + 4 * 128 * 128
+    assert bench.flops_per_token_head(64, 64, 1, "delta") == 41_088 + 2 * 64 * 64   # plus S k_hat
+    assert bench.flops_per_token_head_short(64, 64, 1) == 24_576                     # 4 d^2 + 2 d dv
+
+
+@pytest.mark.parametrize("idx,nbytes", [(0, 320), (1, 1280), (2, 640), (3, 2560), (4, 1024)])
+def test_streamed_bytes_per_token_head(idx, nbytes):
+    # q, k, u and v in, o out: (2 d + r d + 2 dv) times the I/O element size
+    assert bench.streamed_bytes_per_token_head(workloads.get(idx)) == nbytes
+
+
+def test_reference_arm_prints_one_contract_line():
+    class Args:
+        gpus, steps, warmup = 1, 1, 0
+
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        bench.run_reference(Args, workloads.get(0))
+    lines = [ln for ln in buf.getvalue().splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == bench.UNIT
+    assert d["value"] > 0 and d["higher_is_better"] is True and d["vs_baseline"] is None
+    assert d["config"]["workload"] == "tiny_d16_f32"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and "pairs" in cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_traffic_table_names_its_capture():
+    for (name, mode), (traffic, source) in bench.TRAFFIC.items():
+        assert workloads.get(name).name == name and mode in bench.MODE_DTYPE
+        assert "profiles/" in source
+        if traffic is not None:
+            assert traffic > 0
+            # a capture's DRAM traffic is at least the bytes the launch must stream
+            w = workloads.get(name)
+            assert traffic >= 0.9 * w.pairs * w.T * bench.streamed_bytes_per_token_head(w)
