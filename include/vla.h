@@ -203,6 +203,15 @@ vla_err_t vla_host_path_info(vla_handle_t h, int* gathered, long long* seg);
 vla_err_t vla_project_u(vla_handle_t h, const void* k_raw, const float* W_u, void* u, long long n_tokens,
                         int d, int r, vla_dtype_t io_dtype, void* stream);
 
+/* Self-test of the kernels' bounded waits: launches one CTA whose thread waits, for
+ * limit_ms milliseconds (1..5000), on an mbarrier that nothing completes, gives up and
+ * sets VLA_STATUS_TIMEOUT in the handle's status, the path a scan kernel takes when an
+ * input copy or a tensor-core product does not land within its limit (2 s).  It
+ * shows that a wait that runs out returns control and reports through vla_status()
+ * with the context still usable.  Asynchronous on `stream`.  Errors: INVALID_ARG for a
+ * NULL handle or limit_ms outside 1..5000; CUDA if the launch fails. */
+vla_err_t vla_selftest_wait(vla_handle_t h, unsigned int limit_ms, void* stream);
+
 /* Synchronise `stream`, copy the accumulated status into *out and reset it.
  * Errors: INVALID_ARG (NULL argument), CUDA. */
 vla_err_t vla_status(vla_handle_t h, void* stream, vla_status_t* out);

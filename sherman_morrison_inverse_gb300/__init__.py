@@ -89,6 +89,8 @@ def load_library():
         lib.vla_scan_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, cll, ci, ci, ci,
                                           ci, cf, cf, cll, ci, ci, ci, cll, vp]
         lib.vla_scan_fwd_host.restype = ci
+        lib.vla_selftest_wait.argtypes = [vp, ctypes.c_uint, vp]
+        lib.vla_selftest_wait.restype = ci
         lib.vla_host_path_info.argtypes = [vp, ctypes.POINTER(ci), ctypes.POINTER(cll)]
         lib.vla_host_path_info.restype = ci
         lib.vla_project_u.argtypes = [vp, vp, vp, vp, cll, ci, ci, ci, vp]
@@ -210,6 +212,11 @@ class Handle:
             io, mode_i, int(chunk), _stream_ptr(stream, self.device))
         _check(self.lib, self._h, code)
         return o
+
+    def selftest_wait(self, limit_ms: int = 200, stream=None):
+        """Launch a wait that nothing completes; it gives up after limit_ms and sets the
+        timeout flag in status() (the bounded-wait path of the scan kernels)."""
+        _check(self.lib, self._h, self.lib.vla_selftest_wait(self._h, int(limit_ms), _stream_ptr(stream, self.device)))
 
     def host_path_info(self) -> dict:
         """How the last scan_fwd_host call moved its inputs: {"gathered": 1 (SM gather),

@@ -475,6 +475,17 @@ vla_err_t vla_project_u(vla_handle_t h, const void* k_raw, const float* W_u, voi
   return VLA_OK;
 }
 
+vla_err_t vla_selftest_wait(vla_handle_t h, unsigned int limit_ms, void* stream) {
+  if (!h) return fail(nullptr, VLA_ERR_INVALID_ARG, "vla_selftest_wait: handle is NULL");
+  h->last_error.clear();
+  if (limit_ms < 1 || limit_ms > 5000) return fail(h, VLA_ERR_INVALID_ARG, "vla_selftest_wait: limit_ms must be 1..5000");
+  cudaError_t e = on_device(h->device, [&]() {
+    return vla::launch_wait_selftest(h->status, 1000000ull * limit_ms, static_cast<cudaStream_t>(stream));
+  });
+  if (e != cudaSuccess) return fail(h, VLA_ERR_CUDA, cuda_msg("vla_selftest_wait: launch", e));
+  return VLA_OK;
+}
+
 vla_err_t vla_status(vla_handle_t h, void* stream, vla_status_t* out) {
   if (!h || !out) return fail(h, VLA_ERR_INVALID_ARG, "vla_status: NULL argument");
   vla::DevStatus st{};

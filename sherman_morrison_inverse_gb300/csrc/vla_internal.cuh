@@ -63,6 +63,10 @@ cudaError_t launch_gather_window(const void* const src[4], void* const dst[4], c
                                  long long pairs, long long T, long long off, long long tj, int ctas,
                                  cudaStream_t s);
 
+// One CTA whose thread 0 waits limit_ns on an mbarrier that nothing completes and then
+// sets kStatusTimeout in *status (the path every bounded wait of the scans takes).
+cudaError_t launch_wait_selftest(DevStatus* status, unsigned long long limit_ns, cudaStream_t s);
+
 // Message returned by vla_last_error(NULL) on the calling thread.
 void set_thread_error(const char* msg);
 
@@ -113,13 +117,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait: true when the phase completed, false after kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+// Bounded wait: true when the phase completed, false after limit_ns (kWaitLimitNs).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t_start = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer_ns() - t_start > kWaitLimitNs) return false;
+    if (globaltimer_ns() - t_start > limit_ns) return false;
   }
 }
 

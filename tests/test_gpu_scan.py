@@ -207,3 +207,24 @@ def test_outputs_stay_inside_their_buffers():
         assert torch.all(flat[:pad] == poison) and torch.all(flat[-pad:] == poison), key
     assert h.status()["flags"] == 0
     h.close()
+
+
+def test_a_wait_that_runs_out_reports_a_timeout_and_leaves_the_context_usable():
+    """The bounded-wait path of every kernel: a wait on an mbarrier that nothing completes
+    gives up after its limit and sets the timeout flag; the next scan runs normally."""
+    import time
+    import sherman_morrison_inverse_gb300 as vla
+    h = vla.default_handle()
+    h.status()
+    t0 = time.perf_counter()
+    h.selftest_wait(200)
+    st = h.status()   # synchronises
+    waited = time.perf_counter() - t0
+    assert st["timeout"] and st["flags"] == vla.STATUS_TIMEOUT
+    assert 0.19 <= waited < 5.0
+    x = workloads.gaussian_inputs(2, 50, 16, 16, 1, "f32", seed=9)
+    got = gpu_scan(x, 1, 2, P=16, eps_n=1e-3, tau=1e4)
+    assert got[4]["flags"] == 0
+    assert max(errs(got, oracle_scan(x, P=16, eps_n=1e-3, tau=1e4)).values()) <= 1e-4
+    with pytest.raises(vla.VlaError, match="INVALID_ARG"):
+        h.selftest_wait(0)
