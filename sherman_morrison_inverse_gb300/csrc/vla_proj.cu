@@ -195,23 +195,22 @@ __global__ void __launch_bounds__(NTH) project_u_tc_kernel(const TIO* __restrict
       st4(Cf::F_WH + tk_off(j, m, D), h0, h1, h2, h3);
       st4(Cf::F_WL + tk_off(j, m, D), w.x - h0, w.y - h1, w.z - h2, w.w - h3);
     }
-    // this thread's key row of the next tile, loaded a tile ahead so that the load
-    // overlaps the product and the epilogue of the tile before
-    uint4 kn[NV];
-    auto fetch = [&](long long tile) {
+    // this thread's key rows of the next two tiles, loaded two tiles ahead so that the
+    // loads overlap the products and epilogues of the tiles before (two register
+    // buffers, used alternately by the two halves of the unrolled tile loop)
+    auto fetch = [&](long long tile, uint4 (&buf)[NV]) {
       const long long t = tile * NTH + tid;
       const uint4* kv = reinterpret_cast<const uint4*>(k + t * D);
 #pragma unroll
-      for (int v = 0; v < NV; ++v) kn[v] = (tile < ntiles && t < n) ? __ldg(kv + v) : make_uint4(0u, 0u, 0u, 0u);
+      for (int v = 0; v < NV; ++v) buf[v] = (tile < ntiles && t < n) ? __ldg(kv + v) : make_uint4(0u, 0u, 0u, 0u);
     };
-    fetch(blockIdx.x);
-    for (long long tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    auto process = [&](long long tile, uint4 (&buf)[NV]) -> bool {
       const long long t = tile * NTH + tid;   // this thread's token (row tid of the tile)
       {
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
           float x[V::N];
-          V::load(kn[v], x);
+          V::load(buf[v], x);
 #pragma unroll
           for (int q = 0; q < V::N; q += 4) {
             const int m = V::N * v + q;
@@ -243,13 +242,13 @@ __global__ void __launch_bounds__(NTH) project_u_tc_kernel(const TIO* __restrict
                          tc::sdesc(sbase + 4u * ys[p] + 256u * kk, sbo), idesc, p > 0 || kk > 0);
         tc::mma_commit(bar);
       }
-      fetch(tile + gridDim.x);   // the staged keys are consumed; the registers are free
+      fetch(tile + 2 * (long long)gridDim.x, buf);   // the staged keys are consumed; refill two tiles ahead
       if (tid == 0 && !mbar_wait_bounded(bar, phase)) failed = true;
       phase ^= 1u;
       tc::fence_before_sync();
       failed = __syncthreads_or(failed) != 0;
       tc::fence_after_sync();
-      if (failed) break;
+      if (failed) return false;
       // epilogue: |x| of this thread's row, then the scaled row
       constexpr int CW = D < 32 ? 16 : 32;   // columns per TMEM load
       float nrm = 0.f;
@@ -278,6 +277,14 @@ __global__ void __launch_bounds__(NTH) project_u_tc_kernel(const TIO* __restrict
           }
         }
       }
+      return true;
+    };
+    uint4 ka[NV], kb[NV];
+    fetch(blockIdx.x, ka);
+    fetch(blockIdx.x + (long long)gridDim.x, kb);
+    for (long long tile = blockIdx.x; tile < ntiles; tile += 2 * (long long)gridDim.x) {
+      if (!process(tile, ka)) break;
+      if (tile + gridDim.x < ntiles && !process(tile + gridDim.x, kb)) break;
     }
   }
   tc::fence_before_sync();
