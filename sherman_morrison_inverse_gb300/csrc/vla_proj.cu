@@ -71,9 +71,9 @@ __global__ void __launch_bounds__(NTH) project_u_kernel(const TIO* __restrict__ 
   using V = Vec<TIO>;
   constexpr int TP = tpt<D>();
   constexpr int NV = D / V::N;   // 16-byte vectors per row
-  extern __shared__ __align__(16) float sm[];
-  float* sW = sm + L::W_OFF;
-  float* sX = sm + L::X_OFF + threadIdx.x * TP * (D + 1);   // this thread's TP rows of x
+  extern __shared__ __align__(16) float smc[];
+  float* sW = smc + L::W_OFF;
+  float* sX = smc + L::X_OFF + threadIdx.x * TP * (D + 1);   // this thread's TP rows of x
   const long long stride = (long long)gridDim.x * NTH * TP;
   for (int i = 0; i < r; ++i) {
     __syncthreads();   // every thread is done with the previous rank's W
