@@ -202,6 +202,31 @@ class OracleLeg:
         return f"all {self.w.pairs} pairs x first {steps} of {self.w.T} steps of {self.w.name} ({wall:.1f} s wall)"
 
 
+def host_info() -> dict:
+    """The host the oracle ran on: logical CPUs, CPU model, BLAS threads (when threadpoolctl
+    is importable)."""
+    info = {"host_cpus": os.cpu_count()}
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                key = ln.split(":")[0].strip().lower()
+                if key in ("model name", "cpu part", "hardware") and ":" in ln:
+                    model = ln.split(":", 1)[1].strip()
+                    if key == "model name":
+                        break
+    except OSError:
+        pass
+    import platform
+    info["cpu_model"] = model or platform.processor() or platform.machine()
+    try:
+        from threadpoolctl import threadpool_info
+        info["blas_threads"] = max((p.get("num_threads", 1) for p in threadpool_info()), default=1)
+    except Exception:  # noqa: BLE001 - not installed on every host
+        info["blas_threads"] = None
+    return info
+
+
 def oracle_leg(w, budget_s: float = 15.0):
     leg = OracleLeg(w)
     steps = leg.calibrate(budget_s)
@@ -230,7 +255,7 @@ def run_reference(args, w):
             "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d": w.d, "dv": w.dv, "r": w.r,
                        "io": w.io},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": sample},
+                             "sample": sample, **host_info()},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -472,7 +497,8 @@ def main():
                          "note": "untimed; M = A_0^-1 + sum u u^T in float64 on the host"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, cores, sample = oracle_leg(w)
-        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
+                                **host_info()}
     if rank == 0:
         print(json.dumps(line), flush=True)
     h.close()
