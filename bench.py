@@ -68,6 +68,9 @@ TRAFFIC = {
     ("b8h16_t16384_d64_bf16_recall", "sequential"):
         (325.31e6 * 4, "bytes per launch: profiles/seq_block_kernel_b8h16_d64_bf16.md, 325.3 MB at "
                        "T = 4096 scaled by 4 to T = 16384"),
+    ("b8h16_t16384_d64_bf16_recall", "delta"):
+        (325.57e6 * 4, "bytes per launch: profiles/seq_block_kernel_delta_b8h16_d64_bf16.md, 325.6 MB at "
+                       "T = 4096 scaled by 4 to T = 16384"),
     ("b8h16_t16384_d64_bf16_recall", "chunked"):
         (156.69e6 * 8, "bytes per launch: profiles/chunk_scan_kernel_b8h16_d64_bf16.md, 156.7 MB at "
                        "T = 2048 scaled by 8 to T = 16384"),
