@@ -205,7 +205,7 @@ class OracleLeg:
         return f"all {self.w.pairs} pairs x first {steps} of {self.w.T} steps of {self.w.name} ({wall:.1f} s wall)"
 
 
-def host_info() -> dict:
+def host_cpu_info() -> dict:
     """The host the oracle ran on: logical CPUs, CPU model, BLAS threads (when threadpoolctl
     is importable)."""
     info = {"host_cpus": os.cpu_count()}
@@ -258,7 +258,7 @@ def run_reference(args, w):
             "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d": w.d, "dv": w.dv, "r": w.r,
                        "io": w.io},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": sample, **host_info()},
+                             "sample": sample, **host_cpu_info()},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -501,7 +501,7 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, cores, sample = oracle_leg(w)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
-                                **host_info()}
+                                **host_cpu_info()}
     if rank == 0:
         print(json.dumps(line), flush=True)
     h.close()

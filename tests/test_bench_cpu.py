@@ -63,3 +63,19 @@ def test_traffic_table_names_its_capture():
             # a capture's DRAM traffic is at least the bytes the launch must stream
             w = workloads.get(name)
             assert traffic >= 0.9 * w.pairs * w.T * bench.streamed_bytes_per_token_head(w)
+
+
+def test_no_function_shadows_a_module_function_it_calls():
+    """bench.py's GPU legs run only on a GPU; this static check catches a local variable
+    that hides a module-level function the same body calls (an error the CPU suite would
+    not reach otherwise)."""
+    import ast
+    tree = ast.parse(open(os.path.join(ROOT, "bench.py")).read())
+    module_funcs = {n.name for n in tree.body if isinstance(n, ast.FunctionDef)}
+    for fn in ast.walk(tree):
+        if not isinstance(fn, ast.FunctionDef):
+            continue
+        stored = {n.id for n in ast.walk(fn) if isinstance(n, ast.Name) and isinstance(n.ctx, ast.Store)}
+        called = {n.func.id for n in ast.walk(fn) if isinstance(n, ast.Call) and isinstance(n.func, ast.Name)}
+        clash = stored & called & module_funcs
+        assert not clash, (fn.name, clash)
