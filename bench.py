@@ -221,6 +221,9 @@ def host_cpu_info() -> dict:
     except OSError:
         pass
     import platform
+    arm_parts = {"0xd4f": "Arm Neoverse V2", "0xd40": "Arm Neoverse V1", "0xd0c": "Arm Neoverse N1"}
+    if model in arm_parts:
+        model = f"{arm_parts[model]} (cpu part {model})"
     info["cpu_model"] = model or platform.processor() or platform.machine()
     try:
         from threadpoolctl import threadpool_info
