@@ -357,8 +357,8 @@ vla_err_t vla_scan_fwd_host(vla_handle_t h, const void* q, const void* k, const 
   const size_t need = bA + bS + bn + kHostSlots * slot;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // CTAs of the gather: the SMs the scan leaves idle (one scan CTA per pair, or per pair
-  // and half in the two-CTA sequential variant), at least 8 and at most 32.
+  // CTAs of the gather: the SMs the scan leaves idle (one scan CTA per pair, two in the
+  // two-CTA cluster variants), at least 8 and at most 32.
   const long long scan_sms = std::min<long long>(pairs * (ctas == 2 ? 2 : 1), h->sm_count);
   const int gather_ctas = (int)std::max<long long>(8, std::min<long long>(32, h->sm_count - scan_sms));
   e = on_device(h->device, [&]() -> cudaError_t {
