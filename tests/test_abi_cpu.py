@@ -1,6 +1,7 @@
 """C ABI checks that need no GPU: the library builds, loads and exports every
 function include/vla.h declares, and argument errors come back as codes."""
 import ctypes
+import os
 
 import pytest
 import torch
@@ -69,3 +70,32 @@ def test_host_entry_point_and_path_info_reject_a_null_handle(lib):
 
 def test_projection_rejects_a_null_handle(lib):
     assert lib.vla_project_u(None, None, None, None, 4, 64, 1, 0, None) == 1
+
+
+def test_header_and_library_serve_a_plain_c_program(lib, tmp_path):
+    """include/vla.h compiles as strict C99 and a C program links against libvla.so and
+    calls through it (NULL handles only: no GPU needed)."""
+    import shutil
+    import subprocess
+    from _util import HEADER
+    import sherman_morrison_inverse_gb300 as vla
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_vla.c"
+    src.write_text(
+        '#include "vla.h"\n'
+        "#include <string.h>\n"
+        "int main(void) {\n"
+        "  vla_status_t st;\n"
+        "  if (vla_destroy(0) != VLA_OK) return 1;\n"
+        "  if (vla_status(0, 0, &st) != VLA_ERR_INVALID_ARG) return 2;\n"
+        "  if (vla_scan_fwd(0, 0, 0, 0, 0, 0, 0, 0, 0, 1, 1, 4, 64, 64, 1, 0, 0.f, 1.f, 0, VLA_F32,\n"
+        "                   VLA_SEQUENTIAL, 0, 0) != VLA_ERR_INVALID_ARG) return 3;\n"
+        "  return strlen(vla_last_error(0)) > 0 ? 0 : 4;\n"
+        "}\n")
+    libdir = os.path.dirname(vla.library_path())
+    exe = tmp_path / "use_vla"
+    cmd = ["gcc", "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.dirname(HEADER),
+           str(src), "-L", libdir, "-lvla", f"-Wl,-rpath,{libdir}", "-o", str(exe)]
+    subprocess.run(cmd, check=True, capture_output=True, text=True)
+    assert subprocess.run([str(exe)]).returncode == 0
