@@ -62,15 +62,16 @@ typedef enum {
 typedef enum { VLA_F32 = 0, VLA_BF16 = 1 } vla_dtype_t;        /* dtype of q, k, v, u, o */
 
 typedef enum {
-  VLA_SEQUENTIAL = 0,   /* one step after another (the pages' recurrence) */
+  VLA_SEQUENTIAL = 0,   /* the pages' recurrence in its step order, taken in rounds of a few
+                           steps in exact Woodbury form (one set of reductions per round;
+                           the same result up to rounding) */
   VLA_CHUNKED = 1,      /* `chunk` steps at a time in exact Woodbury / LDL^T form */
   VLA_DELTA = 2         /* the delta-rule variant (gist.science summary §2.3, "Recursive
                            Update Rule"): A tracked as above, then alpha_hat = A k_hat / |A k_hat|
                            with k_hat = phi(k) / |phi(k)|, S += (v - S k_hat) alpha_hat^T; n,
                            renormalisation and readout unchanged; computed in rounds of
                            several steps like VLA_SEQUENTIAL (CTAs per pair chosen as its
-                           default), so splitting a sequence into calls gives the same bits
-                           only at multiples of the tile (32 steps at d = 64) */
+                           default; see t0 below for split calls) */
 } vla_mode_t;
 
 /* Status flags, ORed over all pairs since the last vla_status() call. */
@@ -102,7 +103,13 @@ vla_err_t vla_create(vla_handle_t* h, int device);
  *   tau       renormalisation threshold on ||S||_F (> 0; +inf disables it).
  *   t0        steps already taken by earlier calls on this state (>= 0): the
  *             nudge fires at global steps t0 + t that are multiples of P, so
- *             splitting a sequence into several calls gives the same result.
+ *             splitting a sequence into several calls computes the same
+ *             recurrence: the same bits when the calls split it at multiples of
+ *             the kernel's input tile (sequential and delta modes: 32 steps at
+ *             d <= 64 and r = 1, 16 at d = 64, r = 4 and at d = 128, r = 1, 8 at
+ *             d = 128, r = 4; chunked mode: the chunk, 64 steps at r = 1 and 16 at
+ *             r = 4; window boundaries of vla_scan_fwd_host count as splits), the
+ *             same values up to rounding elsewhere.
  *   io_dtype  VLA_F32 or VLA_BF16 for q, k, v, u and o; state is always float32.
  *   mode      VLA_SEQUENTIAL (every built shape) or VLA_CHUNKED (d == 64 only;
  *             `chunk` = steps per chunk, see the built list in the library's
