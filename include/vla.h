@@ -108,8 +108,9 @@ vla_err_t vla_create(vla_handle_t* h, int device);
  *             the kernel's input tile (sequential and delta modes: 32 steps at
  *             d <= 64 and r = 1, 16 at d = 64, r = 4 and at d = 128, r = 1, 8 at
  *             d = 128, r = 4; chunked mode: the chunk, 64 steps at r = 1 and 16 at
- *             r = 4; window boundaries of vla_scan_fwd_host count as splits), the
- *             same values up to rounding elsewhere.
+ *             r = 4; window boundaries of vla_scan_fwd_host count as splits) while no
+ *             renormalisation has fired before the split (a call ends by folding
+ *             its lazy scale into S); the same values up to rounding otherwise.
  *   io_dtype  VLA_F32 or VLA_BF16 for q, k, v, u and o; state is always float32.
  *   mode      VLA_SEQUENTIAL (every built shape) or VLA_CHUNKED (d == 64 only;
  *             `chunk` = steps per chunk, see the built list in the library's
