@@ -65,6 +65,14 @@ def streamed_bytes_per_token_head(w) -> int:
 # captured T to the full launch; traffic grows with T).  None when the kernel has
 # changed since its capture.
 TRAFFIC = {
+    ("b16h16_t8192_d64_bf16_r4", "chunked"):
+        (274.16e6 * 8, "bytes per launch: profiles/chunk_scan_kernel_r4_b16h16_d64_bf16.md, 274.2 MB at "
+                       "T = 1024 scaled by 8 to T = 8192"),
+    ("b4h8_t4096_d64_f32", "sequential"):
+        (154.31e6, "bytes per launch: profiles/seq_block_kernel_b4h8_d64_f32.md (the full T = 4096)"),
+    ("b2h8_t65536_d128_f32", "sequential"):
+        (156.39e6 * 16, "bytes per launch: profiles/seq_block_kernel_cluster_b2h8_d128_f32.md, 156.4 MB at "
+                        "T = 4096 scaled by 16 to T = 65536"),
     ("b8h16_t16384_d64_bf16_recall", "sequential"):
         (325.31e6 * 4, "bytes per launch: profiles/seq_block_kernel_b8h16_d64_bf16.md, 325.3 MB at "
                        "T = 4096 scaled by 4 to T = 16384"),
