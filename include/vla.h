@@ -193,9 +193,10 @@ vla_err_t vla_host_path_info(vla_handle_t h, int* gathered, long long* seg);
 /* The learned penalty directions before the scan: for every token t < n_tokens and
  * rank i < r,  u[t][i] = W_u[i] k_raw[t] / max(|W_u[i] k_raw[t]|_2, 1e-12)  (README
  * "VLA v3" item 2, "u_t = normalize(W_u k_t^raw)").  The products run on the tensor
- * cores in tf32 with W (and float32 keys) split into hi + lo parts, accurate to about
- * 2^-21 relative (float32 arithmetic on CUDA cores for d = 128 with float32 keys);
- * the norm and scaling are float32.  A product that does not complete sets
+ * cores: bfloat16 keys as bf16 operands with W carried as three bf16 terms (about 24
+ * bits), float32 keys in tf32 with keys and W split into hi + lo parts (about 2^-21
+ * relative; float32 arithmetic on CUDA cores for d = 128 with float32 keys); fp32
+ * accumulation, norm and scaling.  A product that does not complete sets
  * VLA_STATUS_TIMEOUT in the handle's status.
  *
  *   k_raw     [n_tokens, d] in io_dtype: the keys before the feature map (for the scan's

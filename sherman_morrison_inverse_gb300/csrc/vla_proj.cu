@@ -1,7 +1,8 @@
 // Direction projection u_{t,i} = W_u[i] k_t / max(|W_u[i] k_t|_2, 1e-12) for sm_103a: the
 // README "VLA v3" item 2 "u_t = normalize(W_u k_t^raw)", computed before the scan (whose u
-// input it produces, [n, r, d]).  Two forms: the tensor-core one (below, every shape whose
-// operands fit in shared memory) and a CUDA-core one (d = 128 with float32 keys).
+// input it produces, [n, r, d]).  Three forms: tensor cores with bf16 operands (bfloat16
+// keys), tensor cores in tf32 (float32 keys whose operands fit in shared memory) and CUDA
+// cores (d = 128 with float32 keys).
 //
 // CUDA-core form: each thread takes TPT consecutive tokens (4 at d = 16, 2 at d = 64, 1 at d = 128),
 // groups taken grid-stride, the ranks one after another (W_u[i] in shared memory, d x d
@@ -294,11 +295,159 @@ __global__ void __launch_bounds__(NTH) project_u_tc_kernel(const TIO* __restrict
   if (failed && tid == 0) atomicOr(&status->flags, kStatusTimeout);
 }
 
+// ---------------------------------------------------------------------------
+// bfloat16 keys: the same product as kind::f16 with bf16 operands.  A key row of d bf16
+// values is already a row of operand core matrices, so each 16-byte load is stored as it
+// is; W is carried as three bf16 terms w1 + w2 + w3 (w1 = bf16(W), w2 = bf16(W - w1),
+// w3 = bf16(W - w1 - w2): about 24 bits), three passes with fp32 accumulation.  The
+// operands take 40 KB at d = 64 (the tf32 form 64 KB), so more CTAs share an SM and
+// keep more key rows in flight.
+template <int D>
+struct Bf16Cfg {
+  static constexpr int B_K = 0;                                // [128][D] keys, bf16
+  static constexpr int B_W = B_K + 128 * D * 2;                // 3 x [D][D] W terms, bf16
+  static constexpr int B_END = B_W + 3 * D * D * 2;
+  static constexpr size_t bytes = (size_t)B_END + 16;          // + mbarrier, TMEM slot
+  static constexpr uint32_t TCOLS = D < 32 ? 32 : D;
+};
+
+template <int D>
+__global__ void __launch_bounds__(NTH) project_u_bf16_kernel(const __nv_bfloat16* __restrict__ k,
+                                                             const float* __restrict__ W,
+                                                             __nv_bfloat16* __restrict__ u, long long n, int r,
+                                                             DevStatus* __restrict__ status) {
+  using Cf = Bf16Cfg<D>;
+  using V = Vec<__nv_bfloat16>;
+  using tc::tk16_off;
+  constexpr int NV = D / 8;   // 16-byte vectors (8 bf16) per row
+  static_assert(NTH == 128, "one thread per TMEM lane of an M = 128 product");
+  extern __shared__ __align__(1024) unsigned char smb[];
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smb + Cf::B_END);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const uint32_t sbase = smem_u32(smb);
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tc::tmem_alloc(tslot, Cf::TCOLS);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tslot;
+  const uint32_t tlane = tmem + ((uint32_t)(32 * warp) << 16);
+  uint32_t phase = 0;
+  bool failed = false;
+  auto st16 = [&](int byte_off, const uint4& v) { *reinterpret_cast<uint4*>(smb + byte_off) = v; };
+  const long long ntiles = (n + NTH - 1) / NTH;
+  for (int i = 0; i < r && !failed; ++i) {
+    // W_u[i] -> three bf16 terms, K-major (row j = output, K = input m), 8 values a store
+    for (int e8 = tid; e8 < D * D / 8; e8 += NTH) {
+      const int j = (8 * e8) / D, m = 8 * e8 - j * D;
+      const float4 a = reinterpret_cast<const float4*>(W + (size_t)i * D * D)[2 * e8];
+      const float4 b = reinterpret_cast<const float4*>(W + (size_t)i * D * D)[2 * e8 + 1];
+      float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int term = 0; term < 3; ++term) {
+        float t[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          t[q] = __bfloat162float(__float2bfloat16_rn(x[q]));
+          x[q] -= t[q];   // exact: t is x rounded to 8 significant bits
+        }
+        st16(Cf::B_W + term * D * D * 2 + 2 * tk16_off(j, m, D), V::pack(t));
+      }
+    }
+    auto fetch = [&](long long tile, uint4 (&buf)[NV]) {
+      const long long t = tile * NTH + tid;
+      const uint4* kv = reinterpret_cast<const uint4*>(k + t * D);
+#pragma unroll
+      for (int v = 0; v < NV; ++v) buf[v] = (tile < ntiles && t < n) ? __ldg(kv + v) : make_uint4(0u, 0u, 0u, 0u);
+    };
+    auto process = [&](long long tile, uint4 (&buf)[NV]) -> bool {
+      const long long t = tile * NTH + tid;
+#pragma unroll
+      for (int v = 0; v < NV; ++v) st16(Cf::B_K + 2 * tk16_off(tid, 8 * v, D), buf[v]);
+      fence_proxy_async_smem();
+      tc::fence_before_sync();
+      __syncthreads();
+      tc::fence_after_sync();
+      if (tid == 0) {
+        constexpr uint32_t sbo = 16u * D;
+        constexpr uint32_t idesc = tc::idesc_bf16(128, D);
+#pragma unroll
+        for (int p = 0; p < 3; ++p)
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            tc::mma_f16(tmem, tc::sdesc(sbase + Cf::B_K + 256u * kk, sbo),
+                        tc::sdesc(sbase + Cf::B_W + p * D * D * 2 + 256u * kk, sbo), idesc, p > 0 || kk > 0);
+        tc::mma_commit(bar);
+      }
+      fetch(tile + 2 * (long long)gridDim.x, buf);   // the staged keys are consumed; refill two tiles ahead
+      if (tid == 0 && !mbar_wait_bounded(bar, phase)) failed = true;
+      phase ^= 1u;
+      tc::fence_before_sync();
+      failed = __syncthreads_or(failed) != 0;
+      tc::fence_after_sync();
+      if (failed) return false;
+      constexpr int CW = D < 32 ? 16 : 32;   // columns per TMEM load
+      float nrm = 0.f;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += CW) {
+        float x[CW];
+        if constexpr (CW == 32) tc::tmem_ld32(tlane + (uint32_t)c0, x);
+        else tc::tmem_ld16(tlane + (uint32_t)c0, x);
+#pragma unroll
+        for (int j = 0; j < CW; ++j) nrm = fmaf(x[j], x[j], nrm);
+      }
+      const float inv = 1.f / fmaxf(sqrtf(nrm), 1e-12f);
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += CW) {
+        float x[CW];
+        if constexpr (CW == 32) tc::tmem_ld32(tlane + (uint32_t)c0, x);
+        else tc::tmem_ld16(tlane + (uint32_t)c0, x);
+        if (t < n) {
+          uint4* uv = reinterpret_cast<uint4*>(u + (t * r + i) * D + c0);
+#pragma unroll
+          for (int v = 0; v < CW / 8; ++v) {
+            float y[8];
+#pragma unroll
+            for (int m = 0; m < 8; ++m) y[m] = x[8 * v + m] * inv;
+            uv[v] = V::pack(y);
+          }
+        }
+      }
+      return true;
+    };
+    uint4 ka[NV], kb[NV];
+    fetch(blockIdx.x, ka);
+    fetch(blockIdx.x + (long long)gridDim.x, kb);
+    for (long long tile = blockIdx.x; tile < ntiles; tile += 2 * (long long)gridDim.x) {
+      if (!process(tile, ka)) break;
+      if (tile + gridDim.x < ntiles && !process(tile + gridDim.x, kb)) break;
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 0) tc::tmem_dealloc(tmem, Cf::TCOLS);
+  if (failed && tid == 0) atomicOr(&status->flags, kStatusTimeout);
+}
+
 template <int D, typename TIO>
 cudaError_t launch_project_t(const void* k, const float* W, void* u, long long n, int r, int sm_count,
                              DevStatus* status, cudaStream_t s) {
   const int sms = sm_count > 0 ? sm_count : 1;
-  if constexpr (TcCfg<D, TIO>::bytes <= 227 * 1024) {   // the tensor-core form
+  if constexpr (sizeof(TIO) == 2) {   // bfloat16 keys: kind::f16 with bf16 operands
+    auto kern = project_u_bf16_kernel<D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Bf16Cfg<D>::bytes);
+    if (e != cudaSuccess) return e;
+    const long long ntiles = (n + NTH - 1) / NTH;
+    const int grid = (int)min(ntiles, (long long)sms * 8);
+    kern<<<grid, NTH, Bf16Cfg<D>::bytes, s>>>(static_cast<const __nv_bfloat16*>(k), W,
+                                              static_cast<__nv_bfloat16*>(u), n, r, status);
+    return cudaGetLastError();
+  } else if constexpr (TcCfg<D, TIO>::bytes <= 227 * 1024) {   // float32 keys: kind::tf32
     auto kern = project_u_tc_kernel<D, TIO>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TcCfg<D, TIO>::bytes);

@@ -1,6 +1,6 @@
 // tcgen05 (5th-generation tensor core) helpers for sm_103a: TMEM allocation,
-// shared-memory matrix descriptors, kind::tf32 MMA with an mbarrier commit, and
-// TMEM loads.  All inline PTX.
+// shared-memory matrix descriptors, kind::tf32 and kind::f16 (bf16) MMAs with an
+// mbarrier commit, and TMEM loads.  All inline PTX.
 //
 // Operand layout: "K-major, no swizzle".  A row-major M x K fp32 matrix is
 // stored as 8-row x 16-byte core matrices: element (row, k) sits at float offset
@@ -39,6 +39,33 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
          | (2u << 7) | (2u << 10)        // A, B: tf32
          | ((uint32_t)(N >> 3) << 17)    // N / 8
          | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+
+// 16-bit elements (kind::f16) in the same K-major no-swizzle layout: a core matrix is
+// 8 rows x 8 elements (16 bytes a row), so element (row, k) sits at element offset
+//   (row / 8) * (8 K) + (k / 8) * 64 + (row % 8) * 8 + (k % 8);
+// leading-dimension byte offset 128, stride-dimension byte offset 16 K.  One MMA consumes
+// K = 16 (two core matrices); the next K step starts 256 bytes further on, as for tf32.
+__host__ __device__ constexpr int tk16_off(int row, int k, int K) {
+  return (row >> 3) * (8 * K) + (k >> 3) * 64 + (row & 7) * 8 + (k & 7);
+}
+
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4)                       // D: f32
+         | (1u << 7) | (1u << 10)        // A, B: bf16
+         | ((uint32_t)(N >> 3) << 17)    // N / 8
+         | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+
+// One MMA of kind::f16: D (+)= X * Y^T for one K step of 16.
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t xdesc, uint64_t ydesc, uint32_t idesc,
+                                        bool accumulate) {
+  const uint32_t acc = accumulate ? 1u : 0u;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(xdesc), "l"(ydesc), "r"(idesc), "r"(acc)
+      : "memory");
 }
 
 __device__ __forceinline__ void tmem_alloc(uint32_t* slot_smem, uint32_t ncols) {  // one full warp
