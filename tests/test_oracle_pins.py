@@ -433,11 +433,74 @@ def check_project_u_closed_forms(mod):
     assert rel(u3, sgn * w / np.linalg.norm(w)) < 1e-14
 
 
+# ---- the parity metric (the reading adopted for the workloads' "max relative error")
+
+def check_errors_metric(mod):
+    """errors() on constructed discrepancies whose value is known exactly (dyadic numbers,
+    so every expected value below is exact in float64).
+
+    State X in {A, S, n}: per pair max|X - X_ref| / max|X_ref|, then the max over pairs.
+    Outputs: per row ||o_t - o_ref_t||_inf / ||o_ref_t||_inf, then the max over (pair, t)."""
+    d, dv, T = 3, 2, 3
+    A_ref = np.zeros((2, d, d))
+    A_ref[0] = [[2.0, -1.0, 0.0], [-1.0, 2.0, 0.5], [0.0, 0.5, 1.0]]   # max |.| = 2
+    A_ref[1] = 64.0 * np.eye(d)                                         # max |.| = 64
+    S_ref = np.zeros((2, dv, d))
+    S_ref[0] = [[4.0, -2.0, 1.0], [0.5, 0.25, -4.0]]                    # max |.| = 4
+    S_ref[1] = [[64.0, 8.0, -16.0], [2.0, 1.0, 0.5]]                    # max |.| = 64
+    n_ref = np.array([[1.0, 2.0, 8.0], [0.5, 0.25, 0.125]])             # max 8 and 0.5
+    o_ref = np.zeros((2, T, dv))
+    o_ref[0] = [[1024.0, -512.0], [0.25, -0.125], [2.0, 1.0]]           # rows of very different scale
+    o_ref[1] = [[1.0, 1.0], [-8.0, 4.0], [0.5, 0.5]]
+
+    # identical inputs: every error is exactly zero
+    e = mod.errors(o_ref, A_ref, S_ref, n_ref, o_ref, A_ref, S_ref, n_ref)
+    assert e == dict(o=0.0, A=0.0, S=0.0, n=0.0), e
+
+    A, S, n, o = A_ref.copy(), S_ref.copy(), n_ref.copy(), o_ref.copy()
+    # A: a zero-crossing off-diagonal entry of the small pair moves by 2^-6 -> 2^-6 / 2 = 2^-7;
+    # the large pair's diagonal moves by 2^-2 -> 2^-2 / 64 = 2^-8 (smaller: the max is pair 0's)
+    A[0, 0, 2] = 2.0 ** -6
+    A[1, 1, 1] += 0.25
+    # S: the largest entry of pair 0 moves down by 1 -> 1/4 (normalising by the moved side would
+    # give 1/4 too, so a second entry of pair 1 rises above its reference max: 72 vs 64 -> 8/64)
+    S[0, 0, 0] = 3.0
+    S[1, 0, 0] = 72.0
+    # n: the largest entry of pair 1 moves by 2^-4 on a max of 0.5 -> 2^-3
+    n[1, 0] += 2.0 ** -4
+    # o: row 1 of pair 0 (scale 0.25) moves by 2^-5 -> 2^-3; row 0 (scale 1024) by 8 -> 2^-7
+    o[0, 1, 1] -= 2.0 ** -5
+    o[0, 0, 0] += 8.0
+    e = mod.errors(o, A, S, n, o_ref, A_ref, S_ref, n_ref)
+    assert e["A"] == 2.0 ** -7, e        # per-pair scale, max over pairs
+    assert e["S"] == 0.25, e             # pair 0: 1/4; pair 1: 8/64 = 1/8
+    assert e["n"] == 2.0 ** -3, e
+    assert e["o"] == 2.0 ** -3, e        # per row: pair-wide scaling would give 2^-5 / 1024
+    # the sides are not interchangeable: the reference side (the last four) sets the scale
+    e2 = mod.errors(o_ref, A_ref, S_ref, n_ref, o, A, S, n)
+    assert e2["n"] == 2.0 ** -4 / (0.5 + 2.0 ** -4), e2
+    two = mod.errors(2 * o_ref, 2 * A_ref, 2 * S_ref, 2 * n_ref, o_ref, A_ref, S_ref, n_ref)
+    half = mod.errors(o_ref, A_ref, S_ref, n_ref, 2 * o_ref, 2 * A_ref, 2 * S_ref, 2 * n_ref)
+    assert two == dict(o=1.0, A=1.0, S=1.0, n=1.0), two
+    assert half == dict(o=0.5, A=0.5, S=0.5, n=0.5), half
+    # the sign of a discrepancy does not matter
+    e3 = mod.errors(2 * o_ref - o, 2 * A_ref - A, 2 * S_ref - S, 2 * n_ref - n, o_ref, A_ref, S_ref, n_ref)
+    assert e3 == e, (e3, e)
+    # a single pair of several: the error of one bad pair is not averaged away
+    N = 8
+    big = np.broadcast_to(A_ref[1], (N, d, d)).copy()
+    bad = big.copy()
+    bad[5, 2, 0] = 16.0
+    assert mod.errors(np.zeros((N, 0, dv)), bad, big[:, :dv], big[:, 0], np.zeros((N, 0, dv)), big,
+                      big[:, :dv], big[:, 0])["A"] == 0.25
+
+
 CHECKS = [check_golden_worked, check_exact_rational, check_gauss_jordan, check_d1_closed_form,
           check_basis_cycling, check_woodbury_rank_r, check_ldl_pivots, check_alpha_least_squares,
           check_invariants, check_guard, check_renorm, check_split_calls,
           check_readout_bruteforce, check_phi, check_delta_d1_overwrite, check_delta_residual_contraction,
-          check_delta_orthogonal_untouched, check_delta_tracks_the_same_A, check_project_u_closed_forms]
+          check_delta_orthogonal_untouched, check_delta_tracks_the_same_A, check_project_u_closed_forms,
+          check_errors_metric]
 
 
 @pytest.mark.parametrize("check", CHECKS, ids=lambda c: c.__name__)
@@ -551,6 +614,16 @@ MUTATIONS = {
     "project_transposed_W": ('x = np.einsum("ijm,nm->nij", W_u, k_raw)', 'x = np.einsum("imj,nm->nij", W_u, k_raw)'),
     "project_no_normalise": ("return x / np.maximum(np.linalg.norm(x, axis=-1, keepdims=True), NORM_EPS)",
                              "return x"),
+    # the parity metric
+    "errors_scale_from_tested_side": ("den = np.abs(xr).reshape(xr.shape[0], -1).max(axis=1)",
+                                      "den = np.abs(x).reshape(x.shape[0], -1).max(axis=1)"),
+    "errors_mean_over_pairs": ("return float(np.max(num / np.maximum(den, 1e-300))) if x.size else 0.0",
+                               "return float(np.mean(num / np.maximum(den, 1e-300))) if x.size else 0.0"),
+    "errors_global_scale": ("den = np.abs(xr).reshape(xr.shape[0], -1).max(axis=1)",
+                            "den = np.abs(xr).max()"),
+    "errors_o_scaled_per_pair": ("den = np.abs(o_ref).max(axis=2)",
+                                 "den = np.abs(o_ref).max(axis=(1, 2))[:, None]"),
+    "errors_o_signed": ("num = np.abs(o - o_ref).max(axis=2)", "num = (o - o_ref).max(axis=2)"),
 }
 
 
