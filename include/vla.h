@@ -266,6 +266,9 @@ vla_err_t vla_destroy(vla_handle_t h);
  * - The first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress) and keeps it for later calls; make that first call
  *   before any stream capture on that device.
+ * - That kept address does not survive cudaDeviceReset: the reset unloads the
+ *   library's device code, and the array may come back elsewhere.  A process
+ *   that resets a device must not call this entry point on it afterwards.
  *
  * Errors (returned before any launch): INVALID_ARG as for vla_scan_fwd, and when
  * B*H exceeds VLA_NOALLOC_MAX_PAIRS; UNSUPPORTED for shapes other than

@@ -57,9 +57,8 @@ namespace chk {
 constexpr int D = 64;
 constexpr int NT = 256;
 constexpr int TILE = 64 * 64;         // floats of a TK(64, 64) operand tile
-constexpr int GLD = 65;               // leading dimension of the fp32 G / L staging
+constexpr int GLD = 68;               // leading dimension of the fp32 G / L staging (16-byte rows)
 constexpr int PLD = 68;               // leading dimension of the prologue's phi(k) / phi(q) scratch
-constexpr int BLK = 272;              // floats per packed 16 x 16 block (leading dimension 17)
 constexpr float kGuardEps = 1e-6f;
 constexpr float kReadoutEps = 1e-6f;
 constexpr float kInvSqrtD = 0.125f;
@@ -73,8 +72,16 @@ __device__ __forceinline__ float tf32_hi(float x) { return __uint_as_float(__flo
 // the chunked path serves bf16 I/O, whose rounding is far coarser)
 __device__ __forceinline__ float phi_fast(float x) { return x > 0.f ? x + 1.f : __expf(x); }
 
-// packed lower-triangular 16 x 16 block (bi >= bj) of a 64 x 64 matrix
-__host__ __device__ constexpr int pblk(int bi, int bj) { return (bi * (bi + 1) / 2 + bj) * BLK; }
+// packed 8 x 8 blocks (leading dimension 9) of a 64 x 64 lower-triangular matrix: block (bi, bj)
+// with bi >= bj, and the strictly lower blocks (bi > bj) of a second one
+__host__ __device__ constexpr int pb8(int bi, int bj) { return (bi * (bi + 1) / 2 + bj) * 72; }
+__host__ __device__ constexpr int pbB(int bi, int bj) { return (bi * (bi - 1) / 2 + bj) * 72; }
+
+// named barriers (ids 1..5; 0 is __syncthreads): `n` threads take part, a multiple of 32
+__device__ __forceinline__ void bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+__device__ __forceinline__ void bar_arrive(int id, int n) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
 
 template <int R, typename TIO>
 struct Cfg {
@@ -113,7 +120,7 @@ struct Cfg {
   static_assert(3 * T6T <= 3 * TILE, "T6 fits in R and L");
   static_assert(64 * GLD <= 2 * TILE, "staging fits in P");
   static_assert(2 * C * PLD <= 3 * TILE, "prologue scratch fits in R and L");
-  static_assert(pblk(3, 3) + BLK <= TILE, "packed blocks fit in one tile");
+  static_assert(pb8(7, 7) + 72 <= TILE && pbB(7, 6) + 72 <= TILE, "packed blocks fit in one tile");
   static_assert(bytes <= 227 * 1024, "shared memory");
 };
 
@@ -228,10 +235,15 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
   auto st4 = [&](int off, float x0, float x1, float x2, float x3) {
     *reinterpret_cast<float4*>(sf + off) = make_float4(x0, x1, x2, x3);
   };
+  // 3xTF32 operands: the tensor core reads an fp32 operand as tf32 by dropping its low 13
+  // mantissa bits, so the fp32 value itself is the high part; the low part x - tf32_hi(x)
+  // is stored beside it
+  auto st4_lo = [&](int off_lo, const float* x) {
+    st4(off_lo, x[0] - tf32_hi(x[0]), x[1] - tf32_hi(x[1]), x[2] - tf32_hi(x[2]), x[3] - tf32_hi(x[3]));
+  };
   auto st4_split = [&](int off_hi, int off_lo, const float* x) {
-    const float h0 = tf32_hi(x[0]), h1 = tf32_hi(x[1]), h2 = tf32_hi(x[2]), h3 = tf32_hi(x[3]);
-    st4(off_hi, h0, h1, h2, h3);
-    st4(off_lo, x[0] - h0, x[1] - h1, x[2] - h2, x[3] - h3);
+    st4(off_hi, x[0], x[1], x[2], x[3]);
+    st4_lo(off_lo, x);
   };
 
   // x[jj] <- x[(jj + g) & 15]: with g = (lane / 4) % 8, store jj of a transposed write then
@@ -423,17 +435,17 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
         fence_proxy_async_smem();
         issue(tile + 1);
       }
-      // A -> hi (R tile 0) + lo (R tile 1)
+      // A's low part -> R tile 1 (A itself is the high part)
       for (int e4 = tid; e4 < TILE / 4; e4 += NT) {
         const float4 x = *reinterpret_cast<const float4*>(sf + Cf::F_A + 4 * e4);
         const float xv[4] = {x.x, x.y, x.z, x.w};
-        st4_split(Cf::F_R + 4 * e4, Cf::F_R + TILE + 4 * e4, xv);
+        st4_lo(Cf::F_R + TILE + 4 * e4, xv);
       }
     }
 
     // ---------------- G1: [W^T; Q^T] = [U; Sigma] A_0^T  (M 128, N 64, K 64), A_0 hi + lo
     {
-      const MmaPass ps[2] = {{Cf::F_P, Cf::F_R, 128, 64, 0, false},
+      const MmaPass ps[2] = {{Cf::F_P, Cf::F_A, 128, 64, 0, false},
                              {Cf::F_P, Cf::F_R + TILE, 128, 64, 0, true}};
       if (!mma_run(ps, 2, 64)) { failed = true; break; }
     }
@@ -469,7 +481,10 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
         float (&v)[16] = *reinterpret_cast<float(*)[16]>(v32 + 16 * cc);
         if (row < 64) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) Gs[row * GLD + col0 + j] = v[j] + ((row == col0 + j) ? 1.f : 0.f);
+          for (int j = 0; j < 16; j += 4)
+            *reinterpret_cast<float4*>(Gs + row * GLD + col0 + j) =
+                make_float4(v[j] + ((row == col0 + j) ? 1.f : 0.f), v[j + 1] + ((row == col0 + j + 1) ? 1.f : 0.f),
+                            v[j + 2] + ((row == col0 + j + 2) ? 1.f : 0.f), v[j + 3] + ((row == col0 + j + 3) ? 1.f : 0.f));
         } else {   // H^T (rows t) fp32 -> R tile 1 (rows 64 + t of [W; H^T])
 #pragma unroll
           for (int j = 0; j < 16; j += 4) st4(Cf::F_R + tk_off(row, col0 + j, 64), v[j], v[j + 1], v[j + 2], v[j + 3]);
@@ -479,234 +494,202 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     tc::fence_before_sync();
     __syncthreads();
 
-    // ---------------- LDL^T of G and X = L^{-1} in 16 x 16 blocks (fp32)
-    // Right-looking block LDL^T with the inverse carried along as a forward
-    // elimination of the identity.  For block column k:
-    //   [a] one warp factors the diagonal block G'_kk = L_kk D_k L_kk^T (2 x 2 blocks of 8)
-    //       and forms X_kk = L_kk^{-1} from the factors in its registers;
-    //   [b] the product of X_kk with 48 columns, 4 lanes a column: the panel rows
-    //       (L D)_r = X_kk G'_rk (i > k) and the columns of X_kj = X_kk B_kj (j < k);
-    //   [c] trailing G'_ij -= L_ik D_k L_jk^T (k < j <= i) and B_ij -= L_ik X_kj (j <= k < i),
-    // where B is the identity being eliminated (B_ij = 0 for i != j at the start).
-    // [c] of step k runs beside [a] of step k + 1: warp 0 updates the next diagonal
-    // block itself and factors it while the other warps update the remaining blocks.
-    // L D (the panel before D^{-1}) is kept, transposed, in the unused upper blocks of the staging.
-    float* XB = sf + Cf::F_Q;   // packed blocks: B, then X = L^{-1}
-    // in-register LDL^T of an 8 x 8 symmetric block (lower triangle of a): a -> L (strict
-    // lower), dd = D, idd = 1 / D
-    auto ldl8 = [](float (&a)[8][8], float (&dd)[8], float (&idd)[8]) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        dd[j] = a[j][j];
-        idd[j] = __fdividef(1.f, dd[j]);
-#pragma unroll
-        for (int i = j + 1; i < 8; ++i) {
-          const float lij = a[i][j] * idd[j];
-#pragma unroll
-          for (int m = j + 1; m <= i; ++m) a[i][m] = fmaf(-lij, a[m][j], a[i][m]);   // a[m][j] = L[m][j] D_j
-        }
-#pragma unroll
-        for (int i = j + 1; i < 8; ++i) a[i][j] *= idd[j];
-      }
-    };
-    // a 2 x 4 tile of [c] for step kc: block blk in the order (trailing blocks, B blocks),
-    // rows 2 rr, 2 rr + 1 and columns 4 cc .. 4 cc + 3 of the block
-    auto trail_tile = [&](int kc, int blk, int rr, int cc) {
-      const int ntr = (3 - kc) * (4 - kc) / 2;
-      const float* lrow;   // L_ik rows (16 values each, stride GLD)
-      const float* xcol;   // columns of (L D)^T_jk or X_kj, row stride sx
-      float* dst;          // destination rows, stride sd
-      int sx, sd;
-      bool fresh = false;
-      if (blk < ntr) {
-        int bi = kc + 1, cnt = blk;   // blk -> (bi, bj) over the lower block triangle of kc+1..3
-#pragma unroll
-        for (int q = 0; q < 6; ++q)
-          if (cnt > bi - (kc + 1)) { cnt -= bi - kc; ++bi; }
-        const int gr = 16 * bi + 2 * rr, gc = 16 * (kc + 1 + cnt) + 4 * cc;
-        lrow = Gs + gr * GLD + 16 * kc;
-        xcol = Gs + 16 * kc * GLD + gc;
-        sx = GLD;
-        dst = Gs + gr * GLD + gc;
-        sd = GLD;
-      } else {
-        const int b2 = blk - ntr, bi = kc + 1 + b2 / (kc + 1), bj = b2 % (kc + 1);
-        lrow = Gs + (16 * bi + 2 * rr) * GLD + 16 * kc;
-        xcol = XB + pblk(kc, bj) + 4 * cc;
-        sx = 17;
-        dst = XB + pblk(bi, bj) + 2 * rr * 17 + 4 * cc;
-        sd = 17;
-        fresh = (kc == bj);   // B_ij starts at 0
-      }
-      float acc[2][4];
-#pragma unroll
-      for (int a2 = 0; a2 < 2; ++a2)
-#pragma unroll
-        for (int b4 = 0; b4 < 4; ++b4) acc[a2][b4] = 0.f;
-#pragma unroll
-      for (int m = 0; m < 16; ++m) {
-        const float l0 = lrow[m], l1 = lrow[GLD + m];
-#pragma unroll
-        for (int b4 = 0; b4 < 4; ++b4) {
-          const float x = xcol[m * sx + b4];
-          acc[0][b4] = fmaf(l0, x, acc[0][b4]);
-          acc[1][b4] = fmaf(l1, x, acc[1][b4]);
-        }
-      }
-#pragma unroll
-      for (int a2 = 0; a2 < 2; ++a2)
-#pragma unroll
-        for (int b4 = 0; b4 < 4; ++b4) {
-          float& dv = dst[a2 * sd + b4];
-          dv = (fresh ? 0.f : dv) - acc[a2][b4];
-        }
-    };
+    // ---------------- LDL^T of G and X = L^{-1} in 8 x 8 blocks (fp32)
+    // Right-looking block LDL^T by block columns of 8.  Warp 0 walks the critical path alone:
+    // for block column k it factors the 8 x 8 diagonal block in every lane's registers, turns
+    // the rows below it into L (forward substitution against L_kk, then D^{-1}), and applies
+    // column k's contribution -L_{.k} D_k L_{k+1,k}^T to block column k+1, so that the next
+    // step can start at once.  Six helper warps follow one step behind: they form block row k
+    // of X = L^{-1} (X_kj = L_kk^{-1} B_kj, where B is the identity being eliminated), update
+    // B_ij -= L_ik X_kj for i > k, and apply column k's contribution to the block columns
+    // beyond k + 1.  Warp 0 and the helpers hand over through named barriers (LB: column k of
+    // L is written; UB: the helpers' trailing update for column k is done), used in
+    // alternation so that a barrier is never reused before its previous round completed.
+    // Warp 4 shares warp 0's SM sub-partition and stays idle.
+    float* XB = sf + Cf::F_Q;   // X = L^{-1}: 36 lower 8 x 8 blocks, leading dimension 9
+    float* BB = sf + Cf::F_L;   // B: 28 strictly lower 8 x 8 blocks
+    if (warp == 0) {
+      float* dsc = misc + Cf::M_VEC;   // warp 0's broadcast scratch (64 floats)
+      auto ld8 = [](const float* pp, float (&v)[8]) {
+        const float4 a0 = *reinterpret_cast<const float4*>(pp), a1 = *reinterpret_cast<const float4*>(pp + 4);
+        v[0] = a0.x; v[1] = a0.y; v[2] = a0.z; v[3] = a0.w; v[4] = a1.x; v[5] = a1.y; v[6] = a1.z; v[7] = a1.w;
+      };
+      auto st8 = [](float* pp, const float (&v)[8]) {
+        *reinterpret_cast<float4*>(pp) = make_float4(v[0], v[1], v[2], v[3]);
+        *reinterpret_cast<float4*>(pp + 4) = make_float4(v[4], v[5], v[6], v[7]);
+      };
 #pragma unroll 1
-    for (int k = 0; k < 4; ++k) {
-      if (warp == 0) {
-        if (k > 0) {   // step k-1's update of diagonal block k (block 0 of the trailing list)
-          trail_tile(k - 1, 0, lane >> 2, lane & 3);
+      for (int k = 0; k < 8; ++k) {
+        const int r0 = 8 * k + lane, r1 = r0 + 32;   // this lane's rows of block column k
+        const bool va = r0 < 64, vb = r1 < 64;
+        float ga[8], gb[8];
+        if (va) ld8(Gs + r0 * GLD + 8 * k, ga);
+        else {
+#pragma unroll
+          for (int c = 0; c < 8; ++c) ga[c] = 0.f;
+        }
+        if (vb) ld8(Gs + r1 * GLD + 8 * k, gb);
+        else {
+#pragma unroll
+          for (int c = 0; c < 8; ++c) gb[c] = 0.f;
+        }
+        if (lane < 8) st8(dsc + 8 * lane, ga);   // the diagonal block, to every lane
+        __syncwarp();
+        float a8[8][8], d8[8], id8[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+#pragma unroll
+          for (int c = 0; c <= r; ++c) a8[r][c] = dsc[8 * r + c];
+        __syncwarp();
+        // a8 -> L_kk (strict lower), d8 = D_k, id8 = 1 / D_k
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          d8[j] = a8[j][j];
+          id8[j] = __fdividef(1.f, d8[j]);
+#pragma unroll
+          for (int i = j + 1; i < 8; ++i) {
+            const float lij = a8[i][j] * id8[j];
+#pragma unroll
+            for (int m = j + 1; m <= i; ++m) a8[i][m] = fmaf(-lij, a8[m][j], a8[i][m]);   // a8[m][j] = L_mj D_j
+          }
+#pragma unroll
+          for (int i = j + 1; i < 8; ++i) a8[i][j] *= id8[j];
+        }
+        // rows -> L: (L D)_r = G'_r L_kk^{-T} by forward substitution, then times D^{-1}.  For the
+        // diagonal rows (lanes 0..7) the entries left of the diagonal are L_kk's.
+        auto panel = [&](float (&g)[8]) {
+#pragma unroll
+          for (int c = 1; c < 8; ++c)
+#pragma unroll
+            for (int m = 0; m < c; ++m) g[c] = fmaf(-a8[c][m], g[m], g[c]);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) g[c] *= id8[c];
+        };
+        panel(ga);
+        panel(gb);
+        if (va) st8(Gs + r0 * GLD + 8 * k, ga);
+        if (vb) st8(Gs + r1 * GLD + 8 * k, gb);
+        if (lane == 0) {
+          st8(misc + Cf::M_D + 8 * k, d8);
+          st8(misc + Cf::M_ID + 8 * k, id8);
+        }
+        bar_arrive(1 + (k & 1), 224);   // LB: block column k of L and D_k are written
+        if (k < 7) {
+          // the helpers' update of block column k + 1 from column k - 1 is done
+          if (k >= 1) bar_sync(3 + ((k - 1) & 1), 224);
+          // column k's contribution to block column k + 1: rows of block k + 1 are lanes 8..15
+          if (lane >= 8 && lane < 16) {
+            float t[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) t[c] = ga[c] * d8[c];   // (L D)_{k+1,k}
+            st8(dsc + 8 * (lane - 8), t);
+          }
           __syncwarp();
-        }
-        // [a]: G'_kk as 2 x 2 blocks of 8: B00 = L00 D0 L00^T in every lane's registers, the rows
-        // of L10 by lanes 0..7, the Schur complement B11 - L10 D0 L10^T by all lanes, then its
-        // LDL^T again in every lane (no shuffles; L10 D0 goes, transposed, into the block's
-        // upper half, which nothing reads afterwards)
-        const int b0 = 16 * k;
-        float a8[8][8], d0[8], id0[8];
-#pragma unroll
-        for (int r = 0; r < 8; ++r)
-#pragma unroll
-          for (int cl = 0; cl <= r; ++cl) a8[r][cl] = Gs[(b0 + r) * GLD + b0 + cl];
-        ldl8(a8, d0, id0);
-        if (lane < 8) {   // row 8 + lane: L10 D0 = B10 L00^{-T}
-          const int r = b0 + 8 + lane;
-          float y[8];
-#pragma unroll
-          for (int cl = 0; cl < 8; ++cl) y[cl] = Gs[r * GLD + b0 + cl];
-#pragma unroll
-          for (int cl = 1; cl < 8; ++cl)
-#pragma unroll
-            for (int m = 0; m < cl; ++m) y[cl] = fmaf(-a8[cl][m], y[m], y[cl]);
-#pragma unroll
-          for (int cl = 0; cl < 8; ++cl) {
-            Gs[(b0 + cl) * GLD + r] = y[cl];               // L10 D0, transposed
-            Gs[r * GLD + b0 + cl] = y[cl] * id0[cl];       // L10
-          }
-        }
-        __syncwarp();
-        for (int e = lane; e < 36; e += 32) {   // Schur complement, lower triangle (row i, column m)
-          int i = 0, m = e;
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            if (m > i) { m -= i + 1; ++i; }
-          const int gr = b0 + 8 + i;
-          float acc = Gs[gr * GLD + b0 + 8 + m];
-#pragma unroll
-          for (int cl = 0; cl < 8; ++cl) acc = fmaf(-Gs[gr * GLD + b0 + cl], Gs[(b0 + cl) * GLD + b0 + 8 + m], acc);
-          Gs[gr * GLD + b0 + 8 + m] = acc;
-        }
-        __syncwarp();
-        float a1[8][8], d1[8], id1[8];
-#pragma unroll
-        for (int r = 0; r < 8; ++r)
-#pragma unroll
-          for (int cl = 0; cl <= r; ++cl) a1[r][cl] = Gs[(b0 + 8 + r) * GLD + b0 + 8 + cl];
-        ldl8(a1, d1, id1);
-        // X_kk = L_kk^{-1}, column c = lane & 15 (lanes 16..31 repeat 0..15 and do not
-        // store): x_top = L00^{-1} e_c[0..7], x_bot = L11^{-1} (e_c[8..15] - L10 x_top), with
-        // L00, L11 in registers and L10 in the staging; entries above the diagonal stay 0
-        {
-          const int c = lane & 15;
-          float xt[8], xb[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            xt[i] = (i == c) ? 1.f : 0.f;
-            xb[i] = (i + 8 == c) ? 1.f : 0.f;
-          }
-#pragma unroll
-          for (int i = 1; i < 8; ++i)
-#pragma unroll
-            for (int m = 0; m < i; ++m) xt[i] = fmaf(-a8[i][m], xt[m], xt[i]);
+          float ldm[8][8];
 #pragma unroll
           for (int i = 0; i < 8; ++i)
 #pragma unroll
-            for (int m = 0; m < 8; ++m) xb[i] = fmaf(-Gs[(b0 + 8 + i) * GLD + b0 + m], xt[m], xb[i]);
+            for (int c = 0; c < 8; ++c) ldm[i][c] = dsc[8 * i + c];
+          auto upd = [&](int r, const float (&l)[8]) {
+            float cur[8];
+            ld8(Gs + r * GLD + 8 * (k + 1), cur);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              float acc = 0.f;
+#pragma unroll
+              for (int c = 0; c < 8; ++c) acc = fmaf(l[c], ldm[i][c], acc);
+              cur[i] -= acc;
+            }
+            st8(Gs + r * GLD + 8 * (k + 1), cur);
+          };
+          if (lane >= 8 && va) upd(r0, ga);
+          if (vb) upd(r1, gb);
+          __syncwarp();
+        }
+      }
+    } else if (warp != 4) {
+      const int ot = ((warp < 4) ? warp - 1 : warp - 2) * 32 + lane;   // 0..191
+#pragma unroll 1
+      for (int m = 0; m < 8; ++m) {
+        bar_sync(1 + (m & 1), 224);   // LB: block column m of L is written
+        // block row m of X: X_mj = L_mm^{-1} B_mj (j < m), X_mm = L_mm^{-1}; a column per thread
+        if (ot < 8 * (m + 1)) {
+          const int j = ot >> 3, c = ot & 7;
+          float x[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) x[i] = (j == m) ? ((i == c) ? 1.f : 0.f) : BB[pbB(m, j) + 9 * i + c];
+          const float* lmm = Gs + 8 * m * GLD + 8 * m;
 #pragma unroll
           for (int i = 1; i < 8; ++i)
 #pragma unroll
-            for (int m = 0; m < i; ++m) xb[i] = fmaf(-a1[i][m], xb[m], xb[i]);
-          if (lane < 16) {
+            for (int pp = 0; pp < i; ++pp) x[i] = fmaf(-lmm[i * GLD + pp], x[pp], x[i]);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              XB[pblk(k, k) + i * 17 + c] = xt[i];
-              XB[pblk(k, k) + (8 + i) * 17 + c] = xb[i];
+          for (int i = 0; i < 8; ++i) XB[pb8(m, j) + 9 * i + c] = x[i];
+        }
+        bar_sync(5, 192);
+        if (m < 7) {
+          // 2 x 4 tiles of: B_ij -= L_im X_mj (i > m, j <= m; B_im starts at 0), and of the
+          // trailing update G'_ic -= L_im D_m L_cm^T (c >= m + 2, i >= c)
+          const int nb = (7 - m) * (m + 1), nt = (6 - m) * (7 - m) / 2;
+          const float* dm = misc + Cf::M_D + 8 * m;
+          for (int q = ot; q < 8 * (nb + nt); q += 192) {
+            const int blk = q >> 3, rr = (q >> 1) & 3, cc = q & 1;
+            float acc[2][4];
+#pragma unroll
+            for (int a2 = 0; a2 < 2; ++a2)
+#pragma unroll
+              for (int b4 = 0; b4 < 4; ++b4) acc[a2][b4] = 0.f;
+            if (blk < nb) {
+              const int i = m + 1 + blk / (m + 1), j = blk % (m + 1);
+              const float* lr = Gs + (8 * i + 2 * rr) * GLD + 8 * m;
+              const float* xc = XB + pb8(m, j) + 4 * cc;
+#pragma unroll
+              for (int pp = 0; pp < 8; ++pp) {
+                const float l0 = lr[pp], l1 = lr[GLD + pp];
+#pragma unroll
+                for (int b4 = 0; b4 < 4; ++b4) {
+                  const float xv = xc[9 * pp + b4];
+                  acc[0][b4] = fmaf(l0, xv, acc[0][b4]);
+                  acc[1][b4] = fmaf(l1, xv, acc[1][b4]);
+                }
+              }
+              float* dst = BB + pbB(i, j) + 9 * 2 * rr + 4 * cc;
+#pragma unroll
+              for (int a2 = 0; a2 < 2; ++a2)
+#pragma unroll
+                for (int b4 = 0; b4 < 4; ++b4) {
+                  float& dv = dst[9 * a2 + b4];
+                  dv = ((j == m) ? 0.f : dv) - acc[a2][b4];
+                }
+            } else {
+              int c = m + 2, rem = blk - nb;
+              while (rem >= 8 - c) { rem -= 8 - c; ++c; }
+              const int i = c + rem;
+              const float* lr = Gs + (8 * i + 2 * rr) * GLD + 8 * m;
+              const float* lc = Gs + (8 * c + 4 * cc) * GLD + 8 * m;
+#pragma unroll
+              for (int pp = 0; pp < 8; ++pp) {
+                const float dp = dm[pp];
+                const float l0 = lr[pp] * dp, l1 = lr[GLD + pp] * dp;
+#pragma unroll
+                for (int b4 = 0; b4 < 4; ++b4) {
+                  const float lv = lc[b4 * GLD + pp];
+                  acc[0][b4] = fmaf(l0, lv, acc[0][b4]);
+                  acc[1][b4] = fmaf(l1, lv, acc[1][b4]);
+                }
+              }
+              float* dst = Gs + (8 * i + 2 * rr) * GLD + 8 * c + 4 * cc;
+#pragma unroll
+              for (int a2 = 0; a2 < 2; ++a2)
+#pragma unroll
+                for (int b4 = 0; b4 < 4; ++b4) dst[GLD * a2 + b4] -= acc[a2][b4];
             }
           }
-        }
-        if (lane == 0) {
-#pragma unroll
-          for (int r = 0; r < 8; ++r) {
-            misc[Cf::M_D + b0 + r] = d0[r];
-            misc[Cf::M_ID + b0 + r] = id0[r];
-            misc[Cf::M_D + b0 + 8 + r] = d1[r];
-            misc[Cf::M_ID + b0 + 8 + r] = id1[r];
-          }
-        }
-      } else if (k > 0 && warp != 4) {   // the rest of step k-1's [c]; warp 4 leaves warp 0's
-                                         // sub-partition to it
-        const int kc = k - 1;
-        const int nblk = (3 - kc) * (4 - kc) / 2 + (3 - kc) * (kc + 1);
-        const int w6 = (warp < 4) ? warp - 1 : warp - 2;   // 0..5
-        for (int q = 32 * w6 + lane; q < 32 * (nblk - 1); q += 6 * 32)
-          trail_tile(kc, 1 + (q >> 5), (q >> 2) & 7, q & 3);
-      }
-      __syncthreads();
-      if (warp < 6) {   // [b]: Y = X_kk R for the 48 right-hand columns R, 4 lanes a column
-        // columns 0 .. npan-1: panel rows r = 16 (k+1) + col (Y = (L D)_r, stored transposed in
-        // the upper block and, times D^{-1}, as L_r); the rest: columns of B_kj, j < k (Y = X_kj)
-        const int npan = 48 - 16 * k;
-        const int col = 8 * warp + (lane >> 2), g = lane & 3;   // rows 4 g .. 4 g + 3 of Y
-        float* rp;      // column col of R: element m at rp[m * rs]
-        int rs;
-        int r = 0;
-        if (col < npan) {
-          r = 16 * (k + 1) + col;
-          rp = Gs + r * GLD + 16 * k;
-          rs = 1;
-        } else {
-          const int idx = col - npan, bj = idx >> 4, cl = idx & 15;
-          rp = XB + pblk(k, bj) + cl;
-          rs = 17;
-        }
-        float rv[16];
-#pragma unroll
-        for (int m = 0; m < 16; ++m) rv[m] = rp[m * rs];
-        const float* xr = XB + pblk(k, k) + 4 * g * 17;
-        float y[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          float acc = 0.f;
-#pragma unroll
-          for (int m = 0; m < 16; ++m) acc = fmaf(xr[j * 17 + m], rv[m], acc);
-          y[j] = acc;
-        }
-        __syncwarp();   // the column's 4 lanes are in this warp: all read R before any writes it
-        if (col < npan) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int i = 4 * g + j;
-            Gs[(16 * k + i) * GLD + r] = y[j];                             // L D, transposed (upper block)
-            rp[i] = y[j] * misc[Cf::M_ID + 16 * k + i];                    // L
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) rp[(4 * g + j) * 17] = y[j];
+          if (m <= 5) bar_arrive(3 + (m & 1), 224);   // UB: columns >= m + 2 have column m's part
         }
       }
-      __syncthreads();
     }
-    // step 3 has no [c]
+    __syncthreads();
     // pivot check: the guard would fire inside the chunk
     int bad = 0;
     if (tid < 64) {
@@ -796,18 +779,18 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
       for (int s = 0; s < 4; ++s) {
         const int f = tid + NT * s;
         const int l = (f >> 7) * 8 + (f & 7), j4 = ((f >> 3) & 15) * 4;
-        const int bi = l >> 4, bj = j4 >> 4;
+        const int bi = l >> 3, bj = j4 >> 3;
         loff[s] = tk_off(l, j4, 64);
 #pragma unroll
-        for (int m = 0; m < 4; ++m) lv[s][m] = (bi >= bj) ? Xp[pblk(bi, bj) + (l & 15) * 17 + (j4 & 15) + m] : 0.f;
+        for (int m = 0; m < 4; ++m) lv[s][m] = (bi >= bj) ? Xp[pb8(bi, bj) + (l & 7) * 9 + (j4 & 7) + m] : 0.f;
       }
       __syncthreads();
 #pragma unroll
       for (int s = 0; s < 4; ++s) st4_split(Cf::F_L + loff[s], Cf::F_Q + loff[s], lv[s]);
-      for (int e4 = tid; e4 < 2 * TILE / 4; e4 += NT) {
+      for (int e4 = tid; e4 < 2 * TILE / 4; e4 += NT) {   // [W; H^T] stays as the high part
         const float4 x = *reinterpret_cast<const float4*>(sf + Cf::F_R + 4 * e4);
         const float xv[4] = {x.x, x.y, x.z, x.w};
-        st4_split(Cf::F_R + 4 * e4, Cf::F_P + 4 * e4, xv);
+        st4_lo(Cf::F_P + 4 * e4, xv);
       }
     }
     // ---------------- G3: [Z; F^T] = [W; H^T] Linv^T  (M 128, N 64, K 64), 3xTF32

@@ -1,12 +1,20 @@
 """GPU parity of the direction projection u = normalize(W_u k_raw) (vla_project_u).
 
 README "VLA v3" item 2 forms the scan's directions as u_t = normalize(W_u k_t^raw).
-The kernel computes it in float32; the float64 oracle (oracle.project_u, pinned by
-closed forms) on the same rounded keys and float32 weights, rounded to the I/O
-dtype, is the reference.  The tolerance follows from the arithmetic: a float32 dot
-product of length d errs by at most about d * 2^-24 times the sum of its terms' sizes,
-i.e. a few 1e-6 in absolute terms on a unit vector, and a bfloat16 result may round
-to the neighbour of the rounded float64 value (one unit in the last place).
+The float64 oracle (oracle.project_u, pinned by closed forms) on the same rounded
+keys and float32 weights, rounded to the I/O dtype, is the reference.
+
+The kernel's arithmetic: float32 keys go through tcgen05 kind::tf32 with keys and W
+split into tf32 high and low parts (about 2^-21 relative); bfloat16 keys (exact in
+bf16) go through kind::f16 with W carried as three bfloat16 terms w1 + w2 + w3
+(about 24 bits), accumulated in float32.  The tolerance follows: a float32 dot
+product of length d errs by at most about d * 2^-24 times the sum of its terms'
+sizes, a few 1e-6 in absolute terms on a unit vector, and a bfloat16 result may
+round to the neighbour of the rounded float64 value (one unit in the last place).
+Because one ulp would also hide a lost W term (w1 alone is good to 2^-9), the bf16
+tests also require that at least 99.9 % of the outputs equal the rounded float64
+value exactly: with all three terms about 0.01 % differ, without w3 about 0.25 %,
+without w2 and w3 about 40 %.
 """
 from __future__ import annotations
 
@@ -43,6 +51,9 @@ def _check(got, ref, dtype):
     else:
         bound = np.full_like(ref, fp32)
     assert np.all(diff <= bound), float(np.max(diff / bound))
+    if dtype == torch.bfloat16:
+        exact = float(np.mean(got == ref))
+        assert exact >= 0.999, f"only {exact:.5f} of the bf16 outputs equal the rounded float64 value"
 
 
 @pytest.mark.parametrize("d,r,dtype,n", [(16, 1, torch.float32, 300), (64, 1, torch.bfloat16, 1000),
@@ -103,3 +114,29 @@ def test_projection_grid_stride_covers_every_token():
     W = torch.from_numpy(g.normal(size=(2, 16, 16)) / 4.0).float()
     u = vla.project_u(k.cuda(), W.cuda()).double().cpu().numpy()
     _check(u, _ref(k.double().numpy(), W.double().numpy(), torch.float32), torch.float32)
+
+
+@pytest.mark.parametrize("d", [16, 64, 128])
+@pytest.mark.parametrize("r", [1, 4])
+def test_bf16_projection_several_tiles_per_cta(d, r):
+    """bfloat16 keys with more tiles than the grid has CTAs (the grid is 8 CTAs of 128 tokens
+    per SM): every CTA runs its main loop (key rows loaded two tiles ahead) over at least two
+    tiles, and the last tile is ragged.  The outputs are compared on a sample of tokens: the
+    first and last tiles, the second and third tile of the first CTAs, and random ones."""
+    import sherman_morrison_inverse_gb300 as vla
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    grid = 8 * sms
+    n = 2 * grid * 128 + 2 * 128 + 37
+    g = np.random.default_rng([d, r, 7])
+    k = torch.from_numpy(g.normal(size=(n, d)).astype(np.float32)).to(torch.bfloat16)
+    W = torch.from_numpy(g.normal(size=(r, d, d)) / np.sqrt(d)).float()
+    u = vla.project_u(k.cuda(), W.cuda())
+    torch.cuda.synchronize()
+    idx = np.unique(np.concatenate([
+        np.arange(0, 512), np.arange(n - 512, n),
+        np.arange(grid * 128, grid * 128 + 3 * 128),          # CTAs 0..2, second tile
+        np.arange(2 * grid * 128, 2 * grid * 128 + 3 * 128),  # CTAs 0..2, third tile
+        g.integers(0, n, size=16384)]))
+    got = u[torch.from_numpy(idx).cuda()].double().cpu().numpy()
+    ref = _ref(k[torch.from_numpy(idx)].double().numpy(), W.double().numpy(), torch.bfloat16)
+    _check(got, ref, torch.bfloat16)

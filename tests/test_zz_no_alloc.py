@@ -5,7 +5,8 @@ server whose allocator owns the GPU's memory, and callers that keep no handle
 between calls.  vla_scan_fwd_noalloc serves them with the same scan as
 vla_scan_fwd; its scratch (one status record per (batch, head) pair) is a
 static array inside the library.  These tests call it through the C ABI and
-check, on two calls in a row, that it gives the existing entry point's results,
+check, on two calls in a row, that it gives the existing entry point's results
+bit for bit,
 that each call starts its status records from zero, and that sizes beyond the
 static scratch are refused.  This file is collected last so that a failure here
 stops a run only after every other test has run; it passes on its own as well.
@@ -18,14 +19,10 @@ import numpy as np
 import pytest
 import torch
 
-import oracle
 import workloads
 from _util import ensure_built
 
 pytestmark = pytest.mark.gpu
-
-TOL = {"f32": 1e-4, "bf16": 2e-2}
-
 
 @pytest.fixture(scope="module")
 def vla():
@@ -71,9 +68,11 @@ def test_two_calls_match_the_handle_entry_point(vla, io, r):
         assert _noalloc_call(vla, *g, *new_state, o_new, t0=a, pair_status=recs, **kw) == 0, \
             vla.load_library().vla_last_error(None)
         torch.cuda.synchronize()
-        e = oracle.errors(o_new.reshape(N, b - a, 64).cpu(), *(t.reshape(N, *t.shape[2:]).cpu() for t in new_state),
-                          o_ref.reshape(N, b - a, 64).cpu(), *(t.reshape(N, *t.shape[2:]).cpu() for t in ref_state))
-        assert max(e.values()) <= TOL[io], e
+        # both entry points run the same sequential kernel on the same inputs (they differ only
+        # in where the status records go), so the results agree bit for bit
+        assert torch.equal(o_new, o_ref), "o differs from vla_scan_fwd"
+        for got, want, name in zip(new_state, ref_state, "ASn"):
+            assert torch.equal(got, want), f"{name} differs from vla_scan_fwd"
         st = h.status()
         assert st["flags"] == 0 and all(rec.flags == 0 for rec in recs)
         assert sum(rec.renorm_count for rec in recs) == st["renorm_count"]
