@@ -38,9 +38,9 @@ import workloads  # noqa: E402
 
 METRIC = "VLA scan tokens*heads/s (d=64, T=16384)"
 UNIT = "tokens*heads/s"
-SM_COUNT_NOMINAL = 152
 FP32_LANES_PER_SM = 128
 SM_MAX_MHZ_NOMINAL = 2070.0
+CSRC = os.path.join(ROOT, "sherman_morrison_inverse_gb300", "csrc")
 
 
 def flops_per_token_head(d: int, dv: int, r: int, mode: str = "sequential") -> int:
@@ -60,39 +60,106 @@ def streamed_bytes_per_token_head(w) -> int:
     return (2 * w.d + w.r * w.d + 2 * w.dv) * es
 
 
-# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
-# timed kernel, from the ncu captures summarised under profiles/ (scaled from the
-# captured T to the full launch; traffic grows with T).  None when the kernel has
-# changed since its capture.
-TRAFFIC = {
-    ("b16h16_t8192_d64_bf16_r4", "chunked"):
-        (274.16e6 * 8, "bytes per launch: profiles/chunk_scan_kernel_r4_b16h16_d64_bf16.md, 274.2 MB at "
-                       "T = 1024 scaled by 8 to T = 8192"),
-    ("b4h8_t4096_d64_f32", "sequential"):
-        (154.31e6, "bytes per launch: profiles/seq_block_kernel_b4h8_d64_f32.md (the full T = 4096)"),
-    ("b2h8_t65536_d128_f32", "sequential"):
-        (156.39e6 * 16, "bytes per launch: profiles/seq_block_kernel_cluster_b2h8_d128_f32.md, 156.4 MB at "
-                        "T = 4096 scaled by 16 to T = 65536"),
-    ("b8h16_t16384_d64_bf16_recall", "sequential"):
-        (325.31e6 * 4, "bytes per launch: profiles/seq_block_kernel_b8h16_d64_bf16.md, 325.3 MB at "
-                       "T = 4096 scaled by 4 to T = 16384"),
-    ("b8h16_t16384_d64_bf16_recall", "delta"):
-        (325.57e6 * 4, "bytes per launch: profiles/seq_block_kernel_delta_b8h16_d64_bf16.md, 325.6 MB at "
-                       "T = 4096 scaled by 4 to T = 16384"),
-    ("b8h16_t16384_d64_bf16_recall", "chunked"):
-        (156.69e6 * 8, "bytes per launch: profiles/chunk_scan_kernel_b8h16_d64_bf16.md, 156.7 MB at "
-                       "T = 2048 scaled by 8 to T = 16384"),
+def chunk_tensor_flops_per_token_head(r: int) -> float:
+    """Tensor-core flops the chunked kernel executes per step of a pair (d = d_v = 64, 64
+    directions a chunk, C = 64 / r steps): the 128 x 64 x 64 products G1 (2 passes), G2 (1),
+    G3 (3), G4 (3), G5 (128 x 128 x 64) and G6 (2 x 128 x 64 x C), each pass counted."""
+    C = 64 // r
+    base = 2.0 * 128 * 64 * 64
+    per_chunk = (2 + 1 + 3 + 3) * base + 2.0 * 128 * 128 * 64 + 2 * (2.0 * 128 * 64 * C)
+    return per_chunk / C
+
+
+# Source files of each timed kernel; a traffic record holds the hash of these files at the
+# time of its ncu capture and is reported only while the hash still matches.
+KERNEL_SOURCES = {
+    "sequential": ["vla_seqk.cuh", "vla_internal.cuh", "vla_seqk_d16.cu", "vla_seqk_d64.cu", "vla_seqk_d128.cu"],
+    "delta": ["vla_seqk.cuh", "vla_internal.cuh", "vla_seqk_delta_d16.cu", "vla_seqk_delta_d64.cu",
+              "vla_seqk_delta_d128.cu", "vla_delta.cu"],
+    "chunked": ["vla_chunk.cuh", "vla_tc.cuh", "vla_internal.cuh", "vla_chunked.cu"],
 }
+
+
+def kernel_source_hash(mode: str) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[mode]:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the timed kernel
+# from ncu captures: (bytes per full-length launch, captured T, kernel source hash).  Captures
+# at a truncated T are scaled by the units processed (traffic grows with T).
+TRAFFIC = {
+    ("b4h8_t4096_d64_f32", "sequential"): (154.31e6, 4096, "2d1fb8f16cca4b57"),
+    ("b2h8_t65536_d128_f32", "sequential"): (156.39e6 * 16, 4096, "2d1fb8f16cca4b57"),
+    ("b8h16_t16384_d64_bf16_recall", "sequential"): (325.31e6 * 4, 4096, "2d1fb8f16cca4b57"),
+    ("b8h16_t16384_d64_bf16_recall", "delta"): (325.57e6 * 4, 4096, "4c6f6c798db6d4c6"),
+    ("b8h16_t16384_d64_bf16_recall", "chunked"): (156.69e6 * 8, 2048, "3c99f484200b99c1"),
+    ("b16h16_t8192_d64_bf16_r4", "chunked"): (274.16e6 * 8, 1024, "3c99f484200b99c1"),
+}
+
+
+def traffic_record(workload: str, mode: str, T: int, T_full: int):
+    """(bytes per launch or None, how it was obtained)."""
+    rec = TRAFFIC.get((workload, mode))
+    if rec is None:
+        return None, "no ncu capture of this kernel on this workload"
+    if T != T_full:
+        return None, "not the full-length workload"
+    nbytes, t_cap, src = rec
+    if src != kernel_source_hash(mode):
+        return None, "the kernel source changed since its last ncu capture (source hash %s, now %s)" % (
+            src, kernel_source_hash(mode))
+    how = "ncu dram__bytes_read.sum + dram__bytes_write.sum"
+    if t_cap != T_full:
+        how += f", captured at T = {t_cap} and scaled by {T_full // t_cap} to T = {T_full}"
+    return nbytes, how
+
 
 # arithmetic type of each mode's path
 MODE_DTYPE = {"sequential": "f32", "chunked": "tf32", "delta": "f32"}
 
 
-def fp32_peak_tflops(peaks: dict) -> tuple[float, str]:
-    """FP32 CUDA-core peak: SMs x 128 FMA lanes x 2 flops x max SM clock."""
+def sm_count(dev) -> int:
+    return int(torch.cuda.get_device_properties(dev).multi_processor_count)
+
+
+def fp32_peak_derived(peaks: dict, sms: int) -> tuple[float, str]:
+    """FP32 CUDA-core peak from the unit count: SMs x 128 FMA lanes x 2 flops x max SM clock."""
     mhz = float(peaks.get("sm_max_mhz", SM_MAX_MHZ_NOMINAL))
-    return SM_COUNT_NOMINAL * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12, (
-        f"{SM_COUNT_NOMINAL} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 flop x {mhz:.0f} MHz")
+    return sms * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12, (
+        f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 flop x {mhz:.0f} MHz")
+
+
+def measure_fp32_peak(h, dev, stream, target_ms: float = 10.0, launches: int = 3) -> dict:
+    """The FP32 CUDA-core throughput of this GPU, measured: the library's packed-FMA probe
+    (every SM busy) timed with CUDA events on the launching stream, clocks sampled beside it."""
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    iters = 1 << 12
+    for _ in range(8):   # calibrate to about target_ms a launch
+        e0.record(stream)
+        h.ffma_probe(iters, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1)
+        if ms >= 0.5 * target_ms:
+            break
+        iters = min(1 << 30, int(iters * max(2.0, target_ms / max(ms, 1e-3))))
+    clocks = ClockSampler(dev.index)
+    time.sleep(0.2)
+    best = 0.0
+    for _ in range(launches):
+        e0.record(stream)
+        flops = h.ffma_probe(iters, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        best = max(best, flops / (e0.elapsed_time(e1) / 1e3) / 1e12)
+    clk = clocks.stop()
+    st = h.status()
+    return {"tflops": best, "iters": iters, "launches": launches, "clocks": clk, "status_flags": st["flags"]}
 
 
 def load_peaks() -> dict:
@@ -181,25 +248,50 @@ def job_value(units_per_rank: int, world: int, ms_max: float) -> float:
     return units_per_rank * world / (ms_max / 1e3)
 
 
-class OracleLeg:
-    """The float64 oracle, as it stands, timed on the host cores on a bounded
-    sample of the workload: every pair, the first `steps` steps."""
+_ORACLE_STATE = {}   # per worker process: the inputs of its pairs
 
-    def __init__(self, w, T_max: int = 8192):
-        import oracle
-        self.oracle = oracle
+
+def _oracle_prepare(job):
+    """Worker: generate the inputs of this worker's pairs (the seeded generators are
+    subset-stable, so each pair's inputs are the same as in the full workload)."""
+    w, T_max, pairs = job
+    _ORACLE_STATE["w"] = w
+    _ORACLE_STATE["x"] = workloads.make_inputs(w, pairs=list(pairs), T=T_max)
+    return len(pairs)
+
+
+def _oracle_run(steps):
+    """Worker: the oracle over its pairs and the first `steps` steps; returns its wall time."""
+    import oracle
+    x, w = _ORACLE_STATE["x"], _ORACLE_STATE["w"]
+    t0 = time.perf_counter()
+    oracle.scan(x["q"][:, :steps], x["k"][:, :steps], x["v"][:, :steps], x["u"][:, :steps],
+                x["A0"], x["S0"], x["n0"], P=w.P, eps_n=w.eps_n, tau=w.tau)
+    return time.perf_counter() - t0
+
+
+class OracleLeg:
+    """The float64 oracle, as it stands, timed on the host cores on a bounded sample of the
+    workload: every pair, the first `steps` steps.  The pairs are independent, so they are
+    shared out over one single-threaded process per host CPU (spawned, so no process is
+    forked from one that has used the GPU); the wall time of all of them together is timed."""
+
+    def __init__(self, w, T_full: int, T_max: int = 8192, procs: int | None = None):
+        import multiprocessing as mp
+        for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ.setdefault(var, "1")   # one BLAS thread per worker process
         self.w = w
         self.T_max = min(w.T, T_max)
-        self.x = workloads.make_inputs(w, T=self.T_max)
+        self.procs = max(1, min(procs or (os.cpu_count() or 1), w.pairs))
+        groups = np.array_split(np.arange(w.pairs), self.procs)
+        self.pool = mp.get_context("spawn").Pool(self.procs)
+        self.pool.map(_oracle_prepare, [(w.with_(T=T_full), self.T_max, tuple(int(p) for p in g)) for g in groups])
 
     def run(self, steps: int):
-        x, w = self.x, self.w
-        c0, t0 = time.process_time(), time.perf_counter()
-        self.oracle.scan(x["q"][:, :steps], x["k"][:, :steps], x["v"][:, :steps], x["u"][:, :steps],
-                         x["A0"], x["S0"], x["n0"], P=w.P, eps_n=w.eps_n, tau=w.tau)
+        t0 = time.perf_counter()
+        self.pool.map(_oracle_run, [steps] * self.procs)
         wall = time.perf_counter() - t0
-        cpu = time.process_time() - c0
-        return self.w.pairs * steps / wall, wall, max(1, round(cpu / wall))
+        return self.w.pairs * steps / wall, wall, self.procs
 
     def calibrate(self, budget_s: float) -> int:
         steps = 16
@@ -210,12 +302,16 @@ class OracleLeg:
             steps = min(self.T_max, steps * 4)
 
     def sample_text(self, steps: int, wall: float) -> str:
-        return f"all {self.w.pairs} pairs x first {steps} of {self.w.T} steps of {self.w.name} ({wall:.1f} s wall)"
+        return (f"all {self.w.pairs} pairs x first {steps} of {self.w.T} steps of {self.w.name}, "
+                f"pairs shared out over {self.procs} single-threaded processes ({wall:.1f} s wall)")
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
 
 
 def host_cpu_info() -> dict:
-    """The host the oracle ran on: logical CPUs, CPU model, BLAS threads (when threadpoolctl
-    is importable)."""
+    """The host the oracle ran on: logical CPUs, CPU model, BLAS threads per process."""
     info = {"host_cpus": os.cpu_count()}
     model = None
     try:
@@ -233,25 +329,47 @@ def host_cpu_info() -> dict:
     if model in arm_parts:
         model = f"{arm_parts[model]} (cpu part {model})"
     info["cpu_model"] = model or platform.processor() or platform.machine()
-    try:
-        from threadpoolctl import threadpool_info
-        info["blas_threads"] = max((p.get("num_threads", 1) for p in threadpool_info()), default=1)
-    except Exception:  # noqa: BLE001 - not installed on every host
-        info["blas_threads"] = None
+    info["blas_threads_per_process"] = int(os.environ.get("OMP_NUM_THREADS", "1"))
     return info
 
 
-def oracle_leg(w, budget_s: float = 15.0):
-    leg = OracleLeg(w)
-    steps = leg.calibrate(budget_s)
-    value, wall, cores = leg.run(steps)
+def oracle_leg(w, T_full: int, budget_s: float = 15.0):
+    leg = OracleLeg(w, T_full)
+    try:
+        steps = leg.calibrate(budget_s)
+        value, wall, cores = leg.run(steps)
+    finally:
+        leg.close()
     return value, cores, leg.sample_text(steps, wall)
+
+
+def sampled_pair_errors(h, w, T_full: int, modes, dev, pairs=(0, 1)) -> dict:
+    """Errors of each mode against the oracle on a sample of pairs over the whole sequence,
+    from the workload's initial state (part of the CPU-baseline leg: the oracle runs here)."""
+    import oracle
+    x = workloads.make_inputs(w.with_(T=T_full), pairs=list(pairs), T=w.T)
+    N = len(pairs)
+    ref = oracle.scan(x["q"], x["k"], x["v"], x["u"], x["A0"], x["S0"], x["n0"], P=w.P, eps_n=w.eps_n, tau=w.tau)
+    out = {"pairs": list(pairs), "T": w.T, "metric": "oracle.errors (state: per pair max|X - X_ref| / max|X_ref|; "
+                                                     "o: per row)"}
+    for mode in modes:
+        g = {k: x[k].reshape(1, N, *x[k].shape[1:]).to(dev).contiguous() for k in ("q", "k", "v", "u")}
+        A = x["A0"].reshape(1, N, w.d, w.d).to(dev).contiguous()
+        S = x["S0"].reshape(1, N, w.dv, w.d).to(dev).contiguous()
+        n = x["n0"].reshape(1, N, w.d).to(dev).contiguous()
+        o = h.scan_fwd(g["q"], g["k"], g["v"], g["u"], A, S, n, P=w.P, eps_n=w.eps_n, tau=w.tau, mode=mode)
+        st = h.status()
+        f = lambda t: t.reshape(N, *t.shape[2:]).double().cpu().numpy()
+        e = oracle.errors(f(o), f(A), f(S), f(n), *ref)
+        out[mode] = {k: float(v) for k, v in e.items()}
+        out[mode]["status_flags"] = st["flags"]
+    return out
 
 
 def run_reference(args, w):
     if int(os.environ.get("RANK", "0")) != 0:      # torchrun: rank 0 alone times the oracle
         return
-    leg = OracleLeg(w)
+    leg = OracleLeg(w, args.T_full)
     per_step = max(1.0, 150.0 / (args.warmup + args.steps))
     steps = leg.calibrate(per_step)
     for _ in range(args.warmup):
@@ -261,6 +379,7 @@ def run_reference(args, w):
         v, wall, cores = leg.run(steps)
         vals.append(v)
         walls.append(wall)
+    leg.close()
     value = len(vals) * w.pairs * steps / sum(walls)
     sample = leg.sample_text(steps, statistics.median(walls)) + " per step"
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
@@ -300,20 +419,26 @@ def run_project_u(args, w):
     peaks = load_peaks()
     flops = 2 * w.r * w.d * w.d * n
     nbytes = n * (w.d + w.r * w.d) * k.element_size()   # keys in, directions out (W: a few KB)
-    # the tensor-core form (tcgen05 kind::tf32, W as hi + lo) serves every shape but d = 128 with
-    # float32 keys; it is bound by HBM: a few flops per byte, far below the tensor ridge
+    # the tensor-core forms serve every shape but d = 128 with float32 keys; the projection is
+    # bound by HBM: a few flops per byte, far below the tensor ridge
     tc = not (w.d == 128 and w.io == "f32")
+    if w.io == "bf16":
+        form, dt = "tcgen05 kind::f16: bf16 keys, W as three bf16 terms (3 passes), fp32 accumulation", "bf16"
+    elif tc:
+        form, dt = "tcgen05 kind::tf32: keys and W as tf32 hi + lo (3 passes), fp32 accumulation", "tf32"
+    else:
+        form, dt = "CUDA cores, float32", "f32"
     gbs = nbytes / (ms / 1e3) / 1e9
     line = {"metric": "u projection tokens/s (normalize(W_u k_raw))", "value": n / (ms / 1e3), "unit": "tokens/s",
             "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "tf32" if tc else "f32", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": dt, "data": "synthetic",
             "config": {"workload": w.name, "tokens": n, "d": w.d, "r": w.r, "io": w.io, "op": "project_u",
                        "l2": "keys and directions 2 x %.0f MB > 129 MB L2 (no flush)" % (n * w.d * k.element_size() / 1e6)},
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
                          "frac": gbs / float(peaks["hbm_gbs"]), "traffic": None,
                          "peak_how": "%s HBM copy bandwidth" % peaks["_source"],
                          "algorithmic_bytes": nbytes, "tflops": flops / (ms / 1e3) / 1e12,
-                         "form": "tcgen05 kind::tf32, 2 passes (W hi + lo)" if tc else "CUDA cores, float32"},
+                         "form": form},
             "clocks": clk, "gpu_launches": args.steps}
     print(json.dumps(line), flush=True)
     h.close()
@@ -371,12 +496,18 @@ def main():
                     help="steps per window of the host-buffer (e2e) path; 0 = the library's choice")
     ap.add_argument("--T", type=int, default=None,
                     help="truncate the sequence (profiling a smaller case; not a bench number)")
+    ap.add_argument("--tau", type=float, default=None,
+                    help="renormalisation threshold in place of the workload's (a labelled companion run, "
+                         "e.g. 500 on the long-context workload so that renormalisation fires)")
     args = ap.parse_args()
     w = workloads.get(int(args.workload) if args.workload.isdigit() else args.workload)
     T_full = w.T
     if args.T is not None:
         w = w.with_(T=args.T)
+    if args.tau is not None:
+        w = w.with_(tau=args.tau)
 
+    args.T_full = T_full
     if args.mode == "auto":
         args.mode = "chunked" if (w.d == 64 and w.dv == 64 and w.io == "bf16" and w.r in (1, 4)) else "sequential"
     if args.impl == "reference":
@@ -464,36 +595,81 @@ def main():
     e2e_value = job_value(B * H * T * e2e_steps, world, e2e_ms)
     st_e2e = h.status()
 
-    # ---- roofline of the (only) kernel: FP32 CUDA-core arithmetic binds
+    # ---- the other kernel on the same workload: the sequential fp32 CUDA-core scan beside
+    # the chunked tensor-core one (timed the same way, after the headline legs)
+    other = "sequential" if args.mode == "chunked" else None
+    modes = {args.mode: {"ms_per_step": ms_per_step, "value": value}}
+    if other is not None:
+        okw = dict(kw, mode=other, chunk=0)
+        A2, S2, n2 = A.clone(), S.clone(), n.clone()
+        for _ in range(2):
+            h.scan_fwd(g["q"], g["k"], g["v"], g["u"], A2, S2, n2, o, t0=t0, **okw)
+            t0 += T
+        o_steps = max(3, args.steps // 4)
+        barrier(dist)
+        torch.cuda.synchronize(dev)
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(o_steps):
+            h.scan_fwd(g["q"], g["k"], g["v"], g["u"], A2, S2, n2, o, t0=t0, **okw)
+            t0 += T
+        f1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(dist)
+        o_ms = max_over_ranks(f0.elapsed_time(f1), dist, dev) / o_steps
+        modes[other] = {"ms_per_step": o_ms, "value": job_value(B * H * T, world, o_ms), "steps": o_steps,
+                        "status": h.status()}
+
+    # ---- roofline: FP32 CUDA-core arithmetic binds (both kernels quoted on this one scale);
+    # the peak is measured here, on this GPU, by the library's packed-FMA probe
     peaks = load_peaks()
-    peak_tf, peak_how = fp32_peak_tflops(peaks)
+    sms = sm_count(dev)
+    probe = measure_fp32_peak(h, dev, stream)
+    peak_tf = probe["tflops"]
+    derived_tf, derived_how = fp32_peak_derived(peaks, sms)
     F = flops_per_token_head(w.d, w.dv, w.r, args.mode)
     achieved_tf = B * H * T * F / (ms_per_step / 1e3) / 1e12
     bytes_step = B * H * T * streamed_bytes_per_token_head(w)
-    traffic = TRAFFIC.get((w.name, args.mode), (None, "no capture for this workload"))
-    if w.T != T_full:
-        traffic = (None, "not the full-length workload")
+    traffic, traffic_how = traffic_record(w.name, args.mode, T, T_full)
+    for m, rec in modes.items():
+        rec["frac"] = B * H * T * flops_per_token_head(w.d, w.dv, w.r, m) / (rec["ms_per_step"] / 1e3) / 1e12 / peak_tf
+        rec["dtype"] = MODE_DTYPE[m]
+    roofline = {"bound": "alu", "achieved": achieved_tf, "peak": peak_tf, "unit": "TFLOP/s",
+                "frac": achieved_tf / peak_tf, "traffic": traffic, "traffic_how": traffic_how,
+                "peak_how": (f"measured: the library's packed-FMA probe on all {sms} SMs, best of "
+                             f"{probe['launches']} launches of {probe['iters']} rounds, median SM clock "
+                             f"{probe['clocks'].get('sm_mhz')} MHz; derived {derived_tf:.1f} TFLOP/s = {derived_how}"),
+                "peak_derived": derived_tf, "flops_per_token_head": F,
+                "frac_short_count": (B * H * T * flops_per_token_head_short(w.d, w.dv, w.r)
+                                     / (ms_per_step / 1e3) / 1e12) / peak_tf,
+                "hbm_gbs": bytes_step / (ms_per_step / 1e3) / 1e9,
+                "hbm_frac": bytes_step / (ms_per_step / 1e3) / 1e9 / float(peaks["hbm_gbs"]),
+                "sm_count": sms, "sm_ceiling": min(1.0, B * H / sms)}
+    if args.mode == "chunked":
+        tf32_peak = float(peaks["bf16_tflops"]) / 2.0
+        tfl = B * H * T * chunk_tensor_flops_per_token_head(w.r) / (ms_per_step / 1e3) / 1e12
+        roofline["tensor"] = {
+            "bound": "tensor", "achieved": tfl, "peak": tf32_peak, "unit": "TFLOP/s", "frac": tfl / tf32_peak,
+            "flops_per_token_head": chunk_tensor_flops_per_token_head(w.r),
+            "counts": "every tcgen05 pass the kernel executes (a 3xTF32 product counts three times)",
+            "peak_how": "%s bf16 burst (%.0f TFLOP/s) x 1/2, the nominal tf32:bf16 dense ratio" % (
+                peaks["_source"], float(peaks["bf16_tflops"]))}
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": MODE_DTYPE[args.mode], "data": "synthetic",
         "config": {"workload": w.name, "B": B, "H": H, "T": T, "d": w.d, "dv": w.dv, "r": w.r,
-                   "io": w.io, "state": "f32", "mode": args.mode,
+                   "io": w.io, "state": "f32", "mode": args.mode, "P": w.P, "eps_n": w.eps_n, "tau": w.tau,
+                   "tau_override": args.tau is not None,
                    "precision": ("tcgen05 kind::tf32, 3xTF32 on the products that carry A; fp32 state"
                                  if args.mode == "chunked" else "fp32 CUDA-core arithmetic"),
                    "rule": "delta (gist.science summary §2.3)" if args.mode == "delta" else "additive",
                    "l2": f"inputs {bytes_step / 1e9:.2f} GB per step > 129 MB L2 (no flush)",
                    "parallelism": f"replicas x{world}, one CTA per (b,h) pair"},
-        "roofline": {"bound": "alu", "achieved": achieved_tf, "peak": peak_tf, "unit": "TFLOP/s",
-                     "frac": achieved_tf / peak_tf, "traffic": traffic[0], "traffic_source": traffic[1],
-                     "peak_how": peak_how + " (derived; FP32 is not in the measured-peaks file)",
-                     "flops_per_token_head": F,
-                     "frac_short_count": (B * H * T * flops_per_token_head_short(w.d, w.dv, w.r)
-                                          / (ms_per_step / 1e3) / 1e12) / peak_tf,
-                     "hbm_gbs": bytes_step / (ms_per_step / 1e3) / 1e9,
-                     "hbm_frac": bytes_step / (ms_per_step / 1e3) / 1e9 / float(peaks["hbm_gbs"]),
-                     "sm_ceiling": min(1.0, B * H / SM_COUNT_NOMINAL)},
+        "roofline": roofline,
+        "modes": modes,
+        "fp32_probe": probe,
         "clocks": clk,
         "gpu_launches": args.steps,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -510,9 +686,12 @@ def main():
         line["trace"] = {"seg": args.trace, "P": tkw["P"], "tau": w.tau, "rows": rows, "status": h.status(),
                          "note": "untimed; M = A_0^-1 + sum u u^T in float64 on the host"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, cores, sample = oracle_leg(w)
+        v, cores, sample = oracle_leg(w, T_full)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
                                 **host_cpu_info()}
+        errs = sampled_pair_errors(h, w, T_full, list(modes), dev)
+        for m in modes:
+            modes[m]["errors"] = {"pairs": errs["pairs"], "T": errs["T"], **errs[m]}
     if rank == 0:
         print(json.dumps(line), flush=True)
     h.close()

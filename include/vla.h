@@ -221,6 +221,15 @@ vla_err_t vla_project_u(vla_handle_t h, const void* k_raw, const float* W_u, voi
  * NULL handle or limit_ms outside 1..5000; CUDA if the launch fails. */
 vla_err_t vla_selftest_wait(vla_handle_t h, unsigned int limit_ms, void* stream);
 
+/* Measurement helper, not part of the scan (the pages have no counterpart): the FP32
+ * CUDA-core throughput of the handle's device, against which the scan's roofline is
+ * quoted.  Launches 4 CTAs of 256 threads per SM; each thread runs 8 independent chains
+ * of packed fp32 FMAs for `iters` rounds (rounded up to a multiple of 8).  *flops
+ * receives the launch's flop count (FMA = 2); the caller times the launch on `stream`
+ * (for instance with events) and divides.  Asynchronous on `stream`.  Errors:
+ * INVALID_ARG for a NULL argument or iters outside 8..2^30; CUDA if the launch fails. */
+vla_err_t vla_ffma_probe(vla_handle_t h, long long iters, double* flops, void* stream);
+
 /* Synchronise `stream`, copy the accumulated status into *out and reset it.
  * Errors: INVALID_ARG (NULL argument), CUDA. */
 vla_err_t vla_status(vla_handle_t h, void* stream, vla_status_t* out);

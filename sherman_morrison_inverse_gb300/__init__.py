@@ -91,6 +91,8 @@ def load_library():
         lib.vla_scan_fwd_host.restype = ci
         lib.vla_selftest_wait.argtypes = [vp, ctypes.c_uint, vp]
         lib.vla_selftest_wait.restype = ci
+        lib.vla_ffma_probe.argtypes = [vp, cll, ctypes.POINTER(ctypes.c_double), vp]
+        lib.vla_ffma_probe.restype = ci
         lib.vla_host_path_info.argtypes = [vp, ctypes.POINTER(ci), ctypes.POINTER(cll)]
         lib.vla_host_path_info.restype = ci
         lib.vla_project_u.argtypes = [vp, vp, vp, vp, cll, ci, ci, ci, vp]
@@ -212,6 +214,14 @@ class Handle:
             io, mode_i, int(chunk), _stream_ptr(stream, self.device))
         _check(self.lib, self._h, code)
         return o
+
+    def ffma_probe(self, iters: int, stream=None) -> float:
+        """Launch the FP32 throughput probe (packed FMAs on every SM) on `stream`; returns
+        the launch's flop count.  Time the launch on the same stream to get FLOP/s."""
+        flops = ctypes.c_double(0.0)
+        _check(self.lib, self._h, self.lib.vla_ffma_probe(self._h, int(iters), ctypes.byref(flops),
+                                                          _stream_ptr(stream, self.device)))
+        return float(flops.value)
 
     def selftest_wait(self, limit_ms: int = 200, stream=None):
         """Launch a wait that nothing completes; it gives up after limit_ms and sets the

@@ -486,6 +486,27 @@ vla_err_t vla_selftest_wait(vla_handle_t h, unsigned int limit_ms, void* stream)
   return VLA_OK;
 }
 
+}  // extern "C"
+
+namespace vla {
+// The FP32 throughput probe (vla_peak.cu): 4 CTAs of 256 threads per SM, `iters` (rounded
+// up to a multiple of 8) packed FMAs on 8 chains per thread; *flops = the launch's flops.
+cudaError_t launch_ffma_probe(long long iters, int sm_count, DevStatus* status, cudaStream_t s, double* flops);
+}  // namespace vla
+
+extern "C" {
+
+vla_err_t vla_ffma_probe(vla_handle_t h, long long iters, double* flops, void* stream) {
+  if (!h || !flops) return fail(h, VLA_ERR_INVALID_ARG, "vla_ffma_probe: NULL argument");
+  h->last_error.clear();
+  if (iters < 8 || iters > (1ll << 30)) return fail(h, VLA_ERR_INVALID_ARG, "vla_ffma_probe: iters must be 8..2^30");
+  cudaError_t e = on_device(h->device, [&]() {
+    return vla::launch_ffma_probe(iters, h->sm_count, h->status, static_cast<cudaStream_t>(stream), flops);
+  });
+  if (e != cudaSuccess) return fail(h, VLA_ERR_CUDA, cuda_msg("vla_ffma_probe: launch", e));
+  return VLA_OK;
+}
+
 vla_err_t vla_status(vla_handle_t h, void* stream, vla_status_t* out) {
   if (!h || !out) return fail(h, VLA_ERR_INVALID_ARG, "vla_status: NULL argument");
   vla::DevStatus st{};

@@ -36,6 +36,7 @@ def test_streamed_bytes_per_token_head(idx, nbytes):
 def test_reference_arm_prints_one_contract_line():
     class Args:
         gpus, steps, warmup = 1, 1, 0
+        T_full = workloads.get(0).T
 
     buf = io.StringIO()
     with redirect_stdout(buf):
@@ -54,15 +55,50 @@ def test_reference_arm_prints_one_contract_line():
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
 
 
-def test_traffic_table_names_its_capture():
-    for (name, mode), (traffic, source) in bench.TRAFFIC.items():
-        assert workloads.get(name).name == name and mode in bench.MODE_DTYPE
-        assert "profiles/" in source
-        if traffic is not None:
-            assert traffic > 0
-            # a capture's DRAM traffic is at least the bytes the launch must stream
-            w = workloads.get(name)
-            assert traffic >= 0.9 * w.pairs * w.T * bench.streamed_bytes_per_token_head(w)
+def test_traffic_records_are_tied_to_their_kernel_source():
+    for (name, mode), (traffic, t_cap, src) in bench.TRAFFIC.items():
+        w = workloads.get(name)
+        assert w.name == name and mode in bench.MODE_DTYPE and mode in bench.KERNEL_SOURCES
+        assert len(src) == 16 and int(src, 16) >= 0 and w.T % t_cap == 0
+        # a capture's DRAM traffic is at least the bytes the launch must stream
+        assert traffic >= 0.9 * w.pairs * w.T * bench.streamed_bytes_per_token_head(w)
+        got, how = bench.traffic_record(name, mode, w.T, w.T)
+        if src == bench.kernel_source_hash(mode):
+            assert got == traffic and "ncu" in how
+        else:   # the kernel changed since the capture: no traffic figure
+            assert got is None and "changed" in how
+    # a truncated run reports none
+    assert bench.traffic_record("b4h8_t4096_d64_f32", "sequential", 1024, 4096)[0] is None
+
+
+def test_kernel_source_hash_follows_the_files(tmp_path, monkeypatch):
+    h = bench.kernel_source_hash("chunked")
+    assert h == bench.kernel_source_hash("chunked") and len(h) == 16
+    for f in bench.KERNEL_SOURCES["chunked"]:
+        (tmp_path / f).write_bytes(open(os.path.join(bench.CSRC, f), "rb").read())
+    monkeypatch.setattr(bench, "CSRC", str(tmp_path))
+    assert bench.kernel_source_hash("chunked") == h
+    (tmp_path / "vla_chunk.cuh").write_bytes(b"// changed\n" + (tmp_path / "vla_chunk.cuh").read_bytes())
+    assert bench.kernel_source_hash("chunked") != h
+
+
+def test_tensor_flops_of_the_chunked_kernel():
+    base = 2 * 128 * 64 * 64   # one pass of a 128 x 64 x 64 product
+    # r = 1, 64 steps a chunk: G1 2 + G2 1 + G3 3 + G4 3 passes, G5 128 x 128 x 64, G6 2 x 128 x 64 x 64
+    assert bench.chunk_tensor_flops_per_token_head(1) == 13 * base / 64
+    # r = 4, 16 steps a chunk: G6 has K = 16
+    assert bench.chunk_tensor_flops_per_token_head(4) == (9 * base + 2 * base + 2 * base / 4) / 16
+
+
+def test_oracle_leg_shares_the_pairs_over_processes():
+    w = workloads.get(0).with_(B=1, H=4, T=64)
+    leg = bench.OracleLeg(w, T_full=64, procs=2)
+    try:
+        value, wall, procs = leg.run(16)
+    finally:
+        leg.close()
+    assert procs == 2 and value > 0 and wall > 0
+    assert "2 single-threaded processes" in leg.sample_text(16, wall)
 
 
 def test_no_function_shadows_a_module_function_it_calls():
