@@ -57,8 +57,8 @@ namespace chk {
 constexpr int D = 64;
 constexpr int NT = 256;
 constexpr int TILE = 64 * 64;         // floats of a TK(64, 64) operand tile
-constexpr int GLD = 68;               // leading dimension of the fp32 G / L staging (16-byte rows)
 constexpr int PLD = 68;               // leading dimension of the prologue's phi(k) / phi(q) scratch
+constexpr int GLD = 68;               // leading dimension of the fp32 G / L staging (16-byte rows)
 constexpr float kGuardEps = 1e-6f;
 constexpr float kReadoutEps = 1e-6f;
 constexpr float kInvSqrtD = 0.125f;
@@ -72,10 +72,10 @@ __device__ __forceinline__ float tf32_hi(float x) { return __uint_as_float(__flo
 // the chunked path serves bf16 I/O, whose rounding is far coarser)
 __device__ __forceinline__ float phi_fast(float x) { return x > 0.f ? x + 1.f : __expf(x); }
 
-// packed 8 x 8 blocks (leading dimension 9) of a 64 x 64 lower-triangular matrix: block (bi, bj)
+// packed 8 x 8 blocks (row-major, 64 floats) of a 64 x 64 lower-triangular matrix: block (bi, bj)
 // with bi >= bj, and the strictly lower blocks (bi > bj) of a second one
-__host__ __device__ constexpr int pb8(int bi, int bj) { return (bi * (bi + 1) / 2 + bj) * 72; }
-__host__ __device__ constexpr int pbB(int bi, int bj) { return (bi * (bi - 1) / 2 + bj) * 72; }
+__host__ __device__ constexpr int pb8(int bi, int bj) { return (bi * (bi + 1) / 2 + bj) * 64; }
+__host__ __device__ constexpr int pbB(int bi, int bj) { return (bi * (bi - 1) / 2 + bj) * 64; }
 
 // named barriers (ids 1..5; 0 is __syncthreads): `n` threads take part, a multiple of 32
 __device__ __forceinline__ void bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
@@ -120,7 +120,7 @@ struct Cfg {
   static_assert(3 * T6T <= 3 * TILE, "T6 fits in R and L");
   static_assert(64 * GLD <= 2 * TILE, "staging fits in P");
   static_assert(2 * C * PLD <= 3 * TILE, "prologue scratch fits in R and L");
-  static_assert(pb8(7, 7) + 72 <= TILE && pbB(7, 6) + 72 <= TILE, "packed blocks fit in one tile");
+  static_assert(pb8(7, 7) + 64 <= TILE && pbB(7, 6) + 64 <= TILE, "packed blocks fit in one tile");
   static_assert(bytes <= 227 * 1024, "shared memory");
 };
 
@@ -148,6 +148,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
   uint64_t* mma_bar = in_bar + 1;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(in_bar + 2);
   volatile int* flag = reinterpret_cast<volatile int*>(in_bar + 3);
+  volatile int* issued = reinterpret_cast<volatile int*>(in_bar + 4);   // the last tile whose copy was issued
   const uint32_t sbase = smem_u32(sf);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -182,7 +183,8 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
   const uint32_t tmem = *tslot;
 
   const int ntiles = (int)((T + TS - 1) / TS);
-  auto issue = [&](int tile) {  // thread 0 only
+  auto issue = [&](int tile) {  // one thread
+    *issued = tile;
     const long long t_start = (long long)tile * TS;
     const int nst = (int)min((long long)TS, T - t_start);
     const uint32_t qb = (uint32_t)nst * D * sizeof(TIO), ub = (uint32_t)nst * R * D * sizeof(TIO);
@@ -303,6 +305,16 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
   };
 
   long long pos = 0;
+  // steps left until the next nudge (the global step t0 + pos + to_nudge is a multiple of P),
+  // carried from chunk to chunk instead of a 64-bit remainder per chunk
+  long long to_nudge = (a.P > 0) ? a.P - (a.t0 % a.P) : 0;
+  auto advance = [&](int c) {
+    pos += c;
+    if (a.P > 0) {
+      to_nudge -= c;
+      if (to_nudge == 0) to_nudge = a.P;
+    }
+  };
   int loaded = -1;
   while (pos < T && !failed) {
     // ---------------- schedule: chunk [pos, pos + c) inside one input tile, ending at a nudge
@@ -311,7 +323,6 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     int c = (int)min((long long)(TS - ts), T - pos);
     bool nudge = false;
     if (a.P > 0) {
-      const long long to_nudge = a.P - ((a.t0 + pos) % a.P);
       if (to_nudge <= c) { c = (int)to_nudge; nudge = true; }
     }
     if (tile != loaded) {
@@ -388,22 +399,30 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
       // n_t = n_{t-1} + phi(k_t): column i, four segments of C/4 steps (one per thread)
       constexpr int SEG = C / 4;
       const int ci = tid & 63, sg4 = tid >> 6;
+      float kseg[SEG], qseg[SEG];   // the segment's phi(k) and phi(q), kept in registers
+#pragma unroll
+      for (int j = 0; j < SEG; ++j) kseg[j] = pk[(SEG * sg4 + j) * PLD + ci];
       {
         float tot = 0.f;
 #pragma unroll
-        for (int j = 0; j < SEG; ++j) tot += pk[(SEG * sg4 + j) * PLD + ci];
+        for (int j = 0; j < SEG; ++j) tot += kseg[j];
         misc[Cf::M_NSEG + sg4 * 64 + ci] = tot;
       }
       if (tid < D) misc[Cf::M_SL + tid] = sf[Cf::F_P + tk_off(64 + c - 1, tid, 64)];   // s of the chunk's last step
+#pragma unroll
+      for (int j = 0; j < SEG; ++j) qseg[j] = pq[(SEG * sg4 + j) * PLD + ci];
       __syncthreads();
       float nrun = misc[Cf::M_N + ci];
-      for (int s2 = 0; s2 < sg4; ++s2) nrun += misc[Cf::M_NSEG + s2 * 64 + ci];
+#pragma unroll
+      for (int s2 = 0; s2 < 3; ++s2)
+        if (s2 < sg4) nrun += misc[Cf::M_NSEG + s2 * 64 + ci];
 #pragma unroll
       for (int j = 0; j < SEG; ++j) {
-        const int t = SEG * sg4 + j;
-        nrun += pk[t * PLD + ci];
-        pk[t * PLD + ci] = nrun * pq[t * PLD + ci];
+        nrun += kseg[j];
+        kseg[j] = nrun * qseg[j];
       }
+#pragma unroll
+      for (int j = 0; j < SEG; ++j) pk[(SEG * sg4 + j) * PLD + ci] = kseg[j];
       __syncthreads();
       if (sg4 == 3) misc[Cf::M_N + ci] = nrun;   // n after the chunk (zero rows past c add nothing)
       {  // 1/den_t and |v_t|: NT / C threads per step (every lane takes part in the shuffles)
@@ -411,12 +430,22 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
         constexpr int EPT = 64 / TPS;
         const int t = tid / TPS, part = tid - t * TPS;
         float dn = 0.f, vv = 0.f;
+        static_assert(EPT % 4 == 0, "den reduction layout");
         if (t < c) {
 #pragma unroll
-          for (int j = 0; j < EPT; ++j) {
-            dn += pk[t * PLD + part * EPT + j];
-            const float x = to_f32(vb[t * 64 + part * EPT + j]);
-            vv = fmaf(x, x, vv);
+          for (int j = 0; j < EPT; j += 4) {
+            const float4 p4 = *reinterpret_cast<const float4*>(pk + t * PLD + part * EPT + j);
+            const uint2 w2 = *reinterpret_cast<const uint2*>(vb + t * 64 + part * EPT + j);
+            const float2 v01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w2.x));
+            const float2 v23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w2.y));
+            dn += p4.x;
+            dn += p4.y;
+            dn += p4.z;
+            dn += p4.w;
+            vv = fmaf(v01.x, v01.x, vv);
+            vv = fmaf(v01.y, v01.y, vv);
+            vv = fmaf(v23.x, v23.x, vv);
+            vv = fmaf(v23.y, v23.y, vv);
           }
         }
 #pragma unroll
@@ -506,7 +535,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     // L is written; UB: the helpers' trailing update for column k is done), used in
     // alternation so that a barrier is never reused before its previous round completed.
     // Warp 4 shares warp 0's SM sub-partition and stays idle.
-    float* XB = sf + Cf::F_Q;   // X = L^{-1}: 36 lower 8 x 8 blocks, leading dimension 9
+    float* XB = sf + Cf::F_Q;   // X = L^{-1}: 36 lower 8 x 8 blocks
     float* BB = sf + Cf::F_L;   // B: 28 strictly lower 8 x 8 blocks
     if (warp == 0) {
       float* dsc = misc + Cf::M_VEC;   // warp 0's broadcast scratch (64 floats)
@@ -518,28 +547,25 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
         *reinterpret_cast<float4*>(pp) = make_float4(v[0], v[1], v[2], v[3]);
         *reinterpret_cast<float4*>(pp + 4) = make_float4(v[4], v[5], v[6], v[7]);
       };
+      // lane l owns rows l and 32 + l; ga / gb hold their entries of the current block column
+      // (Schur-updated), carried in registers from one step to the next
+      float ga[8], gb[8];
+      ld8(Gs + lane * GLD, ga);
+      ld8(Gs + (32 + lane) * GLD, gb);
 #pragma unroll 1
       for (int k = 0; k < 8; ++k) {
-        const int r0 = 8 * k + lane, r1 = r0 + 32;   // this lane's rows of block column k
-        const bool va = r0 < 64, vb = r1 < 64;
-        float ga[8], gb[8];
-        if (va) ld8(Gs + r0 * GLD + 8 * k, ga);
-        else {
+        // the diagonal block's rows 8k..8k+7 are lanes 8 (k % 4) .. 8 (k % 4) + 7 of row set k / 4
+        const bool owner = (lane >> 3) == (k & 3);
+        if (owner) {
+          float t[8];
 #pragma unroll
-          for (int c = 0; c < 8; ++c) ga[c] = 0.f;
+          for (int c = 0; c < 8; ++c) t[c] = (k >= 4) ? gb[c] : ga[c];
+          st8(dsc + 8 * (lane & 7), t);
         }
-        if (vb) ld8(Gs + r1 * GLD + 8 * k, gb);
-        else {
-#pragma unroll
-          for (int c = 0; c < 8; ++c) gb[c] = 0.f;
-        }
-        if (lane < 8) st8(dsc + 8 * lane, ga);   // the diagonal block, to every lane
         __syncwarp();
         float a8[8][8], d8[8], id8[8];
 #pragma unroll
-        for (int r = 0; r < 8; ++r)
-#pragma unroll
-          for (int c = 0; c <= r; ++c) a8[r][c] = dsc[8 * r + c];
+        for (int r = 0; r < 8; ++r) ld8(dsc + 8 * r, a8[r]);   // (entries above the diagonal unused)
         __syncwarp();
         // a8 -> L_kk (strict lower), d8 = D_k, id8 = 1 / D_k
 #pragma unroll
@@ -556,7 +582,8 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
           for (int i = j + 1; i < 8; ++i) a8[i][j] *= id8[j];
         }
         // rows -> L: (L D)_r = G'_r L_kk^{-T} by forward substitution, then times D^{-1}.  For the
-        // diagonal rows (lanes 0..7) the entries left of the diagonal are L_kk's.
+        // diagonal rows the entries left of the diagonal are L_kk's.  Rows above the block are
+        // not stored.
         auto panel = [&](float (&g)[8]) {
 #pragma unroll
           for (int c = 1; c < 8; ++c)
@@ -567,48 +594,66 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
         };
         panel(ga);
         panel(gb);
-        if (va) st8(Gs + r0 * GLD + 8 * k, ga);
-        if (vb) st8(Gs + r1 * GLD + 8 * k, gb);
+        if (lane >= 8 * k) st8(Gs + lane * GLD + 8 * k, ga);
+        if (32 + lane >= 8 * k) st8(Gs + (32 + lane) * GLD + 8 * k, gb);
         if (lane == 0) {
           st8(misc + Cf::M_D + 8 * k, d8);
           st8(misc + Cf::M_ID + 8 * k, id8);
         }
         bar_arrive(1 + (k & 1), 224);   // LB: block column k of L and D_k are written
         if (k < 7) {
-          // the helpers' update of block column k + 1 from column k - 1 is done
-          if (k >= 1) bar_sync(3 + ((k - 1) & 1), 224);
-          // column k's contribution to block column k + 1: rows of block k + 1 are lanes 8..15
-          if (lane >= 8 && lane < 16) {
-            float t[8];
+          // column k's contribution to block column k + 1, -L_{.k} D_k L_{k+1,k}^T: (L D)_{k+1,k}
+          // (lanes 8 ((k+1) % 4) .. + 7 of row set (k+1) / 4), transposed, to every lane
+          if ((lane >> 3) == ((k + 1) & 3)) {
 #pragma unroll
-            for (int c = 0; c < 8; ++c) t[c] = ga[c] * d8[c];   // (L D)_{k+1,k}
-            st8(dsc + 8 * (lane - 8), t);
+            for (int c = 0; c < 8; ++c) dsc[8 * c + (lane & 7)] = ((k + 1 >= 4) ? gb[c] : ga[c]) * d8[c];
           }
           __syncwarp();
-          float ldm[8][8];
+          float2 ldm2[8][4];   // ldm2[c][h] = ((L D)[2h][c], (L D)[2h + 1][c])
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
+          for (int c = 0; c < 8; ++c) {
+            float t[8];
+            ld8(dsc + 8 * c, t);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) ldm[i][c] = dsc[8 * i + c];
-          auto upd = [&](int r, const float (&l)[8]) {
-            float cur[8];
-            ld8(Gs + r * GLD + 8 * (k + 1), cur);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              float acc = 0.f;
-#pragma unroll
-              for (int c = 0; c < 8; ++c) acc = fmaf(l[c], ldm[i][c], acc);
-              cur[i] -= acc;
-            }
-            st8(Gs + r * GLD + 8 * (k + 1), cur);
-          };
-          if (lane >= 8 && va) upd(r0, ga);
-          if (vb) upd(r1, gb);
+            for (int h = 0; h < 4; ++h) ldm2[c][h] = make_float2(t[2 * h], t[2 * h + 1]);
+          }
           __syncwarp();
+          // the helpers' contributions of columns <= k - 1 to column k + 1 are in the staging
+          if (k >= 1) bar_sync(3 + ((k - 1) & 1), 224);
+          auto next = [&](int r, float (&g)[8]) {   // g: this row's L_{r,k}; becomes G'_{r,k+1}
+            float cur[8];
+            if (r >= 8 * (k + 1)) {
+              ld8(Gs + r * GLD + 8 * (k + 1), cur);
+            } else {
+#pragma unroll
+              for (int c = 0; c < 8; ++c) cur[c] = 0.f;
+            }
+            float2 acc[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) acc[h] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const float2 lc = make_float2(g[c], g[c]);
+#pragma unroll
+              for (int h = 0; h < 4; ++h) acc[h] = __ffma2_rn(lc, ldm2[c][h], acc[h]);
+            }
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              g[2 * h] = cur[2 * h] - acc[h].x;
+              g[2 * h + 1] = cur[2 * h + 1] - acc[h].y;
+            }
+          };
+          next(lane, ga);
+          next(32 + lane, gb);
         }
       }
-    } else if (warp != 4) {
+        } else if (warp != 4) {
       const int ot = ((warp < 4) ? warp - 1 : warp - 2) * 32 + lane;   // 0..191
+      auto ld4 = [](const float* pp) { return *reinterpret_cast<const float4*>(pp); };
+      auto ldrow8 = [&](const float* pp, float (&v)[8]) {
+        const float4 x0 = ld4(pp), x1 = ld4(pp + 4);
+        v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w; v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
+      };
 #pragma unroll 1
       for (int m = 0; m < 8; ++m) {
         bar_sync(1 + (m & 1), 224);   // LB: block column m of L is written
@@ -617,21 +662,24 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
           const int j = ot >> 3, c = ot & 7;
           float x[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) x[i] = (j == m) ? ((i == c) ? 1.f : 0.f) : BB[pbB(m, j) + 9 * i + c];
+          for (int i = 0; i < 8; ++i) x[i] = (j == m) ? ((i == c) ? 1.f : 0.f) : BB[pbB(m, j) + 8 * i + c];
           const float* lmm = Gs + 8 * m * GLD + 8 * m;
 #pragma unroll
-          for (int i = 1; i < 8; ++i)
+          for (int i = 1; i < 8; ++i) {
+            float li[8];
+            ldrow8(lmm + i * GLD, li);
 #pragma unroll
-            for (int pp = 0; pp < i; ++pp) x[i] = fmaf(-lmm[i * GLD + pp], x[pp], x[i]);
+            for (int pp = 0; pp < i; ++pp) x[i] = fmaf(-li[pp], x[pp], x[i]);
+          }
 #pragma unroll
-          for (int i = 0; i < 8; ++i) XB[pb8(m, j) + 9 * i + c] = x[i];
+          for (int i = 0; i < 8; ++i) XB[pb8(m, j) + 8 * i + c] = x[i];
         }
         bar_sync(5, 192);
         if (m < 7) {
           // 2 x 4 tiles of: B_ij -= L_im X_mj (i > m, j <= m; B_im starts at 0), and of the
-          // trailing update G'_ic -= L_im D_m L_cm^T (c >= m + 2, i >= c)
+          // trailing update G'_ic -= L_im D_m L_cm^T (c >= m + 2, i >= c); rows in registers,
+          // 16-byte loads
           const int nb = (7 - m) * (m + 1), nt = (6 - m) * (7 - m) / 2;
-          const float* dm = misc + Cf::M_D + 8 * m;
           for (int q = ot; q < 8 * (nb + nt); q += 192) {
             const int blk = q >> 3, rr = (q >> 1) & 3, cc = q & 1;
             float acc[2][4];
@@ -641,48 +689,59 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
               for (int b4 = 0; b4 < 4; ++b4) acc[a2][b4] = 0.f;
             if (blk < nb) {
               const int i = m + 1 + blk / (m + 1), j = blk % (m + 1);
-              const float* lr = Gs + (8 * i + 2 * rr) * GLD + 8 * m;
+              float l0[8], l1[8];
+              ldrow8(Gs + (8 * i + 2 * rr) * GLD + 8 * m, l0);
+              ldrow8(Gs + (8 * i + 2 * rr + 1) * GLD + 8 * m, l1);
               const float* xc = XB + pb8(m, j) + 4 * cc;
 #pragma unroll
               for (int pp = 0; pp < 8; ++pp) {
-                const float l0 = lr[pp], l1 = lr[GLD + pp];
+                const float4 xv = ld4(xc + 8 * pp);
+                const float xa[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
                 for (int b4 = 0; b4 < 4; ++b4) {
-                  const float xv = xc[9 * pp + b4];
-                  acc[0][b4] = fmaf(l0, xv, acc[0][b4]);
-                  acc[1][b4] = fmaf(l1, xv, acc[1][b4]);
+                  acc[0][b4] = fmaf(l0[pp], xa[b4], acc[0][b4]);
+                  acc[1][b4] = fmaf(l1[pp], xa[b4], acc[1][b4]);
                 }
               }
-              float* dst = BB + pbB(i, j) + 9 * 2 * rr + 4 * cc;
+              float* dst = BB + pbB(i, j) + 8 * 2 * rr + 4 * cc;
 #pragma unroll
-              for (int a2 = 0; a2 < 2; ++a2)
-#pragma unroll
-                for (int b4 = 0; b4 < 4; ++b4) {
-                  float& dv = dst[9 * a2 + b4];
-                  dv = ((j == m) ? 0.f : dv) - acc[a2][b4];
-                }
+              for (int a2 = 0; a2 < 2; ++a2) {
+                float4 dv = (j == m) ? make_float4(0.f, 0.f, 0.f, 0.f) : ld4(dst + 8 * a2);
+                dv.x -= acc[a2][0];
+                dv.y -= acc[a2][1];
+                dv.z -= acc[a2][2];
+                dv.w -= acc[a2][3];
+                *reinterpret_cast<float4*>(dst + 8 * a2) = dv;
+              }
             } else {
               int c = m + 2, rem = blk - nb;
               while (rem >= 8 - c) { rem -= 8 - c; ++c; }
               const int i = c + rem;
-              const float* lr = Gs + (8 * i + 2 * rr) * GLD + 8 * m;
-              const float* lc = Gs + (8 * c + 4 * cc) * GLD + 8 * m;
+              float dm[8], l0[8], l1[8], lc[4][8];
+              ldrow8(misc + Cf::M_D + 8 * m, dm);
+              ldrow8(Gs + (8 * i + 2 * rr) * GLD + 8 * m, l0);
+              ldrow8(Gs + (8 * i + 2 * rr + 1) * GLD + 8 * m, l1);
+#pragma unroll
+              for (int b4 = 0; b4 < 4; ++b4) ldrow8(Gs + (8 * c + 4 * cc + b4) * GLD + 8 * m, lc[b4]);
 #pragma unroll
               for (int pp = 0; pp < 8; ++pp) {
-                const float dp = dm[pp];
-                const float l0 = lr[pp] * dp, l1 = lr[GLD + pp] * dp;
+                const float a0 = l0[pp] * dm[pp], a1 = l1[pp] * dm[pp];
 #pragma unroll
                 for (int b4 = 0; b4 < 4; ++b4) {
-                  const float lv = lc[b4 * GLD + pp];
-                  acc[0][b4] = fmaf(l0, lv, acc[0][b4]);
-                  acc[1][b4] = fmaf(l1, lv, acc[1][b4]);
+                  acc[0][b4] = fmaf(a0, lc[b4][pp], acc[0][b4]);
+                  acc[1][b4] = fmaf(a1, lc[b4][pp], acc[1][b4]);
                 }
               }
               float* dst = Gs + (8 * i + 2 * rr) * GLD + 8 * c + 4 * cc;
 #pragma unroll
-              for (int a2 = 0; a2 < 2; ++a2)
-#pragma unroll
-                for (int b4 = 0; b4 < 4; ++b4) dst[GLD * a2 + b4] -= acc[a2][b4];
+              for (int a2 = 0; a2 < 2; ++a2) {
+                float4 dv = ld4(dst + GLD * a2);
+                dv.x -= acc[a2][0];
+                dv.y -= acc[a2][1];
+                dv.z -= acc[a2][2];
+                dv.w -= acc[a2][3];
+                *reinterpret_cast<float4*>(dst + GLD * a2) = dv;
+              }
             }
           }
           if (m <= 5) bar_arrive(3 + (m & 1), 224);   // UB: columns >= m + 2 have column m's part
@@ -766,7 +825,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
         if (cq == 0) go[st * D + ar] = from_f32<TIO>(op * misc[Cf::M_RDEN + t]);
         __syncthreads();
       }
-      pos += c;
+      advance(c);
       continue;
     }
     // ---------------- Linv -> hi / lo operand tiles
@@ -782,7 +841,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
         const int bi = l >> 3, bj = j4 >> 3;
         loff[s] = tk_off(l, j4, 64);
 #pragma unroll
-        for (int m = 0; m < 4; ++m) lv[s][m] = (bi >= bj) ? Xp[pb8(bi, bj) + (l & 7) * 9 + (j4 & 7) + m] : 0.f;
+        for (int m = 0; m < 4; ++m) lv[s][m] = (bi >= bj) ? Xp[pb8(bi, bj) + (l & 7) * 8 + (j4 & 7) + m] : 0.f;
       }
       __syncthreads();
 #pragma unroll
@@ -1047,7 +1106,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
           }
           tc::fence_before_sync();
           __syncthreads();
-          pos += c;
+          advance(c);
           continue;
         }
         // fold the per-step scales into tril(aq) (columns t') and alpha^T (columns t)
@@ -1113,7 +1172,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     }
     tc::fence_before_sync();
     __syncthreads();
-    pos += c;
+    advance(c);
   }
 
   // ---- state out, TMEM freed
@@ -1128,7 +1187,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     if (tid < D) gn[tid] = misc[Cf::M_N + tid];
   } else if (tid == 0) {
     flags |= kStatusTimeout;
-    if (loaded + 1 < ntiles) (void)mbar_wait_bounded(in_bar, (uint32_t)((loaded + 1) & 1));
+    if (*issued > loaded) (void)mbar_wait_bounded(in_bar, (uint32_t)((loaded + 1) & 1));   // a copy in flight
   }
   if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
   if (flags) atomicOr(&a.status->flags, flags);
