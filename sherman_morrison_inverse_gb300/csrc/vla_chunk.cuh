@@ -62,7 +62,14 @@ constexpr int GLD = 68;               // leading dimension of the fp32 G / L sta
 constexpr float kGuardEps = 1e-6f;
 constexpr float kReadoutEps = 1e-6f;
 constexpr float kInvSqrtD = 0.125f;
-constexpr uint32_t kTmemCols = 256;   // 0..127: the products; 128..191: V^T alpha of G6
+constexpr uint32_t kTmemCols = 512;
+// tensor-memory columns of the products' accumulators (lanes = rows of the 128-row results)
+constexpr int TC_G1 = 0;      // [W^T; Q^T], read again as G2's X operand and for alpha = Q - Z E
+constexpr int TC_G2 = 64;     // [G - I; H^T]
+constexpr int TC_G3 = 128;    // [Z; F^T]
+constexpr int TC_G4 = 192;    // [Z D^{-1} Z^T; (Z E)^T]
+constexpr int TC_G5 = 256;    // 128 columns: [S alpha, alpha.alpha; S phi(q), phi(q).alpha]; G6 adds tril(aq) V
+constexpr int TC_G6 = 384;    // V^T alpha
 
 // High part of a 3xTF32 split: the value with the low 13 mantissa bits cleared
 // (exactly representable in tf32); the low part is x - hi.
@@ -127,6 +134,7 @@ struct Cfg {
 struct MmaPass {
   int x, y, m, n, col;   // operand offsets (floats), shape, TMEM column
   bool acc;              // accumulate into the column's previous value
+  int tx = -1;           // >= 0: the X operand is in tensor memory from this column (lanes = rows)
 };
 
 }  // namespace chk
@@ -209,25 +217,36 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     __syncthreads();
     tc::fence_after_sync();
   };
-  // Issue the passes (each D (+)= X Y^T over K), wait for them; false on a timeout.
-  auto mma_run = [&](const MmaPass* ps, int np, int K) -> bool {
-    sync_tc();
-    if (tid == 0) {
-      const uint32_t sbo = 32u * (uint32_t)K;
-      for (int p = 0; p < np; ++p) {
-        const uint32_t idesc = tc::idesc_tf32(ps[p].m, ps[p].n);
-        for (int kk = 0; kk < K / 8; ++kk)
+  // Issue the passes (each D (+)= X Y^T over K) and commit them to mma_bar (thread 0).
+  auto mma_issue = [&](const MmaPass* ps, int np, int K) {
+    const uint32_t sbo = 32u * (uint32_t)K;
+    for (int p = 0; p < np; ++p) {
+      const uint32_t idesc = tc::idesc_tf32(ps[p].m, ps[p].n);
+      for (int kk = 0; kk < K / 8; ++kk) {
+        if (ps[p].tx >= 0)
+          tc::mma_tf32_tx(tmem + (uint32_t)ps[p].col, tmem + (uint32_t)(ps[p].tx + 8 * kk),
+                          tc::sdesc(sbase + 4u * ps[p].y + 256u * kk, sbo), idesc, ps[p].acc || kk > 0);
+        else
           tc::mma_tf32(tmem + (uint32_t)ps[p].col, tc::sdesc(sbase + 4u * ps[p].x + 256u * kk, sbo),
                        tc::sdesc(sbase + 4u * ps[p].y + 256u * kk, sbo), idesc, ps[p].acc || kk > 0);
       }
-      tc::mma_commit(mma_bar);
-      if (!mbar_wait_bounded(mma_bar, mma_phase)) *flag = 1;
     }
+    tc::mma_commit(mma_bar);
+  };
+  // Wait for the committed products; false on a timeout.
+  auto mma_wait = [&]() -> bool {
+    if (tid == 0 && !mbar_wait_bounded(mma_bar, mma_phase)) *flag = 1;
     mma_phase ^= 1u;
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     return *flag == 0;
+  };
+  // Issue the passes after the operands written so far, wait for them; false on a timeout.
+  auto mma_run = [&](const MmaPass* ps, int np, int K) -> bool {
+    sync_tc();
+    if (tid == 0) mma_issue(ps, np, K);
+    return mma_wait();
   };
   // the warp's TMEM lane quadrant and column half
   const int q4 = warp & 3, half = warp >> 2;
@@ -474,36 +493,35 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
 
     // ---------------- G1: [W^T; Q^T] = [U; Sigma] A_0^T  (M 128, N 64, K 64), A_0 hi + lo
     {
-      const MmaPass ps[2] = {{Cf::F_P, Cf::F_A, 128, 64, 0, false},
-                             {Cf::F_P, Cf::F_R + TILE, 128, 64, 0, true}};
+      const MmaPass ps[2] = {{Cf::F_P, Cf::F_A, 128, 64, TC_G1, false},
+                             {Cf::F_P, Cf::F_R + TILE, 128, 64, TC_G1, true}};
       if (!mma_run(ps, 2, 64)) { failed = true; break; }
     }
+    // ---------------- G2: [G - I; H^T] = [W^T; Q^T] U^T  (M 128, N 64, K 64), X read from G1's
+    // accumulator in tensor memory; it runs while G1's W is drained.  Q^T stays there for alpha.
     {
+      MmaPass ps[1] = {{0, Cf::F_P, 128, 64, TC_G2, false}};
+      ps[0].tx = TC_G1;
+      if (tid == 0) mma_issue(ps, 1, 64);
+    }
+    if (row < 64) {   // W[i][a] = W^T[a][i], a = row (warp-uniform): fp32 -> R tile 0
       float v32[32];
       const int g = (lane >> 2) & 7;
-      tld32(32 * half, v32);
+      tld32(TC_G1 + 32 * half, v32);
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {   // [W^T; Q^T] -> Q tiles (X of G2); W (rows i) fp32 -> R tile 0
+      for (int cc = 0; cc < 2; ++cc) {
         const int col0 = 32 * half + 16 * cc;
         float (&v)[16] = *reinterpret_cast<float(*)[16]>(v32 + 16 * cc);
+        rot16(v, g);
 #pragma unroll
-        for (int j = 0; j < 16; j += 4) st4(Cf::F_Q + tk_off(row, col0 + j, 64), v[j], v[j + 1], v[j + 2], v[j + 3]);
-        if (row < 64) {   // W[i][a] = W^T[a][i], a = row (warp-uniform)
-          rot16(v, g);
-#pragma unroll
-          for (int jj = 0; jj < 16; ++jj) sf[Cf::F_R + tk_off(col0 + ((jj + g) & 15), row, 64)] = v[jj];
-        }
+        for (int jj = 0; jj < 16; ++jj) sf[Cf::F_R + tk_off(col0 + ((jj + g) & 15), row, 64)] = v[jj];
       }
     }
-    // ---------------- G2: [G - I; H^T] = [W^T; Q^T] U^T  (M 128, N 64, K 64)
-    {
-      const MmaPass ps[1] = {{Cf::F_Q, Cf::F_P, 128, 64, 0, false}};
-      if (!mma_run(ps, 1, 64)) { failed = true; break; }
-    }
+    if (!mma_wait()) { failed = true; break; }
     float* Gs = sf + Cf::F_P;   // [64][GLD]: G, then L (strict lower) in place
     {
       float v32[32];
-      tld32(32 * half, v32);
+      tld32(TC_G2 + 32 * half, v32);
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int col0 = 32 * half + 16 * cc;
@@ -854,14 +872,14 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     }
     // ---------------- G3: [Z; F^T] = [W; H^T] Linv^T  (M 128, N 64, K 64), 3xTF32
     {
-      const MmaPass ps[3] = {{Cf::F_R, Cf::F_L, 128, 64, 0, false},
-                             {Cf::F_R, Cf::F_Q, 128, 64, 0, true},
-                             {Cf::F_P, Cf::F_L, 128, 64, 0, true}};
+      const MmaPass ps[3] = {{Cf::F_R, Cf::F_L, 128, 64, TC_G3, false},
+                             {Cf::F_R, Cf::F_Q, 128, 64, TC_G3, true},
+                             {Cf::F_P, Cf::F_L, 128, 64, TC_G3, true}};
       if (!mma_run(ps, 3, 64)) { failed = true; break; }
     }
     {
       float v32[32];
-      tld32(32 * half, v32);
+      tld32(TC_G3 + 32 * half, v32);
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int col0 = 32 * half + 16 * cc;
@@ -887,15 +905,16 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     }
     // ---------------- G4: [Z D^{-1} Z^T ; (Z E)^T] = [Z/D; E^T] Z^T  (M 128, N 64, K 64), 3xTF32
     {
-      const MmaPass ps[3] = {{Cf::F_R, Cf::F_L, 128, 64, 0, false},
-                             {Cf::F_P, Cf::F_L, 128, 64, 0, true},
-                             {Cf::F_R, Cf::F_Q, 128, 64, 0, true}};
+      const MmaPass ps[3] = {{Cf::F_R, Cf::F_L, 128, 64, TC_G4, false},
+                             {Cf::F_P, Cf::F_L, 128, 64, TC_G4, true},
+                             {Cf::F_R, Cf::F_Q, 128, 64, TC_G4, true}};
       if (!mma_run(ps, 3, 64)) { failed = true; break; }
     }
     {
-      float v32[32];
+      float v32[32], q32[32];
       float an = 0.f;
-      tld32(32 * half, v32);
+      tld32(TC_G4 + 32 * half, v32);
+      if (row >= 64) tld32(TC_G1 + 32 * half, q32);   // Q^T rows (warp-uniform)
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int col0 = 32 * half + 16 * cc;
@@ -922,13 +941,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
           const int t = row - 64;
           float al[16];
 #pragma unroll
-          for (int j = 0; j < 16; j += 4) {
-            const float4 qv = *reinterpret_cast<const float4*>(sf + Cf::F_Q + tk_off(64 + t, col0 + j, 64));
-            al[j] = qv.x - v[j];
-            al[j + 1] = qv.y - v[j + 1];
-            al[j + 2] = qv.z - v[j + 2];
-            al[j + 3] = qv.w - v[j + 3];
-          }
+          for (int j = 0; j < 16; ++j) al[j] = q32[16 * cc + j] - v[j];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             float x = al[j];
@@ -959,7 +972,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     }
     // ---------------- G5: [S alpha ; S phi(q) | alpha.alpha ; phi(q).alpha] = [alpha; phi(q)] [S; alpha]^T
     {
-      const MmaPass ps[1] = {{Cf::F_AL, Cf::F_S, 128, 128, 0, false}};
+      const MmaPass ps[1] = {{Cf::F_AL, Cf::F_S, 128, 128, TC_G5, false}};
       if (!mma_run(ps, 1, 64)) { failed = true; break; }
     }
     if (row >= 64) {   // warp-uniform: quadrants 2, 3 (rows 64 + t); S phi(q_t) stays in TMEM for G6
@@ -967,7 +980,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
       const int t = row - 64;
       if (32 * half < C) {
         float v32[32];
-        tld32(64 + 32 * half, v32);
+        tld32(TC_G5 + 64 + 32 * half, v32);
         if (t < C) {
 #pragma unroll
           for (int j = 0; j < 32; j += 4) {
@@ -1010,7 +1023,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
             float xs = 0.f;
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
-              tld(16 * cc, v);
+              tld(TC_G5 + 16 * cc, v);
 #pragma unroll
               for (int j = 0; j < 16; ++j)
                 if (t < c) xs = fmaf(to_f32(vb[t * 64 + 16 * cc + j]), v[j], xs);
@@ -1019,7 +1032,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
           } else {
 #pragma unroll
             for (int cc = 0; cc < (C + 15) / 16; ++cc) {
-              tld(64 + 16 * cc, v);
+              tld(TC_G5 + 64 + 16 * cc, v);
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
                 const int tp = 16 * cc + j;
@@ -1121,8 +1134,8 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     // ---------------- G6: X = [V^T; tril(aq)] (M 128, K C); Y = V^T accumulates tril(aq) V onto
     // S phi(q_t) (rows 64 + t, columns 0..63); Y = alpha^T gives V^T alpha (rows i, columns 128..191)
     {
-      const MmaPass ps[2] = {{Cf::F_T6, Cf::F_T6 + Cf::T6_V, 128, 64, 0, true},
-                             {Cf::F_T6, Cf::F_T6 + Cf::T6_A, 128, 64, 128, false}};
+      const MmaPass ps[2] = {{Cf::F_T6, Cf::F_T6 + Cf::T6_V, 128, 64, TC_G5, true},
+                             {Cf::F_T6, Cf::F_T6 + Cf::T6_A, 128, 64, TC_G6, false}};
       if (!mma_run(ps, 2, C)) { failed = true; break; }
     }
     {
@@ -1130,7 +1143,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
       if (row >= 64) {   // outputs of step t, columns 32 half .. 32 half + 31 (warp-uniform)
         const int t = row - 64;
         const float sgt = misc[Cf::M_SG + t], rd = misc[Cf::M_RDEN + t];
-        tld32(32 * half, v32);
+        tld32(TC_G5 + 32 * half, v32);
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           const int col0 = 32 * half + 16 * cc;
@@ -1152,7 +1165,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
       } else {           // S_1 = sigma (S + V^T alpha), rows i, columns 32 half .. 32 half + 31
         const int i = row;
         const float sgl = misc[Cf::M_SG + c - 1];
-        tld32(128 + 32 * half, v32);
+        tld32(TC_G6 + 32 * half, v32);
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           const int col0 = 32 * half + 16 * cc;

@@ -93,6 +93,18 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t xdesc, uint64
       : "memory");
 }
 
+// One MMA with the X operand in tensor memory (lane = row of X, one 32-bit column per K
+// element, K = 8 columns from x_tmem): D (+)= X * Y^T for one K step.
+__device__ __forceinline__ void mma_tf32_tx(uint32_t d_tmem, uint32_t x_tmem, uint64_t ydesc, uint32_t idesc,
+                                            bool accumulate) {
+  const uint32_t acc = accumulate ? 1u : 0u;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(x_tmem), "l"(ydesc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
 // Arrive on `bar` once every MMA this thread issued so far has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
