@@ -119,7 +119,8 @@ struct Cfg {
   static constexpr int M_D = 0, M_ID = 64, M_RDEN = 128, M_VN = 192, M_SL = 256, M_XS = 320, M_AN = 384;
   static constexpr int M_SG = 448, M_IS = 512, M_RED = 576, M_VEC = 640, M_VEC2 = 704, M_SCAL = 768;
   static constexpr int M_N = 800, M_NSEG = 864, M_AN2 = 1120;
-  static constexpr int MISC = 1248;
+  static constexpr int M_SS = 1248, M_SSV = 1252, M_EX = 1253;   // ||S||^2 partials, their validity, the bound test
+  static constexpr int MISC = 1256;
   static constexpr int F_VB = F_MISC + MISC;              // V of the chunk (TIO) [C][64]
   static constexpr size_t float_bytes = sizeof(float) * (size_t)F_VB + sizeof(TIO) * C * 64;
   static constexpr size_t bar_off = STAGE_PAD + (float_bytes + 15) / 16 * 16;
@@ -178,6 +179,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     sf[Cf::F_S + tk_off(i, j, 64)] = gS[e];
   }
   if (tid < D) misc[Cf::M_N + tid] = gn[tid];
+  if (tid == 0) misc[Cf::M_SSV] = 0.f;   // ||S||^2 of the initial state: computed by the first chunk
   if (tid == 0) {
     mbar_init(in_bar, 1);
     mbar_init(mma_bar, 1);
@@ -843,6 +845,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
         if (cq == 0) go[st * D + ar] = from_f32<TIO>(op * misc[Cf::M_RDEN + t]);
         __syncthreads();
       }
+      if (tid == 0) misc[Cf::M_SSV] = 0.f;   // S changed step by step: its norm is recomputed
       advance(c);
       continue;
     }
@@ -911,10 +914,31 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
       if (!mma_run(ps, 3, 64)) { failed = true; break; }
     }
     {
-      float v32[32], q32[32];
+      float v32[32], al32[32];
       float an = 0.f;
       tld32(TC_G4 + 32 * half, v32);
-      if (row >= 64) tld32(TC_G1 + 32 * half, q32);   // Q^T rows (warp-uniform)
+      if (row >= 64) {   // alpha_t = Q_t - (Z E)_t (+ eps_n s_t at a nudge step), rows t (warp-uniform)
+        const int t = row - 64;
+        tld32(TC_G1 + 32 * half, al32);   // Q^T rows, from G1's accumulator
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          float x = al32[j] - v32[j];
+          if (nudge && t == c - 1) x = fmaf(a.eps_n, misc[Cf::M_SL + 32 * half + j], x);
+          if (t >= c) x = 0.f;
+          al32[j] = x;
+          an = fmaf(x, x, an);
+        }
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+          st4(Cf::F_AL + tk_off(t, 32 * half + j, 64), al32[j], al32[j + 1], al32[j + 2], al32[j + 3]);
+      }
+      // ---------------- G5: [S alpha ; S phi(q) | alpha.alpha ; phi(q).alpha] = [alpha; phi(q)] [S; alpha]^T,
+      // issued as soon as alpha is written; the rest of G4's drain runs beside it
+      sync_tc();
+      if (tid == 0) {
+        const MmaPass ps[1] = {{Cf::F_AL, Cf::F_S, 128, 128, TC_G5, false}};
+        mma_issue(ps, 1, 64);
+      }
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int col0 = 32 * half + 16 * cc;
@@ -937,30 +961,15 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
             }
             *ap = x;
           }
-        } else {          // alpha_t = Q_t - (Z E)_t (+ eps_n s_t at a nudge step)
+        } else if (row - 64 < C) {
+          // alpha^T (rows j, K = t): lane group g = lane / 4 writes column col0 + ((jj + g) & 15) in
+          // store jj, so the 8 groups hit 8 different core-matrix rows (32 distinct banks)
           const int t = row - 64;
-          float al[16];
+          float (&al)[16] = *reinterpret_cast<float(*)[16]>(al32 + 16 * cc);
+          const int g = (lane >> 2) & 7;
+          rot16(al, g);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) al[j] = q32[16 * cc + j] - v[j];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            float x = al[j];
-            if (nudge && t == c - 1) x = fmaf(a.eps_n, misc[Cf::M_SL + col0 + j], x);
-            if (t >= c) x = 0.f;
-            al[j] = x;
-            an = fmaf(x, x, an);
-          }
-#pragma unroll
-          for (int j = 0; j < 16; j += 4) st4(Cf::F_AL + tk_off(t, col0 + j, 64), al[j], al[j + 1], al[j + 2], al[j + 3]);
-          if (t < C) {
-            // alpha^T (rows j, K = t): lane group g = lane / 4 writes column col0 + ((jj + g) & 15) in
-            // store jj, so the 8 groups hit 8 different core-matrix rows (32 distinct banks)
-            const int g = (lane >> 2) & 7;
-            rot16(al, g);
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj)
-              sf[Cf::F_T6 + Cf::T6_A + tk_off(col0 + ((jj + g) & 15), t, C)] = al[jj];
-          }
+          for (int jj = 0; jj < 16; ++jj) sf[Cf::F_T6 + Cf::T6_A + tk_off(col0 + ((jj + g) & 15), t, C)] = al[jj];
         }
       }
       if (row >= 64) misc[Cf::M_AN2 + 64 * half + (row - 64)] = an;   // |alpha_t|^2, two halves
@@ -969,11 +978,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
         const int i = ((e >> 5) & 7) * 8 + ((e >> 2) & 7), t = (e >> 8) * 4 + (e & 3);
         sf[Cf::F_T6 + Cf::T6_V + tk_off(i, t, C)] = to_f32(vb[t * 64 + i]);
       }
-    }
-    // ---------------- G5: [S alpha ; S phi(q) | alpha.alpha ; phi(q).alpha] = [alpha; phi(q)] [S; alpha]^T
-    {
-      const MmaPass ps[1] = {{Cf::F_AL, Cf::F_S, 128, 128, TC_G5, false}};
-      if (!mma_run(ps, 1, 64)) { failed = true; break; }
+      if (!mma_wait()) { failed = true; break; }
     }
     if (row >= 64) {   // warp-uniform: quadrants 2, 3 (rows 64 + t); S phi(q_t) stays in TMEM for G6
       // aq[t][t'] = phi(q_t) . alpha_t', t' <= t -> tril(aq) rows t of T6 (half h: t' = 32 h .. 32 h + 31)
@@ -995,20 +1000,36 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     }
     // ||S||^2, the bound and the renormalisation decisions
     {
-      float sq = 0.f, bsum = 0.f;
-      for (int e4 = tid; e4 < TILE / 4; e4 += NT) {
-        const float4 x = *reinterpret_cast<const float4*>(sf + Cf::F_S + 4 * e4);
-        sq = fmaf(x.x, x.x, fmaf(x.y, x.y, fmaf(x.z, x.z, fmaf(x.w, x.w, sq))));
+      // ||S||^2: carried from the previous chunk's state update (M_SS), else recomputed
+      float ns;
+      if (misc[Cf::M_SSV] != 0.f) {
+        ns = (misc[Cf::M_SS] + misc[Cf::M_SS + 1]) + (misc[Cf::M_SS + 2] + misc[Cf::M_SS + 3]);
+      } else {
+        float sq = 0.f;
+        for (int e4 = tid; e4 < TILE / 4; e4 += NT) {
+          const float4 x = *reinterpret_cast<const float4*>(sf + Cf::F_S + 4 * e4);
+          sq = fmaf(x.x, x.x, fmaf(x.y, x.y, fmaf(x.z, x.z, fmaf(x.w, x.w, sq))));
+        }
+        ns = block_sum(sq);
       }
-      __syncthreads();   // the |alpha_t|^2 halves from the G4 drain
-      if (tid < c) {
-        const float an = misc[Cf::M_AN2 + tid] + misc[Cf::M_AN2 + 64 + tid];
-        misc[Cf::M_AN + tid] = an;
-        bsum = misc[Cf::M_VN + tid] * sqrtf(fmaxf(an, 0.f));
+      // the bound ||S|| + sum_t |v_t| |alpha_t| (one warp), |alpha_t|^2 -> M_AN
+      if (warp == 0) {
+        float bsum = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int t = lane + 32 * h;
+          if (t < c) {
+            const float an = misc[Cf::M_AN2 + t] + misc[Cf::M_AN2 + 64 + t];
+            misc[Cf::M_AN + t] = an;
+            bsum = fmaf(misc[Cf::M_VN + t], sqrtf(fmaxf(an, 0.f)), bsum);
+          }
+        }
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) bsum += __shfl_xor_sync(0xffffffffu, bsum, m);
+        if (lane == 0) misc[Cf::M_EX] = (sqrtf(ns) + bsum <= a.tau * (1.f - 0x1p-12f)) ? 0.f : 1.f;
       }
-      block_sum2(sq, bsum);   // contains __syncthreads: the drain writes above are visible
-      const float ns = sq;
-      const bool exact = !(sqrtf(ns) + bsum <= a.tau * (1.f - 0x1p-12f));
+      __syncthreads();
+      const bool exact = misc[Cf::M_EX] != 0.f;
       if (!exact) {
         if (tid < 64) {
           misc[Cf::M_SG + tid] = 1.f;   // sigma after step t
@@ -1117,6 +1138,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
             op += __shfl_xor_sync(0xffffffffu, op, 2);
             if (cq == 0) go[(pos + t) * D + ar] = from_f32<TIO>(op * misc[Cf::M_RDEN + t]);
           }
+          if (tid == 0) misc[Cf::M_SSV] = 0.f;   // S changed step by step: its norm is recomputed
           tc::fence_before_sync();
           __syncthreads();
           advance(c);
@@ -1165,6 +1187,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
       } else {           // S_1 = sigma (S + V^T alpha), rows i, columns 32 half .. 32 half + 31
         const int i = row;
         const float sgl = misc[Cf::M_SG + c - 1];
+        float ss = 0.f;   // this thread's part of ||S_1||^2 for the next chunk's bound
         tld32(TC_G6 + 32 * half, v32);
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
@@ -1179,8 +1202,13 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
             x.z = sgl * (x.z + v[j + 2]);
             x.w = sgl * (x.w + v[j + 3]);
             *sp = x;
+            ss = fmaf(x.x, x.x, fmaf(x.y, x.y, fmaf(x.z, x.z, fmaf(x.w, x.w, ss))));
           }
         }
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+        if (lane == 0) misc[Cf::M_SS + q4 + 2 * half] = ss;   // warps 0, 1, 4, 5
+        if (tid == 0) misc[Cf::M_SSV] = 1.f;
       }
     }
     tc::fence_before_sync();
