@@ -84,6 +84,14 @@ __device__ __forceinline__ float phi_fast(float x) { return x > 0.f ? x + 1.f : 
 __host__ __device__ constexpr int pb8(int bi, int bj) { return (bi * (bi + 1) / 2 + bj) * 64; }
 __host__ __device__ constexpr int pbB(int bi, int bj) { return (bi * (bi - 1) / 2 + bj) * 64; }
 
+// 1/x by the SFU's approximate reciprocal (rcp.approx.ftz.f32: about 1 ulp; the pivots of D are >=
+// 1 for an SPD A, far from the flushed range; a pivot below the guard threshold is caught anyway)
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
 // named barriers (ids 1..5; 0 is __syncthreads): `n` threads take part, a multiple of 32
 __device__ __forceinline__ void bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 __device__ __forceinline__ void bar_arrive(int id, int n) {
@@ -591,12 +599,17 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           d8[j] = a8[j][j];
-          id8[j] = __fdividef(1.f, d8[j]);
+          id8[j] = rcp_approx(d8[j]);
 #pragma unroll
           for (int i = j + 1; i < 8; ++i) {
             const float lij = a8[i][j] * id8[j];
 #pragma unroll
-            for (int m = j + 1; m <= i; ++m) a8[i][m] = fmaf(-lij, a8[m][j], a8[i][m]);   // a8[m][j] = L_mj D_j
+            for (int m = j + 1; m <= i; ++m) {
+              if (m == i && i == j + 1)   // the next pivot: one rounding step after the reciprocal
+                a8[i][m] = fmaf(-(a8[i][j] * a8[i][j]), id8[j], a8[i][m]);
+              else
+                a8[i][m] = fmaf(-lij, a8[m][j], a8[i][m]);   // a8[m][j] = L_mj D_j
+            }
           }
 #pragma unroll
           for (int i = j + 1; i < 8; ++i) a8[i][j] *= id8[j];
