@@ -59,6 +59,7 @@ constexpr int NT = 256;
 constexpr int TILE = 64 * 64;         // floats of a TK(64, 64) operand tile
 constexpr int PLD = 68;               // leading dimension of the prologue's phi(k) / phi(q) scratch
 constexpr int GLD = 68;               // leading dimension of the fp32 G / L staging (16-byte rows)
+constexpr int kHelpers = 224;         // threads of the LDL^T helper warps (warps 1..7)
 constexpr float kGuardEps = 1e-6f;
 constexpr float kReadoutEps = 1e-6f;
 constexpr float kInvSqrtD = 0.125f;
@@ -633,7 +634,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
           st8(misc + Cf::M_D + 8 * k, d8);
           st8(misc + Cf::M_ID + 8 * k, id8);
         }
-        bar_arrive(1 + (k & 1), 224);   // LB: block column k of L and D_k are written
+        bar_arrive(1 + (k & 1), 32 + kHelpers);   // LB: block column k of L and D_k are written
         if (k < 7) {
           // column k's contribution to block column k + 1, -L_{.k} D_k L_{k+1,k}^T: (L D)_{k+1,k}
           // (lanes 8 ((k+1) % 4) .. + 7 of row set (k+1) / 4), transposed, to every lane
@@ -652,7 +653,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
           }
           __syncwarp();
           // the helpers' contributions of columns <= k - 1 to column k + 1 are in the staging
-          if (k >= 1) bar_sync(3 + ((k - 1) & 1), 224);
+          if (k >= 1) bar_sync(3 + ((k - 1) & 1), 32 + kHelpers);
           auto next = [&](int r, float (&g)[8]) {   // g: this row's L_{r,k}; becomes G'_{r,k+1}
             float cur[8];
             if (r >= 8 * (k + 1)) {
@@ -680,8 +681,8 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
           next(32 + lane, gb);
         }
       }
-        } else if (warp != 4) {
-      const int ot = ((warp < 4) ? warp - 1 : warp - 2) * 32 + lane;   // 0..191
+        } else {
+      const int ot = (warp - 1) * 32 + lane;   // 0 .. kHelpers - 1
       auto ld4 = [](const float* pp) { return *reinterpret_cast<const float4*>(pp); };
       auto ldrow8 = [&](const float* pp, float (&v)[8]) {
         const float4 x0 = ld4(pp), x1 = ld4(pp + 4);
@@ -689,7 +690,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
       };
 #pragma unroll 1
       for (int m = 0; m < 8; ++m) {
-        bar_sync(1 + (m & 1), 224);   // LB: block column m of L is written
+        bar_sync(1 + (m & 1), 32 + kHelpers);   // LB: block column m of L is written
         // block row m of X: X_mj = L_mm^{-1} B_mj (j < m), X_mm = L_mm^{-1}; a column per thread
         if (ot < 8 * (m + 1)) {
           const int j = ot >> 3, c = ot & 7;
@@ -707,13 +708,13 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
 #pragma unroll
           for (int i = 0; i < 8; ++i) XB[pb8(m, j) + 8 * i + c] = x[i];
         }
-        bar_sync(5, 192);
+        bar_sync(5, kHelpers);
         if (m < 7) {
           // 2 x 4 tiles of: B_ij -= L_im X_mj (i > m, j <= m; B_im starts at 0), and of the
           // trailing update G'_ic -= L_im D_m L_cm^T (c >= m + 2, i >= c); rows in registers,
           // 16-byte loads
           const int nb = (7 - m) * (m + 1), nt = (6 - m) * (7 - m) / 2;
-          for (int q = ot; q < 8 * (nb + nt); q += 192) {
+          for (int q = ot; q < 8 * (nb + nt); q += kHelpers) {
             const int blk = q >> 3, rr = (q >> 1) & 3, cc = q & 1;
             float acc[2][4];
 #pragma unroll
@@ -777,7 +778,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
               }
             }
           }
-          if (m <= 5) bar_arrive(3 + (m & 1), 224);   // UB: columns >= m + 2 have column m's part
+          if (m <= 5) bar_arrive(3 + (m & 1), 32 + kHelpers);   // UB: columns >= m + 2 have column m's part
         }
       }
     }
