@@ -19,34 +19,38 @@
 //       [V^T alpha ; .]   = [V^T; tril(aq)] (alpha^T)^T
 //       o_t = (S phi(q_t) + sum_{t'<=t} (alpha_t'.phi(q_t)) v_t') / den_t,   S_1 = S + V^T alpha
 //
-// Every product is arranged so that its TMEM drain (lane = row of the result)
-// writes the next operand row-major: float4 stores into the K-major core-matrix
-// layout, free of bank conflicts.  The one transposed operand (alpha^T) is
-// written with a per-lane register rotation that spreads the lanes over all banks.
+// Every product accumulates in its own range of the 512 TMEM columns, so a result can
+// stay there while later products run: G2 takes its X operand straight from G1's
+// accumulator, and alpha reads Q from it.  The other drains (lane = row of the result)
+// write the next operand row-major: float4 stores into the K-major core-matrix layout,
+// free of bank conflicts; the transposed operands (W, alpha^T) are written with a
+// per-lane register rotation that spreads the lanes over all banks.  G2 is issued as
+// soon as G1 completes, and G5 as soon as alpha is written, so that the rest of the
+// previous drain runs beside the product.
 //
-// LDL^T and L^{-1} run in 16 x 16 blocks, right-looking, with L^{-1} carried along
-// as the forward elimination of the identity: one warp factors a diagonal block as
-// 2 x 2 blocks of 8 in registers and inverts its unit-lower factor there, 192
-// threads multiply that inverse into the panel and the eliminated identity's
-// blocks, and the trailing update of one block column runs beside the factoring of
-// the next diagonal block.
+// LDL^T and L^{-1} run in block columns of 8, right-looking.  Warp 0 walks the chain of
+// pivots: it factors each 8 x 8 diagonal block in registers, forms its panel rows and
+// applies the column's contribution to the next block column, keeping its rows in
+// registers; the seven other warps form L^{-1} block row by block row (the forward
+// elimination of the identity) and the trailing updates one step behind, handing over
+// through named barriers.
 //
 // Renormalisation: ||S_t||^2 = ||S||^2 + 2 sum v_t'^T S alpha_t' + sum (v.v)(alpha.alpha) from the
-// products above; the bound ||S|| + sum |v_t||alpha_t| decides that no step can
-// exceed tau, otherwise the exact per-step norms give the decisions and the
-// per-step scales are folded into tril(aq), alpha^T and the outputs.  When the
-// scales of one chunk fall below 2^-64 (tau far below the norm each step adds),
-// that chunk's S and outputs are taken step by step from its alpha instead.
+// products above; the bound ||S|| + sum |v_t||alpha_t| (||S||^2 carried from the previous
+// chunk's state update) decides that no step can exceed tau, otherwise the exact per-step
+// norms give the decisions and the per-step scales are folded into tril(aq), alpha^T and
+// the outputs.  When the scales of one chunk fall below 2^-64 (tau far below the norm
+// each step adds), that chunk's S and outputs are taken step by step from its alpha instead.
 // A pivot |D_jj| < 1e-6 means the sequential recurrence takes the singularity
 // guard inside the chunk; the chunk is then taken step by step on CUDA cores.
 // Chunks end at nudge steps (A += eps_n I is not a rank-1 update).
 //
-// Precision: operands are fp32 in shared memory, read by the tensor core as
-// tf32.  The products that carry A forward (G1's A_0, G3, G4) are 3xTF32: each
-// fp32 operand x is split into hi = x with its low 13 mantissa bits cleared
-// (exact in tf32) and lo = x - hi, and hi*hi + lo*hi + hi*lo is accumulated, so A
-// tracks the fp32 recurrence.  G2, G5 and G6 are plain tf32.  The state (A, S)
-// stays fp32.  Built for d = d_v = 64 and bfloat16 I/O.
+// Precision: operands are fp32 in shared memory, read by the tensor core as tf32, which
+// drops the low 13 mantissa bits (truncation).  The products that carry A forward (G1's
+// A_0, G3, G4) are 3xTF32: the fp32 operand x is its own high part, lo = x - hi is stored
+// beside it, and hi*hi + lo*hi + hi*lo is accumulated, so A tracks the fp32 recurrence.
+// G2, G5 and G6 are plain tf32.  The state (A, S) stays fp32.  Built for d = d_v = 64
+// and bfloat16 I/O.
 #pragma once
 
 #include "vla_tc.cuh"
@@ -557,13 +561,12 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     // for block column k it factors the 8 x 8 diagonal block in every lane's registers, turns
     // the rows below it into L (forward substitution against L_kk, then D^{-1}), and applies
     // column k's contribution -L_{.k} D_k L_{k+1,k}^T to block column k+1, so that the next
-    // step can start at once.  Six helper warps follow one step behind: they form block row k
+    // step can start at once.  The seven helper warps follow one step behind: they form block row k
     // of X = L^{-1} (X_kj = L_kk^{-1} B_kj, where B is the identity being eliminated), update
     // B_ij -= L_ik X_kj for i > k, and apply column k's contribution to the block columns
     // beyond k + 1.  Warp 0 and the helpers hand over through named barriers (LB: column k of
     // L is written; UB: the helpers' trailing update for column k is done), used in
     // alternation so that a barrier is never reused before its previous round completed.
-    // Warp 4 shares warp 0's SM sub-partition and stays idle.
     float* XB = sf + Cf::F_Q;   // X = L^{-1}: 36 lower 8 x 8 blocks
     float* BB = sf + Cf::F_L;   // B: 28 strictly lower 8 x 8 blocks
     if (warp == 0) {
