@@ -248,33 +248,32 @@ def job_value(units_per_rank: int, world: int, ms_max: float) -> float:
     return units_per_rank * world / (ms_max / 1e3)
 
 
-_ORACLE_STATE = {}   # per worker process: the inputs of its pairs
-
-
-def _oracle_prepare(job):
-    """Worker: generate the inputs of this worker's pairs (the seeded generators are
-    subset-stable, so each pair's inputs are the same as in the full workload)."""
-    w, T_max, pairs = job
-    _ORACLE_STATE["w"] = w
-    _ORACLE_STATE["x"] = workloads.make_inputs(w, pairs=list(pairs), T=T_max)
-    return len(pairs)
-
-
-def _oracle_run(steps):
-    """Worker: the oracle over its pairs and the first `steps` steps; returns its wall time."""
+def _oracle_worker(conn, job):
+    """Worker process: generate the inputs of its pairs (the seeded generators are
+    subset-stable, so each pair's inputs are the same as in the full workload), then, for
+    every `steps` received, run the oracle over its pairs and the first `steps` steps and
+    send back its wall time; None ends it."""
     import oracle
-    x, w = _ORACLE_STATE["x"], _ORACLE_STATE["w"]
-    t0 = time.perf_counter()
-    oracle.scan(x["q"][:, :steps], x["k"][:, :steps], x["v"][:, :steps], x["u"][:, :steps],
-                x["A0"], x["S0"], x["n0"], P=w.P, eps_n=w.eps_n, tau=w.tau)
-    return time.perf_counter() - t0
+    w, T_max, pairs = job
+    x = workloads.make_inputs(w, pairs=list(pairs), T=T_max)
+    conn.send(len(pairs))
+    while True:
+        steps = conn.recv()
+        if steps is None:
+            break
+        t0 = time.perf_counter()
+        oracle.scan(x["q"][:, :steps], x["k"][:, :steps], x["v"][:, :steps], x["u"][:, :steps],
+                    x["A0"], x["S0"], x["n0"], P=w.P, eps_n=w.eps_n, tau=w.tau)
+        conn.send(time.perf_counter() - t0)
+    conn.close()
 
 
 class OracleLeg:
     """The float64 oracle, as it stands, timed on the host cores on a bounded sample of the
     workload: every pair, the first `steps` steps.  The pairs are independent, so they are
     shared out over one single-threaded process per host CPU (spawned, so no process is
-    forked from one that has used the GPU); the wall time of all of them together is timed."""
+    forked from one that has used the GPU), each holding one fixed group of pairs; the wall
+    time of all of them together is timed."""
 
     def __init__(self, w, T_full: int, T_max: int = 8192, procs: int | None = None):
         import multiprocessing as mp
@@ -284,12 +283,24 @@ class OracleLeg:
         self.T_max = min(w.T, T_max)
         self.procs = max(1, min(procs or (os.cpu_count() or 1), w.pairs))
         groups = np.array_split(np.arange(w.pairs), self.procs)
-        self.pool = mp.get_context("spawn").Pool(self.procs)
-        self.pool.map(_oracle_prepare, [(w.with_(T=T_full), self.T_max, tuple(int(p) for p in g)) for g in groups])
+        ctx = mp.get_context("spawn")
+        self.workers = []
+        for g in groups:
+            parent, child = ctx.Pipe()
+            p = ctx.Process(target=_oracle_worker, args=(child, (w.with_(T=T_full), self.T_max,
+                                                                 tuple(int(i) for i in g))), daemon=True)
+            p.start()
+            child.close()
+            self.workers.append((p, parent))
+        done = sum(conn.recv() for _, conn in self.workers)   # every worker holds its inputs
+        assert done == w.pairs, (done, w.pairs)
 
     def run(self, steps: int):
         t0 = time.perf_counter()
-        self.pool.map(_oracle_run, [steps] * self.procs)
+        for _, conn in self.workers:
+            conn.send(steps)
+        for _, conn in self.workers:
+            conn.recv()
         wall = time.perf_counter() - t0
         return self.w.pairs * steps / wall, wall, self.procs
 
@@ -306,8 +317,16 @@ class OracleLeg:
                 f"pairs shared out over {self.procs} single-threaded processes ({wall:.1f} s wall)")
 
     def close(self):
-        self.pool.close()
-        self.pool.join()
+        for p, conn in self.workers:
+            try:
+                conn.send(None)
+                conn.close()
+            except OSError:
+                pass
+        for p, _ in self.workers:
+            p.join(timeout=30)
+            if p.is_alive():
+                p.terminate()
 
 
 def host_cpu_info() -> dict:

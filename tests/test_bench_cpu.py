@@ -101,6 +101,20 @@ def test_oracle_leg_shares_the_pairs_over_processes():
     assert "2 single-threaded processes" in leg.sample_text(16, wall)
 
 
+def test_oracle_leg_runs_every_group_in_its_own_process_each_time():
+    """Each worker holds one fixed group of pairs and runs it on every call (a pool that may
+    hand two calls to one worker would leave a group unrun, or run a worker with no inputs)."""
+    w = workloads.get(0).with_(B=1, H=4, T=32)
+    leg = bench.OracleLeg(w, T_full=32, procs=4)
+    try:
+        for steps in (4, 8, 16):
+            value, wall, procs = leg.run(steps)
+            assert procs == 4 and value > 0
+    finally:
+        leg.close()
+    assert all(not p.is_alive() for p, _ in leg.workers)
+
+
 def test_no_function_shadows_a_module_function_it_calls():
     """bench.py's GPU legs run only on a GPU; this static check catches a local variable
     that hides a module-level function the same body calls (an error the CPU suite would
