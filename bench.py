@@ -412,6 +412,16 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
+def proj_tma_fits(d: int, r: int) -> bool:
+    """Whether vla_project_u takes its TMA-fed bf16 form: the key ring, the staging tiles and
+    W's three bf16 terms for all r ranks fit in one CTA's 227 KB of shared memory."""
+    bx = min(d, 64)
+    slab = 128 * bx * 2
+    ks = 2 if d == 128 else 3
+    nbytes = ks * (d // bx) * slab + 4 * slab + 3 * r * d * d * 2
+    return (nbytes + 15) // 16 * 16 + 8 * (2 * ks + 5) + 16 <= 227 * 1024
+
+
 def run_project_u(args, w):
     """Time vla_project_u (u = normalize(W_u k_raw)) over the workload's B H T keys."""
     import sherman_morrison_inverse_gb300 as vla
@@ -426,30 +436,47 @@ def run_project_u(args, w):
     for _ in range(args.warmup):
         h.project_u(k, W, u)
     torch.cuda.synchronize(dev)
+    # A call takes a fraction of a millisecond: the clock sampler needs a few hundred ms to
+    # start, so warm-up calls continue until it is up, and the timed region repeats blocks of
+    # `steps` calls until it spans at least a second (every call timed, none skipped).
     clocks = ClockSampler(0)
+    t_start = time.perf_counter()
+    while time.perf_counter() - t_start < 0.5:
+        for _ in range(args.steps):
+            h.project_u(k, W, u)
+        torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    calls = 0
     e0.record()
-    for _ in range(args.steps):
-        h.project_u(k, W, u)
+    t_start = time.perf_counter()
+    while calls == 0 or time.perf_counter() - t_start < 1.0:
+        for _ in range(args.steps):
+            h.project_u(k, W, u)
+        calls += args.steps   # the launch queue bounds how far the host runs ahead
     e1.record()
     torch.cuda.synchronize(dev)
     clk = clocks.stop()
-    ms = e0.elapsed_time(e1) / args.steps
+    ms = e0.elapsed_time(e1) / calls
     peaks = load_peaks()
     flops = 2 * w.r * w.d * w.d * n
     nbytes = n * (w.d + w.r * w.d) * k.element_size()   # keys in, directions out (W: a few KB)
     # the tensor-core forms serve every shape but d = 128 with float32 keys; the projection is
     # bound by HBM: a few flops per byte, far below the tensor ridge
     tc = not (w.d == 128 and w.io == "f32")
-    if w.io == "bf16":
-        form, dt = "tcgen05 kind::f16: bf16 keys, W as three bf16 terms (3 passes), fp32 accumulation", "bf16"
+    if w.io == "bf16" and proj_tma_fits(w.d, w.r):
+        form, dt = ("tcgen05 kind::f16: bf16 key tiles by TMA tensor loads (swizzled), the r weight sets "
+                    "stacked into one N = r d product, outputs by TMA tensor stores; W as three bf16 terms "
+                    "(3 passes), fp32 accumulation"), "bf16"
+    elif w.io == "bf16":
+        form, dt = ("tcgen05 kind::f16: bf16 keys through registers, one rank at a time; W as three bf16 "
+                    "terms (3 passes), fp32 accumulation"), "bf16"
     elif tc:
         form, dt = "tcgen05 kind::tf32: keys and W as tf32 hi + lo (3 passes), fp32 accumulation", "tf32"
     else:
         form, dt = "CUDA cores, float32", "f32"
     gbs = nbytes / (ms / 1e3) / 1e9
     line = {"metric": "u projection tokens/s (normalize(W_u k_raw))", "value": n / (ms / 1e3), "unit": "tokens/s",
-            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "n_gpus": 1, "steps": calls, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": dt, "data": "synthetic",
             "config": {"workload": w.name, "tokens": n, "d": w.d, "r": w.r, "io": w.io, "op": "project_u",
                        "l2": "keys and directions 2 x %.0f MB > 129 MB L2 (no flush)" % (n * w.d * k.element_size() / 1e6)},
@@ -458,7 +485,7 @@ def run_project_u(args, w):
                          "peak_how": "%s HBM copy bandwidth" % peaks["_source"],
                          "algorithmic_bytes": nbytes, "tflops": flops / (ms / 1e3) / 1e12,
                          "form": form},
-            "clocks": clk, "gpu_launches": args.steps}
+            "clocks": clk, "gpu_launches": calls}
     print(json.dumps(line), flush=True)
     h.close()
 
@@ -708,7 +735,7 @@ def main():
         v, cores, sample = oracle_leg(w, T_full)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
                                 **host_cpu_info()}
-        errs = sampled_pair_errors(h, w, T_full, list(modes), dev)
+        errs = sampled_pair_errors(h, w, T_full, list(modes), dev, pairs=(0, 1) if w.pairs > 1 else (0,))
         for m in modes:
             modes[m]["errors"] = {"pairs": errs["pairs"], "T": errs["T"], **errs[m]}
     if rank == 0:

@@ -1,8 +1,10 @@
 // Direction projection u_{t,i} = W_u[i] k_t / max(|W_u[i] k_t|_2, 1e-12) for sm_103a: the
 // README "VLA v3" item 2 "u_t = normalize(W_u k_t^raw)", computed before the scan (whose u
-// input it produces, [n, r, d]).  Three forms: tensor cores with bf16 operands (bfloat16
-// keys), tensor cores in tf32 (float32 keys whose operands fit in shared memory) and CUDA
-// cores (d = 128 with float32 keys).
+// input it produces, [n, r, d]).  Four forms: tensor cores with bf16 operands fed by TMA
+// (bfloat16 keys whose r weight sets fit in shared memory; vla_proj_tma.cu), the same
+// product with keys through registers (bfloat16 keys otherwise), tensor cores in tf32
+// (float32 keys whose operands fit in shared memory) and CUDA cores (d = 128 with float32
+// keys).
 //
 // CUDA-core form: each thread takes TPT consecutive tokens (4 at d = 16, 2 at d = 64, 1 at d = 128),
 // groups taken grid-stride, the ranks one after another (W_u[i] in shared memory, d x d
@@ -434,11 +436,21 @@ __global__ void __launch_bounds__(NTH) project_u_bf16_kernel(const __nv_bfloat16
   if (failed && tid == 0) atomicOr(&status->flags, kStatusTimeout);
 }
 
+// The TMA-fed bfloat16 form (vla_proj_tma.cu); *used = false when its operands do not fit.
+template <int D>
+cudaError_t launch_project_tma(const void* k, const float* W, void* u, long long n, int r, int sm_count,
+                               DevStatus* status, cudaStream_t s, bool* used);
+
 template <int D, typename TIO>
 cudaError_t launch_project_t(const void* k, const float* W, void* u, long long n, int r, int sm_count,
                              DevStatus* status, cudaStream_t s) {
   const int sms = sm_count > 0 ? sm_count : 1;
   if constexpr (sizeof(TIO) == 2) {   // bfloat16 keys: kind::f16 with bf16 operands
+    bool used = false;
+    cudaError_t et = launch_project_tma<D>(k, W, u, n, r, sms, status, s, &used);
+    if (used || et != cudaSuccess) return et;
+    // W's three terms for all r ranks beyond shared memory (d = 128 with r > 1, d = 64 with
+    // r > 4): one tile and one rank at a time, keys through registers
     auto kern = project_u_bf16_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Bf16Cfg<D>::bytes);
     if (e != cudaSuccess) return e;

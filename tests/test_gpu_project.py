@@ -119,10 +119,11 @@ def test_projection_grid_stride_covers_every_token():
 @pytest.mark.parametrize("d", [16, 64, 128])
 @pytest.mark.parametrize("r", [1, 4])
 def test_bf16_projection_several_tiles_per_cta(d, r):
-    """bfloat16 keys with more tiles than the grid has CTAs (the grid is 8 CTAs of 128 tokens
-    per SM): every CTA runs its main loop (key rows loaded two tiles ahead) over at least two
-    tiles, and the last tile is ragged.  The outputs are compared on a sample of tokens: the
-    first and last tiles, the second and third tile of the first CTAs, and random ones."""
+    """bfloat16 keys with many tiles per CTA: the TMA form's persistent grid (one CTA per SM)
+    cycles its key stages and both accumulators many times, the register form (d = 128,
+    r = 4: 8 CTAs of 128 tokens per SM) runs its main loop over at least two tiles, and the
+    last tile is ragged.  The outputs are compared on a sample of tokens: the first and last
+    tiles, the second and third tile of the first CTAs, and random ones."""
     import sherman_morrison_inverse_gb300 as vla
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     grid = 8 * sms
@@ -140,3 +141,25 @@ def test_bf16_projection_several_tiles_per_cta(d, r):
     got = u[torch.from_numpy(idx)].double().numpy()
     ref = _ref(k[torch.from_numpy(idx)].double().numpy(), W.double().numpy(), torch.bfloat16)
     _check(got, ref, torch.bfloat16)
+
+
+@pytest.mark.parametrize("d,r,n", [(64, 1, 1), (64, 1, 127), (64, 1, 128), (64, 2, 129), (64, 3, 5000),
+                                   (64, 4, 300), (64, 5, 200), (16, 1, 40), (16, 3, 1000), (16, 5, 777),
+                                   (16, 8, 129), (128, 1, 1000), (128, 2, 300), (128, 3, 130)])
+def test_bf16_projection_every_rank_count_and_no_write_past_the_end(d, r, n):
+    """bfloat16 keys for rank counts 1..8: the r weight sets stacked into one product of
+    N = r d columns (d = 16 up to N = 128, d = 64 up to r = 4), and beyond what shared memory
+    holds (d = 64 with r = 5, d = 128 with r > 1) the one-rank-at-a-time form; n below, at and
+    just past one 128-token tile.  Output rows past n in the caller's buffer keep their
+    contents (the tensor stores clip the ragged last tile)."""
+    import sherman_morrison_inverse_gb300 as vla
+    g = np.random.default_rng([d, r, n, 11])
+    k = torch.from_numpy(g.normal(size=(n, d)).astype(np.float32)).to(torch.bfloat16)
+    W = torch.from_numpy(g.normal(size=(r, d, d)) / np.sqrt(d)).float()
+    sentinel = 7.0
+    ubuf = torch.full((n + 130, r, d), sentinel, dtype=torch.bfloat16, device="cuda")
+    u = ubuf[:n]
+    vla.project_u(k.cuda(), W.cuda(), u)
+    host = ubuf.cpu()
+    assert torch.all(host[n:] == sentinel), "rows past n were written"
+    _check(host[:n].double().numpy(), _ref(k.double().numpy(), W.double().numpy(), torch.bfloat16), torch.bfloat16)
