@@ -412,6 +412,19 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
+def ctas_label(mode: str, d: int, chunk: int, pairs: int, sms: int) -> str:
+    """How the library places one (b, h) pair: the sequential and delta modes take `chunk`
+    CTAs per pair (0: a two-CTA cluster at d = 128 while 2 B H CTAs fit on the SMs)."""
+    if mode == "chunked":
+        return "one CTA per (b,h) pair"
+    ctas = chunk if (mode == "sequential" and chunk) else (2 if d == 128 and 2 * pairs <= sms else 1)
+    if ctas == 1:
+        return "one CTA per (b,h) pair"
+    if ctas == 2:
+        return "a two-CTA cluster per (b,h) pair (A and S on separate SMs)"
+    return f"a cluster of {ctas} CTAs per (b,h) pair (rows of A and columns of S split)"
+
+
 def proj_tma_fits(d: int, r: int) -> bool:
     """Whether vla_project_u takes its TMA-fed bf16 form: the key ring, the staging tiles and
     W's three bf16 terms for all r ranks fit in one CTA's 227 KB of shared memory."""
@@ -712,7 +725,7 @@ def main():
                                  if args.mode == "chunked" else "fp32 CUDA-core arithmetic"),
                    "rule": "delta (gist.science summary §2.3)" if args.mode == "delta" else "additive",
                    "l2": f"inputs {bytes_step / 1e9:.2f} GB per step > 129 MB L2 (no flush)",
-                   "parallelism": f"replicas x{world}, one CTA per (b,h) pair"},
+                   "parallelism": f"replicas x{world}, {ctas_label(args.mode, w.d, args.chunk, B * H, sm_count(dev))}"},
         "roofline": roofline,
         "modes": modes,
         "fp32_probe": probe,

@@ -123,6 +123,11 @@ vla_err_t vla_create(vla_handle_t* h, int device);
  *             tracking A, the other S (the same arithmetic and the same results
  *             bit for bit, except at d == 128, r == 1, where the cluster takes 4
  *             steps per reduction round and one CTA 2: equal up to rounding);
+ *             4 or 8 (d in {64, 128}, r == 1) = a cluster of that many CTAs, each
+ *             holding d/4 or d/8 rows of A and the same columns of S, exchanging
+ *             partial sums every step (the step-by-step recurrence; slower than
+ *             1 or 2 on the built workloads, since every step waits for a
+ *             cross-SM exchange; at most 8 clusters of 8 run at once);
  *             0 = two for d == 128 while 2 B H CTAs fit on the device's SMs, else
  *             one.
  *   stream    cudaStream_t as void*.

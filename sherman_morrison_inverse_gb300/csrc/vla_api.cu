@@ -15,7 +15,11 @@ cudaError_t launch_seq_block_d16(int r, bool bf16, bool cluster, const ScanArgs&
 cudaError_t launch_seq_block_d64(int r, bool bf16, bool cluster, const ScanArgs& a, cudaStream_t s, bool* built);
 cudaError_t launch_seq_block_d128(int r, bool bf16, bool cluster, const ScanArgs& a, cudaStream_t s, bool* built);
 
+// the row-split scan on a cluster of `ctas` (4 or 8) CTAs per pair (vla_rows.cu)
+cudaError_t launch_rows(int d, int r, bool bf16, int ctas, const ScanArgs& a, cudaStream_t s, bool* built);
+
 cudaError_t launch_seq(int d, int r, bool bf16, int ctas, const ScanArgs& a, cudaStream_t s, bool* built) {
+  if (ctas == 4 || ctas == 8) return launch_rows(d, r, bf16, ctas, a, s, built);
   const bool cluster = ctas == 2;
   switch (d) {
     case 16: return launch_seq_block_d16(r, bf16, cluster, a, s, built);
@@ -90,7 +94,8 @@ size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 bool shape_built(int d, int dv, int r, bool bf16, vla_mode_t mode, int chunk, int ctas) {
   if (d != dv || (d != 16 && d != 64 && d != 128) || (r != 1 && r != 4)) return false;
   switch (mode) {
-    case VLA_SEQUENTIAL: return ctas == 1 || ctas == 2;
+    case VLA_SEQUENTIAL:
+      return ctas == 1 || ctas == 2 || ((ctas == 4 || ctas == 8) && r == 1 && (d == 64 || d == 128));
     case VLA_DELTA: return chunk == 0;
     case VLA_CHUNKED:
       return d == 64 && bf16 && ((r == 1 && (chunk == 0 || chunk == 64)) || (r == 4 && (chunk == 0 || chunk == 16)));
@@ -126,7 +131,8 @@ vla_err_t check_scan(vla_handle_t h, const char* fn, int B, int H, long long T, 
     char buf[400];
     std::snprintf(buf, sizeof buf,
                   "%s: not built for d=%d dv=%d r=%d dtype=%s mode=%s chunk=%d "
-                  "(sequential: d=dv in {16,64,128}, r in {1,4}, chunk = CTAs per pair 1 or 2, 0 = default; "
+                  "(sequential: d=dv in {16,64,128}, r in {1,4}, chunk = CTAs per pair 1 or 2, 0 = default, "
+                  "or 4 / 8 (rows of A split) at d in {64,128} with r = 1; "
                   "chunked: d=dv=64, bf16, r=1 chunk 64 or r=4 chunk 16, 0 = default; "
                   "delta: d=dv in {16,64,128}, r in {1,4}, chunk 0)",
                   fn, d, dv, r, bf16 ? "bf16" : "f32",

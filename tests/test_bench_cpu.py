@@ -129,3 +129,12 @@ def test_no_function_shadows_a_module_function_it_calls():
         called = {n.func.id for n in ast.walk(fn) if isinstance(n, ast.Call) and isinstance(n.func, ast.Name)}
         clash = stored & called & module_funcs
         assert not clash, (fn.name, clash)
+
+
+def test_ctas_label_names_the_placement_the_library_takes():
+    assert bench.ctas_label("chunked", 64, 0, 128, 152) == "one CTA per (b,h) pair"
+    assert bench.ctas_label("sequential", 64, 0, 32, 152) == "one CTA per (b,h) pair"
+    assert "two-CTA cluster" in bench.ctas_label("sequential", 128, 0, 16, 152)
+    assert bench.ctas_label("sequential", 128, 0, 128, 152) == "one CTA per (b,h) pair"   # 256 > 152 SMs
+    assert "two-CTA cluster" in bench.ctas_label("delta", 128, 0, 16, 152)
+    assert "cluster of 4 CTAs" in bench.ctas_label("sequential", 128, 4, 16, 152)
