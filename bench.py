@@ -77,6 +77,7 @@ KERNEL_SOURCES = {
     "delta": ["vla_seqk.cuh", "vla_internal.cuh", "vla_seqk_delta_d16.cu", "vla_seqk_delta_d64.cu",
               "vla_seqk_delta_d128.cu", "vla_delta.cu"],
     "chunked": ["vla_chunk.cuh", "vla_tc.cuh", "vla_internal.cuh", "vla_chunked.cu"],
+    "project_u": ["vla_proj_tma.cu", "vla_tc.cuh", "vla_internal.cuh"],
 }
 
 
@@ -98,7 +99,10 @@ TRAFFIC = {
     ("b8h16_t16384_d64_bf16_recall", "sequential"): (325.31e6 * 4, 4096, "2d1fb8f16cca4b57"),
     ("b8h16_t16384_d64_bf16_recall", "delta"): (325.57e6 * 4, 4096, "4c6f6c798db6d4c6"),
     ("b8h16_t16384_d64_bf16_recall", "chunked"): (156.07e6 * 8, 2048, "535f9a882610171f"),
-    ("b16h16_t8192_d64_bf16_r4", "chunked"): (274.16e6 * 8, 1024, "3c99f484200b99c1"),
+    ("b16h16_t8192_d64_bf16_r4", "chunked"): (274.26e6 * 8, 1024, "535f9a882610171f"),
+    # the u projection's TMA form (whole workload captured)
+    ("b8h16_t16384_d64_bf16_recall", "project_u"): (483.25e6, 16384, "45a13c3d7a59a6b1"),
+    ("b16h16_t8192_d64_bf16_r4", "project_u"): (1281.11e6, 8192, "45a13c3d7a59a6b1"),
 }
 
 
@@ -426,11 +430,12 @@ def ctas_label(mode: str, d: int, chunk: int, pairs: int, sms: int) -> str:
 
 
 def proj_tma_fits(d: int, r: int) -> bool:
-    """Whether vla_project_u takes its TMA-fed bf16 form: the key ring, the staging tiles and
-    W's three bf16 terms for all r ranks fit in one CTA's 227 KB of shared memory."""
+    """Whether vla_project_u takes its TMA-fed bf16 form: a key ring of at least two stages,
+    the staging tiles and W's three bf16 terms for all r ranks fit in one CTA's 227 KB of
+    shared memory."""
     bx = min(d, 64)
     slab = 128 * bx * 2
-    ks = 2 if d == 128 else 3
+    ks = 2
     nbytes = ks * (d // bx) * slab + 4 * slab + 3 * r * d * d * 2
     return (nbytes + 15) // 16 * 16 + 8 * (2 * ks + 5) + 16 <= 227 * 1024
 
@@ -488,13 +493,17 @@ def run_project_u(args, w):
     else:
         form, dt = "CUDA cores, float32", "f32"
     gbs = nbytes / (ms / 1e3) / 1e9
+    if w.io == "bf16" and proj_tma_fits(w.d, w.r):
+        traffic, traffic_how = traffic_record(w.name, "project_u", w.T, w.T)
+    else:
+        traffic, traffic_how = None, "no ncu capture of this form on this workload"
     line = {"metric": "u projection tokens/s (normalize(W_u k_raw))", "value": n / (ms / 1e3), "unit": "tokens/s",
             "n_gpus": 1, "steps": calls, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": dt, "data": "synthetic",
             "config": {"workload": w.name, "tokens": n, "d": w.d, "r": w.r, "io": w.io, "op": "project_u",
                        "l2": "keys and directions 2 x %.0f MB > 129 MB L2 (no flush)" % (n * w.d * k.element_size() / 1e6)},
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
-                         "frac": gbs / float(peaks["hbm_gbs"]), "traffic": None,
+                         "frac": gbs / float(peaks["hbm_gbs"]), "traffic": traffic, "traffic_how": traffic_how,
                          "peak_how": "%s HBM copy bandwidth" % peaks["_source"],
                          "algorithmic_bytes": nbytes, "tflops": flops / (ms / 1e3) / 1e12,
                          "form": form},

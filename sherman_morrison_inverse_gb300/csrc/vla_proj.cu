@@ -450,7 +450,7 @@ cudaError_t launch_project_t(const void* k, const float* W, void* u, long long n
     cudaError_t et = launch_project_tma<D>(k, W, u, n, r, sms, status, s, &used);
     if (used || et != cudaSuccess) return et;
     // W's three terms for all r ranks beyond shared memory (d = 128 with r > 1, d = 64 with
-    // r > 4): one tile and one rank at a time, keys through registers
+    // r > 5): one tile and one rank at a time, keys through registers
     auto kern = project_u_bf16_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Bf16Cfg<D>::bytes);
     if (e != cudaSuccess) return e;

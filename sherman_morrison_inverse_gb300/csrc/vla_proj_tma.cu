@@ -6,10 +6,11 @@
 // Roles, by warp:
 //   warp 0 (one thread)  producer: each key tile [128][d] bf16 arrives with one TMA tensor
 //                        load per 64-column slab (128-byte swizzle; 32-byte at d = 16) into a
-//                        ring of KS stages, completing on the stage's `full` mbarrier;
+//                        ring of `ks` stages (as many as shared memory holds beside W and the
+//                        staging tiles, up to 8), completing on the stage's `full` mbarrier;
 //   warp 1               allocates tensor memory; one thread issues the products: all ranks
-//                        of a tile, stacked, as one x = K W^T of N = r d columns (two rank
-//                        groups at d = 128, r = 2), so every key is read from HBM once.  K is
+//                        of a tile, stacked, as one x = K W^T of N = r d columns (groups of
+//                        256 / d ranks when r d > 256), so every key is read from HBM once.  K is
 //                        read straight from the swizzled stage, W (three bf16 terms w1 + w2 + w3
 //                        of the float32 weights, three passes, fp32 accumulation) from shared
 //                        memory.  Jobs alternate between two TMEM accumulators;
@@ -40,16 +41,24 @@ struct TmaCfg {
   static constexpr int NSLAB = D / BX;                      // slabs per row: 1, or 2 at d = 128
   static constexpr int SLAB = kRows * BX * 2;               // bytes of one [128][BX] bf16 slab
   static constexpr int KEY = NSLAB * SLAB;                  // bytes of one key tile
-  static constexpr int KS = D == 128 ? 2 : 3;               // key stages
+  static constexpr int KMAX = 8;                            // key stages at most
   static constexpr int NSU = 2;                             // staging slabs per epilogue group
   static constexpr int GMAX = 256 / D;                      // ranks per product (N <= 256)
-  static constexpr int OFF_STG = KS * KEY;                  // after the key ring
-  static constexpr int OFF_W = OFF_STG + 2 * NSU * SLAB;    // three W terms, [r d][d] bf16 each
   static constexpr uint32_t SW_MODE = BX == 64 ? 2u : 6u;   // descriptor swizzle: 128 B / 32 B
   static constexpr uint32_t SW_SBO = 8u * BX * 2u;          // bytes between 8-row groups
+  // shared memory: the key ring (ks stages) | staging (2 groups x NSU slabs) | three W terms
+  // ([r d][d] bf16 each) | mbarriers (2 ks + 5) | TMEM slot and failure flag
+  __host__ __device__ static size_t off_stg(int ks) { return (size_t)ks * KEY; }
+  __host__ __device__ static size_t off_w(int ks) { return off_stg(ks) + (size_t)2 * NSU * SLAB; }
   __host__ __device__ static size_t w_bytes(int r) { return (size_t)3 * r * D * D * 2; }
-  __host__ __device__ static size_t bar_off(int r) { return (OFF_W + w_bytes(r) + 15) / 16 * 16; }
-  __host__ __device__ static size_t bytes(int r) { return bar_off(r) + 8 * (2 * KS + 5) + 16; }
+  __host__ __device__ static size_t bar_off(int r, int ks) { return (off_w(ks) + w_bytes(r) + 15) / 16 * 16; }
+  __host__ __device__ static size_t bytes(int r, int ks) { return bar_off(r, ks) + 8 * (2 * ks + 5) + 16; }
+  // the most key stages (<= KMAX) that fit in `limit` bytes beside the rest; 0 if fewer than 2
+  static int stages(int r, size_t limit) {
+    for (int ks = KMAX; ks >= 2; --ks)
+      if (bytes(r, ks) <= limit) return ks;
+    return 0;
+  }
 };
 
 // K-major operand of 16-bit elements in the swizzled layout a TMA tiled load writes: rows of
@@ -140,10 +149,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 template <int D>
 __global__ void __launch_bounds__(kTmaThreads, 1)
     project_u_tma_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_u,
-                         const float* __restrict__ W, long long n, int r, uint32_t tmem_cols,
+                         const float* __restrict__ W, long long n, int r, int ks, uint32_t tmem_cols,
                          DevStatus* __restrict__ status) {
   using Cf = TmaCfg<D>;
-  constexpr int KS = Cf::KS, BX = Cf::BX, NSLAB = Cf::NSLAB;
+  constexpr int BX = Cf::BX, NSLAB = Cf::NSLAB;
   extern __shared__ __align__(1024) unsigned char smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // the swizzled stages need 1024-byte alignment; report rather than run misaligned
@@ -151,10 +160,11 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     if (tid == 0) atomicOr(&status->flags, kStatusTimeout);
     return;
   }
-  const size_t boff = Cf::bar_off(r);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + boff);   // [KS] key stage loaded
-  uint64_t* empty = full + KS;                                  // [KS] key stage consumed
-  uint64_t* tfull = empty + KS;                                 // [2] accumulator written
+  const size_t boff = Cf::bar_off(r, ks);
+  const size_t off_w = Cf::off_w(ks), off_stg = Cf::off_stg(ks);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + boff);   // [ks] key stage loaded
+  uint64_t* empty = full + ks;                                  // [ks] key stage consumed
+  uint64_t* tfull = empty + ks;                                 // [2] accumulator written
   uint64_t* tempty = tfull + 2;                                 // [2] accumulator drained
   uint64_t* done = tempty + 2;                                  // every product issued has completed
   uint32_t* tslot = reinterpret_cast<uint32_t*>(done + 1);
@@ -185,13 +195,13 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
           x[2 * q] -= t0;       // exact: t is x rounded to 8 significant bits
           x[2 * q + 1] -= t1;
         }
-        *reinterpret_cast<uint4*>(smem + Cf::OFF_W + (size_t)term * rows * D * 2 + 2 * tc::tk16_off(row, m, D)) =
+        *reinterpret_cast<uint4*>(smem + off_w + (size_t)term * rows * D * 2 + 2 * tc::tk16_off(row, m, D)) =
             make_uint4(p[0], p[1], p[2], p[3]);
       }
     }
   }
   if (tid == 0) {
-    for (int s = 0; s < KS; ++s) {
+    for (int s = 0; s < ks; ++s) {
       mbar_init(full + s, 1);
       mbar_init(empty + s, 1);
     }
@@ -215,18 +225,19 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     // ---------------- producer
     if (lane == 0) {
       long long lt = 0;
+      int s = 0;          // stage of tile lt
+      uint32_t k = 0;     // use of that stage
       for (; lt < nlt && !*fail; ++lt) {
-        const int s = (int)(lt % KS);
-        const long long k = lt / KS;
-        if (k > 0 && !mbar_wait_bounded(empty + s, (uint32_t)((k - 1) & 1))) { *fail = 1; break; }
+        if (k > 0 && !mbar_wait_bounded(empty + s, (k - 1) & 1u)) { *fail = 1; break; }
         const int y = (int)((blockIdx.x + lt * gridDim.x) * kRows);
         mbar_arrive_expect_tx(full + s, (uint32_t)Cf::KEY);
 #pragma unroll
         for (int sl = 0; sl < NSLAB; ++sl) tma_load_2d(smem + s * Cf::KEY + sl * Cf::SLAB, &map_k, sl * BX, y, full + s);
+        if (++s == ks) { s = 0; ++k; }
       }
       // the last load of each stage has landed before the CTA can leave (bounded)
-      for (long long j = (lt > KS ? lt - KS : 0); j < lt; ++j)
-        if (!mbar_wait_bounded(full + (int)(j % KS), (uint32_t)((j / KS) & 1))) *fail = 1;
+      for (long long j = (lt > ks ? lt - ks : 0); j < lt; ++j)
+        if (!mbar_wait_bounded(full + (int)(j % ks), (uint32_t)((j / ks) & 1))) *fail = 1;
     }
   } else if (warp == 1) {
     // ---------------- products
@@ -234,11 +245,10 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       const uint32_t idesc_full = tc::idesc_bf16(128, G * D);
       const uint32_t sbase = smem_u32(smem);
       const size_t term_bytes = (size_t)r * D * D * 2;
+      int s = 0, g = 0;   // stage of the current tile, rank group of the current job
+      uint32_t k = 0;     // use of that stage
       for (long long jl = 0; jl < njobs && !*fail; ++jl) {
-        const long long lt = jl / ngroups;
-        const int g = (int)(jl - lt * ngroups);
-        const int s = (int)(lt % KS);
-        if (g == 0 && !mbar_wait_bounded(full + s, (uint32_t)((lt / KS) & 1))) { *fail = 1; break; }
+        if (g == 0 && !mbar_wait_bounded(full + s, k & 1u)) { *fail = 1; break; }
         const int b = (int)(jl & 1);
         const long long use = jl >> 1;
         if (use > 0 && !mbar_wait_bounded(tempty + b, (uint32_t)((use - 1) & 1))) { *fail = 1; break; }
@@ -247,7 +257,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         const uint32_t idesc = ng == G ? idesc_full : tc::idesc_bf16(128, ng * D);
         const uint32_t d_tmem = tmem + (uint32_t)b * bufcols;
         const uint32_t kbase = sbase + (uint32_t)(s * Cf::KEY);
-        const uint32_t wbase = sbase + (uint32_t)Cf::OFF_W + (uint32_t)(i0 * D * D * 2);
+        const uint32_t wbase = sbase + (uint32_t)off_w + (uint32_t)(i0 * D * D * 2);
 #pragma unroll
         for (int p = 0; p < 3; ++p)
 #pragma unroll
@@ -257,7 +267,13 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
                         tc::sdesc(wbase + (uint32_t)(p * term_bytes) + 256u * kk, 16u * D), idesc, p > 0 || kk > 0);
           }
         tc::mma_commit(tfull + b);
-        if (g == ngroups - 1) tc::mma_commit(empty + s);   // the stage's last reader
+        if (g == ngroups - 1) {
+          tc::mma_commit(empty + s);   // the stage's last reader
+          g = 0;
+          if (++s == ks) { s = 0; ++k; }
+        } else {
+          ++g;
+        }
       }
       tc::mma_commit(done);
       if (!mbar_wait_bounded(done, 0)) *fail = 1;
@@ -270,7 +286,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     const bool issuer = (warp == 2 + 4 * eg) && lane == 0;
     const int bar_id = 1 + eg;
     const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)eg * bufcols;
-    unsigned char* stg0 = smem + Cf::OFF_STG + eg * Cf::NSU * Cf::SLAB;
+    unsigned char* stg0 = smem + off_stg + eg * Cf::NSU * Cf::SLAB;
     const int swz = BX == 64 ? (row & 7) : ((row >> 2) & 1);
     long long unit = 0;
     for (long long jl = eg; jl < njobs; jl += 2) {
@@ -370,8 +386,9 @@ cudaError_t launch_project_tma(const void* k, const float* W, void* u, long long
                                DevStatus* status, cudaStream_t s, bool* used) {
   using Cf = TmaCfg<D>;
   *used = false;
-  const size_t bytes = Cf::bytes(r);
-  if (bytes > 227 * 1024 || n <= 0 || n >= (1ll << 31) - kRows) return cudaSuccess;
+  const int ks = Cf::stages(r, 227 * 1024);
+  if (ks < 2 || n <= 0 || n >= (1ll << 31) - kRows) return cudaSuccess;
+  const size_t bytes = Cf::bytes(r, ks);
   CUtensorMap mk, mu;
   if (!encode_2d(&mk, k, n, D, Cf::BX, Cf::BX == 64) || !encode_2d(&mu, u, n, (long long)r * D, Cf::BX, Cf::BX == 64))
     return cudaSuccess;
@@ -384,7 +401,7 @@ cudaError_t launch_project_tma(const void* k, const float* W, void* u, long long
   const long long ntiles = (n + kRows - 1) / kRows;
   const int grid = (int)(ntiles < sm_count ? ntiles : (sm_count > 0 ? sm_count : 1));
   *used = true;
-  kern<<<grid, kTmaThreads, bytes, s>>>(mk, mu, W, n, r, cols, status);
+  kern<<<grid, kTmaThreads, bytes, s>>>(mk, mu, W, n, r, ks, cols, status);
   return cudaGetLastError();
 }
 

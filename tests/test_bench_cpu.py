@@ -58,10 +58,16 @@ def test_reference_arm_prints_one_contract_line():
 def test_traffic_records_are_tied_to_their_kernel_source():
     for (name, mode), (traffic, t_cap, src) in bench.TRAFFIC.items():
         w = workloads.get(name)
-        assert w.name == name and mode in bench.MODE_DTYPE and mode in bench.KERNEL_SOURCES
+        assert w.name == name and mode in bench.KERNEL_SOURCES
         assert len(src) == 16 and int(src, 16) >= 0 and w.T % t_cap == 0
-        # a capture's DRAM traffic is at least the bytes the launch must stream
-        assert traffic >= 0.9 * w.pairs * w.T * bench.streamed_bytes_per_token_head(w)
+        # a capture's DRAM traffic is close to the bytes the launch must stream at least (the
+        # last writes may still be in L2 when the kernel ends)
+        if mode == "project_u":   # keys in, r directions out, bf16
+            assert bench.proj_tma_fits(w.d, w.r)
+            assert traffic >= 0.85 * w.pairs * w.T * (w.d + w.r * w.d) * 2
+        else:
+            assert mode in bench.MODE_DTYPE
+            assert traffic >= 0.9 * w.pairs * w.T * bench.streamed_bytes_per_token_head(w)
         got, how = bench.traffic_record(name, mode, w.T, w.T)
         if src == bench.kernel_source_hash(mode):
             assert got == traffic and "ncu" in how

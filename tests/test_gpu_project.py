@@ -144,14 +144,16 @@ def test_bf16_projection_several_tiles_per_cta(d, r):
 
 
 @pytest.mark.parametrize("d,r,n", [(64, 1, 1), (64, 1, 127), (64, 1, 128), (64, 2, 129), (64, 3, 5000),
-                                   (64, 4, 300), (64, 5, 200), (16, 1, 40), (16, 3, 1000), (16, 5, 777),
-                                   (16, 8, 129), (128, 1, 1000), (128, 2, 300), (128, 3, 130)])
+                                   (64, 4, 300), (64, 5, 200), (64, 5, 40000), (64, 8, 150), (16, 1, 40),
+                                   (16, 3, 1000), (16, 5, 777), (16, 8, 129), (128, 1, 1000), (128, 2, 300),
+                                   (128, 3, 130)])
 def test_bf16_projection_every_rank_count_and_no_write_past_the_end(d, r, n):
     """bfloat16 keys for rank counts 1..8: the r weight sets stacked into one product of
-    N = r d columns (d = 16 up to N = 128, d = 64 up to r = 4), and beyond what shared memory
-    holds (d = 64 with r = 5, d = 128 with r > 1) the one-rank-at-a-time form; n below, at and
-    just past one 128-token tile.  Output rows past n in the caller's buffer keep their
-    contents (the tensor stores clip the ragged last tile)."""
+    N = r d columns (d = 16 up to N = 128, d = 64 up to r = 4), two rank groups on one key
+    tile (d = 64, r = 5: N = 256 and 64), and beyond what shared memory holds (d = 64 with
+    r = 8, d = 128 with r > 1) the one-rank-at-a-time form; n below, at and just past one
+    128-token tile, and many tiles per CTA.  Output rows past n in the caller's buffer keep
+    their contents (the tensor stores clip the ragged last tile)."""
     import sherman_morrison_inverse_gb300 as vla
     g = np.random.default_rng([d, r, n, 11])
     k = torch.from_numpy(g.normal(size=(n, d)).astype(np.float32)).to(torch.bfloat16)
