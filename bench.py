@@ -416,6 +416,48 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
+def measure_host_link(dev, nbytes: int = 256 << 20, reps: int = 3) -> dict:
+    """The host <-> device link of this GPU: page-locked buffers of `nbytes` copied with
+    cudaMemcpyAsync host to device, device to host, and both at once on two streams (best of
+    `reps`).  The end-to-end leg's bytes over these rates bound its time from below."""
+    h_src = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    h_dst = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d_src = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+    d_dst = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def run(h2d: bool, d2h: bool) -> float:
+        best = float("inf")
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            e0.record(s1)
+            s2.wait_event(e0)
+            if h2d:
+                with torch.cuda.stream(s1):
+                    d_dst.copy_(h_src, non_blocking=True)
+            if d2h:
+                with torch.cuda.stream(s2):
+                    h_dst.copy_(d_src, non_blocking=True)
+            s1.wait_stream(s2)
+            e1.record(s1)
+            torch.cuda.synchronize(dev)
+            best = min(best, e0.elapsed_time(e1))
+        return best
+
+    t_in, t_out, t_both = run(True, False), run(False, True), run(True, True)
+    gb = nbytes / 1e9
+    return {"h2d_gbs": gb / (t_in / 1e3), "d2h_gbs": gb / (t_out / 1e3), "both_gbs": 2 * gb / (t_both / 1e3),
+            "bytes": nbytes, "how": "cudaMemcpyAsync of page-locked buffers: host to device, device to host, "
+                                    "and both at once on two streams (best of %d)" % reps}
+
+
+def link_bound_ms(h2d: int, d2h: int, link: dict) -> float:
+    """Least time the link allows for moving h2d bytes in and d2h bytes out."""
+    return 1e3 * max((h2d + d2h) / (link["both_gbs"] * 1e9), h2d / (link["h2d_gbs"] * 1e9),
+                     d2h / (link["d2h_gbs"] * 1e9))
+
+
 def ctas_label(mode: str, d: int, chunk: int, pairs: int, sms: int) -> str:
     """How the library places one (b, h) pair: the sequential and delta modes take `chunk`
     CTAs per pair (0: a two-CTA cluster at d = 128 while 2 B H CTAs fit on the SMs)."""
@@ -662,6 +704,8 @@ def main():
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
     e2e_value = job_value(B * H * T * e2e_steps, world, e2e_ms)
     st_e2e = h.status()
+    link = measure_host_link(dev)
+    link_ms = link_bound_ms(h2d, d2h, link)
 
     # ---- the other kernel on the same workload: the sequential fp32 CUDA-core scan beside
     # the chunked tensor-core one (timed the same way, after the headline legs)
@@ -745,7 +789,8 @@ def main():
                 "api": "scan_fwd_host: windows of the sequence copied in, scanned and copied out "
                        "in a pipeline", "seg": host_info["seg"],
                 "copy_in": "SM gather from mapped page-locked memory" if host_info["gathered"] == 1
-                           else "copy engines (cudaMemcpy2DAsync)"},
+                           else "copy engines (cudaMemcpy2DAsync)",
+                "link": link, "link_bound_ms": link_ms, "link_frac": link_ms / (e2e_ms / e2e_steps)},
         "status": {"warmup": st_warm, "timed": st, "e2e": st_e2e},
     }
     if args.trace > 0 and rank == 0:

@@ -144,3 +144,12 @@ def test_ctas_label_names_the_placement_the_library_takes():
     assert bench.ctas_label("sequential", 128, 0, 128, 152) == "one CTA per (b,h) pair"   # 256 > 152 SMs
     assert "two-CTA cluster" in bench.ctas_label("delta", 128, 0, 16, 152)
     assert "cluster of 4 CTAs" in bench.ctas_label("sequential", 128, 4, 16, 152)
+
+
+def test_link_bound_takes_the_tightest_of_the_three_rates():
+    # a link shared by both directions: the sum of the bytes over the shared rate binds
+    shared = {"h2d_gbs": 200.0, "d2h_gbs": 200.0, "both_gbs": 200.0}
+    assert bench.link_bound_ms(2e9, 1e9, shared) == 1e3 * 3e9 / 200e9
+    # independent directions: the larger direction binds
+    duplex = {"h2d_gbs": 200.0, "d2h_gbs": 100.0, "both_gbs": 300.0}
+    assert bench.link_bound_ms(2e9, 1e9, duplex) == 1e3 * max(3e9 / 300e9, 2e9 / 200e9, 1e9 / 100e9)
