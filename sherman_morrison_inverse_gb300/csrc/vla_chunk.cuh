@@ -338,6 +338,26 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     return x;
   };
 
+  // One warp: |alpha_t|^2 -> M_AN and the test ||S|| + sum_t |v_t| |alpha_t| <= tau (with a
+  // relative margin for the rounding of the bound) -> M_EX (0: no step of the chunk can renormalise).
+  // Reads the chunk length c of the chunk being run.
+  int c = 0;
+  auto bound_test = [&](float ns) {
+    float bsum = 0.f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int t = lane + 32 * h;
+      if (t < c) {
+        const float an = misc[Cf::M_AN2 + t] + misc[Cf::M_AN2 + 64 + t];
+        misc[Cf::M_AN + t] = an;
+        bsum = fmaf(misc[Cf::M_VN + t], sqrtf(fmaxf(an, 0.f)), bsum);
+      }
+    }
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) bsum += __shfl_xor_sync(0xffffffffu, bsum, m);
+    if (lane == 0) misc[Cf::M_EX] = (sqrtf(ns) + bsum <= a.tau * (1.f - 0x1p-12f)) ? 0.f : 1.f;
+  };
+
   long long pos = 0;
   // steps left until the next nudge (the global step t0 + pos + to_nudge is a multiple of P),
   // carried from chunk to chunk instead of a 64-bit remainder per chunk
@@ -354,7 +374,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     // ---------------- schedule: chunk [pos, pos + c) inside one input tile, ending at a nudge
     const int tile = (int)(pos / TS);
     const int ts = (int)(pos % TS);
-    int c = (int)min((long long)(TS - ts), T - pos);
+    c = (int)min((long long)(TS - ts), T - pos);
     bool nudge = false;
     if (a.P > 0) {
       if (to_nudge <= c) { c = (int)to_nudge; nudge = true; }
@@ -948,6 +968,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
 #pragma unroll
         for (int j = 0; j < 32; j += 4)
           st4(Cf::F_AL + tk_off(t, 32 * half + j, 64), al32[j], al32[j + 1], al32[j + 2], al32[j + 3]);
+        misc[Cf::M_AN2 + 64 * half + t] = an;   // |alpha_t|^2, two halves
       }
       // ---------------- G5: [S alpha ; S phi(q) | alpha.alpha ; phi(q).alpha] = [alpha; phi(q)] [S; alpha]^T,
       // issued as soon as alpha is written; the rest of G4's drain runs beside it
@@ -989,7 +1010,12 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
           for (int jj = 0; jj < 16; ++jj) sf[Cf::F_T6 + Cf::T6_A + tk_off(col0 + ((jj + g) & 15), t, C)] = al[jj];
         }
       }
-      if (row >= 64) misc[Cf::M_AN2 + 64 * half + (row - 64)] = an;   // |alpha_t|^2, two halves
+      // the renormalisation bound ||S|| + sum_t |v_t| |alpha_t| while G5 runs (one warp), when
+      // ||S||^2 is carried from the previous chunk's state update; |alpha_t|^2 -> M_AN
+      if (warp == 3 && misc[Cf::M_SSV] != 0.f) {
+        const float ns = (misc[Cf::M_SS] + misc[Cf::M_SS + 1]) + (misc[Cf::M_SS + 2] + misc[Cf::M_SS + 3]);
+        bound_test(ns);
+      }
       // V^T (rows i, K = t) for G6: lanes cover 8 rows x 4 steps of one core matrix
       for (int e = tid; e < 64 * C; e += NT) {
         const int i = ((e >> 5) & 7) * 8 + ((e >> 2) & 7), t = (e >> 8) * 4 + (e & 3);
@@ -1017,7 +1043,8 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     }
     // ||S||^2, the bound and the renormalisation decisions
     {
-      // ||S||^2: carried from the previous chunk's state update (M_SS), else recomputed
+      // ||S||^2: carried from the previous chunk's state update (M_SS; the bound was then tested
+      // beside G5), else recomputed here and the bound tested now
       float ns;
       if (misc[Cf::M_SSV] != 0.f) {
         ns = (misc[Cf::M_SS] + misc[Cf::M_SS + 1]) + (misc[Cf::M_SS + 2] + misc[Cf::M_SS + 3]);
@@ -1028,24 +1055,9 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
           sq = fmaf(x.x, x.x, fmaf(x.y, x.y, fmaf(x.z, x.z, fmaf(x.w, x.w, sq))));
         }
         ns = block_sum(sq);
+        if (warp == 0) bound_test(ns);
+        __syncthreads();
       }
-      // the bound ||S|| + sum_t |v_t| |alpha_t| (one warp), |alpha_t|^2 -> M_AN
-      if (warp == 0) {
-        float bsum = 0.f;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int t = lane + 32 * h;
-          if (t < c) {
-            const float an = misc[Cf::M_AN2 + t] + misc[Cf::M_AN2 + 64 + t];
-            misc[Cf::M_AN + t] = an;
-            bsum = fmaf(misc[Cf::M_VN + t], sqrtf(fmaxf(an, 0.f)), bsum);
-          }
-        }
-#pragma unroll
-        for (int m = 16; m >= 1; m >>= 1) bsum += __shfl_xor_sync(0xffffffffu, bsum, m);
-        if (lane == 0) misc[Cf::M_EX] = (sqrtf(ns) + bsum <= a.tau * (1.f - 0x1p-12f)) ? 0.f : 1.f;
-      }
-      __syncthreads();
       const bool exact = misc[Cf::M_EX] != 0.f;
       if (!exact) {
         if (tid < 64) {
