@@ -37,7 +37,8 @@
 //
 // Renormalisation: ||S_t||^2 = ||S||^2 + 2 sum v_t'^T S alpha_t' + sum (v.v)(alpha.alpha) from the
 // products above; the bound ||S|| + sum |v_t||alpha_t| (||S||^2 carried from the previous
-// chunk's state update) decides that no step can exceed tau, otherwise the exact per-step
+// chunk's state update; one warp tests it while G5 runs) decides that no step can exceed
+// tau, otherwise the exact per-step
 // norms give the decisions and the per-step scales are folded into tril(aq), alpha^T and
 // the outputs.  When the scales of one chunk fall below 2^-64 (tau far below the norm
 // each step adds), that chunk's S and outputs are taken step by step from its alpha instead.
