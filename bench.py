@@ -60,13 +60,17 @@ def streamed_bytes_per_token_head(w) -> int:
     return (2 * w.d + w.r * w.d + 2 * w.dv) * es
 
 
-def chunk_tensor_flops_per_token_head(r: int) -> float:
+def chunk_tensor_flops_per_token_head(r: int, f32: bool = False) -> float:
     """Tensor-core flops the chunked kernel executes per step of a pair (d = d_v = 64, 64
     directions a chunk, C = 64 / r steps): the 128 x 64 x 64 products G1 (2 passes), G2 (1),
-    G3 (3), G4 (3), G5 (128 x 128 x 64) and G6 (2 x 128 x 64 x C), each pass counted."""
+    G3 (3), G4 (3), G5 (128 x 128 x 64) and G6 (2 x 128 x 64 x C), each pass counted.  With
+    float32 I/O every product takes 3 passes (3xTF32)."""
     C = 64 // r
     base = 2.0 * 128 * 64 * 64
-    per_chunk = (2 + 1 + 3 + 3) * base + 2.0 * 128 * 128 * 64 + 2 * (2.0 * 128 * 64 * C)
+    if f32:
+        per_chunk = (3 + 3 + 3 + 3) * base + 3 * 2.0 * 128 * 128 * 64 + 3 * 2 * (2.0 * 128 * 64 * C)
+    else:
+        per_chunk = (2 + 1 + 3 + 3) * base + 2.0 * 128 * 128 * 64 + 2 * (2.0 * 128 * 64 * C)
     return per_chunk / C
 
 
@@ -619,7 +623,7 @@ def main():
 
     args.T_full = T_full
     if args.mode == "auto":
-        args.mode = "chunked" if (w.d == 64 and w.dv == 64 and w.io == "bf16" and w.r in (1, 4)) else "sequential"
+        args.mode = "chunked" if (w.d == 64 and w.dv == 64 and w.r in (1, 4)) else "sequential"
     if args.impl == "reference":
         run_reference(args, w)
         return
@@ -759,10 +763,10 @@ def main():
                 "sm_count": sms, "sm_ceiling": min(1.0, B * H / sms)}
     if args.mode == "chunked":
         tf32_peak = float(peaks["bf16_tflops"]) / 2.0
-        tfl = B * H * T * chunk_tensor_flops_per_token_head(w.r) / (ms_per_step / 1e3) / 1e12
+        tfl = B * H * T * chunk_tensor_flops_per_token_head(w.r, w.io == "f32") / (ms_per_step / 1e3) / 1e12
         roofline["tensor"] = {
             "bound": "tensor", "achieved": tfl, "peak": tf32_peak, "unit": "TFLOP/s", "frac": tfl / tf32_peak,
-            "flops_per_token_head": chunk_tensor_flops_per_token_head(w.r),
+            "flops_per_token_head": chunk_tensor_flops_per_token_head(w.r, w.io == "f32"),
             "counts": "every tcgen05 pass the kernel executes (a 3xTF32 product counts three times)",
             "peak_how": "%s bf16 burst (%.0f TFLOP/s) x 1/2, the nominal tf32:bf16 dense ratio" % (
                 peaks["_source"], float(peaks["bf16_tflops"]))}
@@ -774,7 +778,8 @@ def main():
         "config": {"workload": w.name, "B": B, "H": H, "T": T, "d": w.d, "dv": w.dv, "r": w.r,
                    "io": w.io, "state": "f32", "mode": args.mode, "P": w.P, "eps_n": w.eps_n, "tau": w.tau,
                    "tau_override": args.tau is not None,
-                   "precision": ("tcgen05 kind::tf32, 3xTF32 on the products that carry A; fp32 state"
+                   "precision": (("tcgen05 kind::tf32, 3xTF32 on every product; fp32 state" if w.io == "f32" else
+                                  "tcgen05 kind::tf32, 3xTF32 on the products that carry A; fp32 state")
                                  if args.mode == "chunked" else "fp32 CUDA-core arithmetic"),
                    "rule": "delta (gist.science summary §2.3)" if args.mode == "delta" else "additive",
                    "l2": f"inputs {bytes_step / 1e9:.2f} GB per step > 129 MB L2 (no flush)",

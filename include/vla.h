@@ -112,10 +112,12 @@ vla_err_t vla_create(vla_handle_t* h, int device);
  *             renormalisation has fired before the split (a call ends by folding
  *             its lazy scale into S); the same values up to rounding otherwise.
  *   io_dtype  VLA_F32 or VLA_BF16 for q, k, v, u and o; state is always float32.
- *   mode      VLA_SEQUENTIAL (every built shape) or VLA_CHUNKED (d == 64 only;
- *             `chunk` = steps per chunk, see the built list in the library's
- *             error message).  Both compute the same recurrence; they differ in
- *             rounding only.  VLA_DELTA computes the delta-rule variant (every
+ *   mode      VLA_SEQUENTIAL (every built shape) or VLA_CHUNKED (d == dv == 64,
+ *             r 1 or 4, bfloat16 or float32 I/O; `chunk` = steps per chunk, see the
+ *             built list in the library's error message; its products run on the
+ *             tensor cores in tf32, split into three passes (3xTF32) where they
+ *             carry A and, with float32 I/O, everywhere).  Both compute the same
+ *             recurrence; they differ in rounding only.  VLA_DELTA computes the delta-rule variant (every
  *             built shape; `chunk` must be 0).
  *   chunk     VLA_CHUNKED: steps per chunk (0 = the built default).
  *             VLA_SEQUENTIAL: CTAs per (batch, head) pair: 1 = one CTA holds

@@ -98,7 +98,7 @@ bool shape_built(int d, int dv, int r, bool bf16, vla_mode_t mode, int chunk, in
       return ctas == 1 || ctas == 2 || ((ctas == 4 || ctas == 8) && r == 1 && (d == 64 || d == 128));
     case VLA_DELTA: return chunk == 0;
     case VLA_CHUNKED:
-      return d == 64 && bf16 && ((r == 1 && (chunk == 0 || chunk == 64)) || (r == 4 && (chunk == 0 || chunk == 16)));
+      return d == 64 && ((r == 1 && (chunk == 0 || chunk == 64)) || (r == 4 && (chunk == 0 || chunk == 16)));
   }
   return false;
 }
@@ -133,7 +133,7 @@ vla_err_t check_scan(vla_handle_t h, const char* fn, int B, int H, long long T, 
                   "%s: not built for d=%d dv=%d r=%d dtype=%s mode=%s chunk=%d "
                   "(sequential: d=dv in {16,64,128}, r in {1,4}, chunk = CTAs per pair 1 or 2, 0 = default, "
                   "or 4 / 8 (rows of A split) at d in {64,128} with r = 1; "
-                  "chunked: d=dv=64, bf16, r=1 chunk 64 or r=4 chunk 16, 0 = default; "
+                  "chunked: d=dv=64, bf16 or f32, r=1 chunk 64 or r=4 chunk 16, 0 = default; "
                   "delta: d=dv in {16,64,128}, r in {1,4}, chunk 0)",
                   fn, d, dv, r, bf16 ? "bf16" : "f32",
                   mode == VLA_SEQUENTIAL ? "sequential" : mode == VLA_DELTA ? "delta" : "chunked", chunk);

@@ -76,6 +76,7 @@ constexpr int TC_G3 = 128;    // [Z; F^T]
 constexpr int TC_G4 = 192;    // [Z D^{-1} Z^T; (Z E)^T]
 constexpr int TC_G5 = 256;    // 128 columns: [S alpha, alpha.alpha; S phi(q), phi(q).alpha]; G6 adds tril(aq) V
 constexpr int TC_G6 = 384;    // V^T alpha
+constexpr int TC_XL = 448;    // float32 I/O: the low part of G1's accumulator, G2's X lo
 
 // High part of a 3xTF32 split: the value with the low 13 mantissa bits cleared
 // (exactly representable in tf32); the low part is x - hi.
@@ -98,6 +99,11 @@ __device__ __forceinline__ float rcp_approx(float x) {
   return r;
 }
 
+// bring [p, p + bytes) into L2 (16-byte aligned, a multiple of 16 bytes); nothing waits for it
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // named barriers (ids 1..5; 0 is __syncthreads): `n` threads take part, a multiple of 32
 __device__ __forceinline__ void bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 __device__ __forceinline__ void bar_arrive(int id, int n) {
@@ -106,11 +112,14 @@ __device__ __forceinline__ void bar_arrive(int id, int n) {
 
 template <int R, typename TIO>
 struct Cfg {
+  static constexpr bool F32 = sizeof(TIO) == 4;           // float32 I/O: 3xTF32 throughout, no raw stage
   static constexpr int C = 64 / R;                        // steps per chunk
   static constexpr int TS = C;                            // steps per input tile
   static constexpr uint32_t QB = TS * D * sizeof(TIO);
   static constexpr uint32_t UB = TS * R * D * sizeof(TIO);
-  static constexpr uint32_t STAGE = 3 * QB + UB;
+  // bfloat16: the tile of q, k, v, u lands in a raw stage by bulk copies; float32: the prologue
+  // reads it from global memory (prefetched into L2 a tile ahead), the stage would not fit
+  static constexpr uint32_t STAGE = F32 ? 0 : 3 * QB + UB;
   static constexpr uint32_t STAGE_PAD = (STAGE + 1023) / 1024 * 1024;
   static constexpr int T6T = 64 * C;                      // floats of a TK(64, C) tile
   // float offsets (after the raw stage); the lifetimes are listed per region
@@ -160,7 +169,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
   using Cf = Cfg<R, TIO>;
   constexpr int C = Cf::C, TS = Cf::TS;
   using tc::tk_off;
-  static_assert(sizeof(TIO) == 2, "bfloat16 I/O");
+  constexpr bool F32 = Cf::F32;
 
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char* raw = smem;
@@ -212,11 +221,18 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     const long long t_start = (long long)tile * TS;
     const int nst = (int)min((long long)TS, T - t_start);
     const uint32_t qb = (uint32_t)nst * D * sizeof(TIO), ub = (uint32_t)nst * R * D * sizeof(TIO);
-    mbar_arrive_expect_tx(in_bar, 3 * qb + ub);
-    bulk_g2s(raw, gq + t_start * D, qb, in_bar);
-    bulk_g2s(raw + Cf::QB, gk + t_start * D, qb, in_bar);
-    bulk_g2s(raw + 2 * Cf::QB, gv + t_start * D, qb, in_bar);
-    bulk_g2s(raw + 3 * Cf::QB, gu + t_start * R * D, ub, in_bar);
+    if constexpr (F32) {   // into L2 only: the prologue reads the tile from global memory
+      prefetch_l2(gq + t_start * D, qb);
+      prefetch_l2(gk + t_start * D, qb);
+      prefetch_l2(gv + t_start * D, qb);
+      prefetch_l2(gu + t_start * R * D, ub);
+    } else {
+      mbar_arrive_expect_tx(in_bar, 3 * qb + ub);
+      bulk_g2s(raw, gq + t_start * D, qb, in_bar);
+      bulk_g2s(raw + Cf::QB, gk + t_start * D, qb, in_bar);
+      bulk_g2s(raw + 2 * Cf::QB, gv + t_start * D, qb, in_bar);
+      bulk_g2s(raw + 3 * Cf::QB, gu + t_start * R * D, ub, in_bar);
+    }
   };
   if (tid == 0) issue(0);
 
@@ -381,9 +397,11 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
       if (to_nudge <= c) { c = (int)to_nudge; nudge = true; }
     }
     if (tile != loaded) {
-      if (tid == 0 && !mbar_wait_bounded(in_bar, (uint32_t)(tile & 1))) *flag = 1;
-      __syncthreads();
-      if (*flag) { failed = true; break; }
+      if constexpr (!F32) {
+        if (tid == 0 && !mbar_wait_bounded(in_bar, (uint32_t)(tile & 1))) *flag = 1;
+        __syncthreads();
+        if (*flag) { failed = true; break; }
+      }
       loaded = tile;
     }
     const TIO* rq = reinterpret_cast<const TIO*>(raw);
@@ -398,6 +416,11 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
       // Rows of 8-element pieces: in each group of 8 lanes the rows (row % 8) and the pieces
       // differ, so the 16-byte reads of the bf16 rows and the float4 stores into the
       // core-matrix layout are both free of bank conflicts.
+      auto ld8f = [](const TIO* g, float (&x)[8]) {   // float32 I/O: 8 values from global memory
+        const float4 a0 = __ldg(reinterpret_cast<const float4*>(g));
+        const float4 a1 = __ldg(reinterpret_cast<const float4*>(g) + 1);
+        x[0] = a0.x; x[1] = a0.y; x[2] = a0.z; x[3] = a0.w; x[4] = a1.x; x[5] = a1.y; x[6] = a1.z; x[7] = a1.w;
+      };
       auto unpack8 = [](const uint4& w, float (&x)[8]) {
         const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -410,19 +433,35 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
       for (int f = tid; f < 64 * 8; f += NT) {   // U rows a (64 x 8 pieces)
         const int arow = (f >> 6) * 8 + (f & 7), pc = ((f & 7) + (f >> 3)) & 7;
         float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        if (arow / R < c) unpack8(*reinterpret_cast<const uint4*>(ru + (ts * R + arow) * D + 8 * pc), x);
+        if (arow / R < c) {
+          if constexpr (F32)
+            ld8f(gu + (pos * R + arow) * D + 8 * pc, x);
+          else
+            unpack8(*reinterpret_cast<const uint4*>(ru + (ts * R + arow) * D + 8 * pc), x);
+        }
         st4(Cf::F_P + tk_off(arow, 8 * pc, 64), x[0], x[1], x[2], x[3]);
         st4(Cf::F_P + tk_off(arow, 8 * pc + 4, 64), x[4], x[5], x[6], x[7]);
+        if constexpr (F32) {   // [U; Sigma] low parts -> Q tiles (float32 directions are not tf32-exact)
+          st4_lo(Cf::F_Q + tk_off(arow, 8 * pc, 64), x);
+          st4_lo(Cf::F_Q + tk_off(arow, 8 * pc + 4, 64), x + 4);
+        }
       }
       for (int f = tid; f < C * 8; f += NT) {    // step rows t < C; rows c.. are zero (Sigma, phi(q), V)
         const int t = (f >> 6) * 8 + (f & 7), pc = ((f & 7) + (f >> 3)) & 7;
-        float kx[8], qx[8];
+        float kx[8], qx[8], vx[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         uint4 vw = make_uint4(0u, 0u, 0u, 0u);
         if (t < c) {
-          const int off = (ts + t) * D + 8 * pc;
-          unpack8(*reinterpret_cast<const uint4*>(rk + off), kx);
-          unpack8(*reinterpret_cast<const uint4*>(rq + off), qx);
-          vw = *reinterpret_cast<const uint4*>(rv + off);
+          if constexpr (F32) {
+            const long long goff = (pos + t) * D + 8 * pc;
+            ld8f(gk + goff, kx);
+            ld8f(gq + goff, qx);
+            ld8f(gv + goff, vx);
+          } else {
+            const int off = (ts + t) * D + 8 * pc;
+            unpack8(*reinterpret_cast<const uint4*>(rk + off), kx);
+            unpack8(*reinterpret_cast<const uint4*>(rq + off), qx);
+            vw = *reinterpret_cast<const uint4*>(rv + off);
+          }
 #pragma unroll
           for (int m = 0; m < 8; ++m) {
             kx[m] = phi_fast(kx[m]);
@@ -439,16 +478,26 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
           const float* q4p = qx + 4 * h;
           st4(Cf::F_P + tk_off(64 + t, col, 64), k4[0] * kInvSqrtD, k4[1] * kInvSqrtD, k4[2] * kInvSqrtD,
               k4[3] * kInvSqrtD);
+          if constexpr (F32) {
+            const float s4[4] = {k4[0] * kInvSqrtD, k4[1] * kInvSqrtD, k4[2] * kInvSqrtD, k4[3] * kInvSqrtD};
+            st4_lo(Cf::F_Q + tk_off(64 + t, col, 64), s4);
+          }
           st4(Cf::F_PQ + tk_off(t, col, 64), q4p[0], q4p[1], q4p[2], q4p[3]);
           *reinterpret_cast<float4*>(pk + t * PLD + col) = make_float4(k4[0], k4[1], k4[2], k4[3]);
           *reinterpret_cast<float4*>(pq + t * PLD + col) = make_float4(q4p[0], q4p[1], q4p[2], q4p[3]);
         }
-        *reinterpret_cast<uint4*>(vb + t * 64 + 8 * pc) = vw;
+        if constexpr (F32) {
+          *reinterpret_cast<float4*>(vb + t * 64 + 8 * pc) = make_float4(vx[0], vx[1], vx[2], vx[3]);
+          *reinterpret_cast<float4*>(vb + t * 64 + 8 * pc + 4) = make_float4(vx[4], vx[5], vx[6], vx[7]);
+        } else {
+          *reinterpret_cast<uint4*>(vb + t * 64 + 8 * pc) = vw;
+        }
       }
       for (int e4 = tid; e4 < (64 - C) * 16; e4 += NT) {   // zero rows C..63 of Sigma and phi(q)
         const int t = C + (e4 >> 4), col = (e4 & 15) * 4;
         st4(Cf::F_P + tk_off(64 + t, col, 64), 0.f, 0.f, 0.f, 0.f);
         st4(Cf::F_PQ + tk_off(t, col, 64), 0.f, 0.f, 0.f, 0.f);
+        if constexpr (F32) st4(Cf::F_Q + tk_off(64 + t, col, 64), 0.f, 0.f, 0.f, 0.f);
       }
       __syncthreads();
       // n_t = n_{t-1} + phi(k_t): column i, four segments of C/4 steps (one per thread)
@@ -490,9 +539,16 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
 #pragma unroll
           for (int j = 0; j < EPT; j += 4) {
             const float4 p4 = *reinterpret_cast<const float4*>(pk + t * PLD + part * EPT + j);
-            const uint2 w2 = *reinterpret_cast<const uint2*>(vb + t * 64 + part * EPT + j);
-            const float2 v01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w2.x));
-            const float2 v23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w2.y));
+            float2 v01, v23;
+            if constexpr (F32) {
+              const float4 v4 = *reinterpret_cast<const float4*>(vb + t * 64 + part * EPT + j);
+              v01 = make_float2(v4.x, v4.y);
+              v23 = make_float2(v4.z, v4.w);
+            } else {
+              const uint2 w2 = *reinterpret_cast<const uint2*>(vb + t * 64 + part * EPT + j);
+              v01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w2.x));
+              v23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w2.y));
+            }
             dn += p4.x;
             dn += p4.y;
             dn += p4.z;
@@ -527,14 +583,48 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
       }
     }
 
-    // ---------------- G1: [W^T; Q^T] = [U; Sigma] A_0^T  (M 128, N 64, K 64), A_0 hi + lo
+    // ---------------- G1: [W^T; Q^T] = [U; Sigma] A_0^T  (M 128, N 64, K 64), A_0 hi + lo (and, with
+    // float32 I/O, [U; Sigma] lo)
     {
-      const MmaPass ps[2] = {{Cf::F_P, Cf::F_A, 128, 64, TC_G1, false},
-                             {Cf::F_P, Cf::F_R + TILE, 128, 64, TC_G1, true}};
-      if (!mma_run(ps, 2, 64)) { failed = true; break; }
+      const MmaPass ps[3] = {{Cf::F_P, Cf::F_A, 128, 64, TC_G1, false},
+                             {Cf::F_P, Cf::F_R + TILE, 128, 64, TC_G1, true},
+                             {Cf::F_Q, Cf::F_A, 128, 64, TC_G1, true}};
+      if (!mma_run(ps, F32 ? 3 : 2, 64)) { failed = true; break; }
     }
     // ---------------- G2: [G - I; H^T] = [W^T; Q^T] U^T  (M 128, N 64, K 64), X read from G1's
     // accumulator in tensor memory; it runs while G1's W is drained.  Q^T stays there for alpha.
+    if constexpr (F32) {
+      // 3xTF32 for G2 as well: the low part of G1's accumulator goes to TMEM columns TC_XL.., and
+      // G2 takes X hi * U hi + X lo * U hi + X hi * U lo (U lo in the Q tiles)
+      float v32[32];
+      tld32(TC_G1 + 32 * half, v32);
+      float lo[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) lo[j] = v32[j] - tf32_hi(v32[j]);
+      tc::tmem_st32(tmem + ((uint32_t)(32 * q4) << 16) + (uint32_t)(TC_XL + 32 * half), lo);
+      tc::fence_before_sync();
+      __syncthreads();
+      tc::fence_after_sync();
+      if (tid == 0) {
+        MmaPass ps[3] = {{0, Cf::F_P, 128, 64, TC_G2, false}, {0, Cf::F_P, 128, 64, TC_G2, true},
+                         {0, Cf::F_Q, 128, 64, TC_G2, true}};
+        ps[0].tx = TC_G1;
+        ps[1].tx = TC_XL;
+        ps[2].tx = TC_G1;
+        mma_issue(ps, 3, 64);
+      }
+      if (row < 64) {   // W[i][a] = W^T[a][i], a = row (warp-uniform): fp32 -> R tile 0
+        const int g = (lane >> 2) & 7;
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int col0 = 32 * half + 16 * cc;
+          float (&v)[16] = *reinterpret_cast<float(*)[16]>(v32 + 16 * cc);
+          rot16(v, g);
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) sf[Cf::F_R + tk_off(col0 + ((jj + g) & 15), row, 64)] = v[jj];
+        }
+      }
+    } else {
     {
       MmaPass ps[1] = {{0, Cf::F_P, 128, 64, TC_G2, false}};
       ps[0].tx = TC_G1;
@@ -552,6 +642,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) sf[Cf::F_R + tk_off(col0 + ((jj + g) & 15), row, 64)] = v[jj];
       }
+    }
     }
     if (!mma_wait()) { failed = true; break; }
     float* Gs = sf + Cf::F_P;   // [64][GLD]: G, then L (strict lower) in place
@@ -972,11 +1063,29 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
         misc[Cf::M_AN2 + 64 * half + t] = an;   // |alpha_t|^2, two halves
       }
       // ---------------- G5: [S alpha ; S phi(q) | alpha.alpha ; phi(q).alpha] = [alpha; phi(q)] [S; alpha]^T,
-      // issued as soon as alpha is written; the rest of G4's drain runs beside it
+      // issued as soon as alpha is written; the rest of G4's drain runs beside it.  With float32
+      // I/O it is 3xTF32: [S lo; alpha lo; phi(q) lo] go to the P tiles and Q tile 0 (free once
+      // G4 is done), contiguous like [S; alpha; phi(q)]
+      if constexpr (F32) {
+        if (row >= 64) {
+          const int t = row - 64;
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) st4_lo(Cf::F_P + TILE + tk_off(t, 32 * half + j, 64), al32 + j);
+        }
+        for (int e4 = tid; e4 < TILE / 4; e4 += NT) {
+          const float4 s4 = *reinterpret_cast<const float4*>(sf + Cf::F_S + 4 * e4);
+          const float4 q4v = *reinterpret_cast<const float4*>(sf + Cf::F_PQ + 4 * e4);
+          const float sv[4] = {s4.x, s4.y, s4.z, s4.w}, qv[4] = {q4v.x, q4v.y, q4v.z, q4v.w};
+          st4_lo(Cf::F_P + 4 * e4, sv);
+          st4_lo(Cf::F_Q + 4 * e4, qv);
+        }
+      }
       sync_tc();
       if (tid == 0) {
-        const MmaPass ps[1] = {{Cf::F_AL, Cf::F_S, 128, 128, TC_G5, false}};
-        mma_issue(ps, 1, 64);
+        const MmaPass ps[3] = {{Cf::F_AL, Cf::F_S, 128, 128, TC_G5, false},
+                               {Cf::F_P + TILE, Cf::F_S, 128, 128, TC_G5, true},
+                               {Cf::F_AL, Cf::F_P, 128, 128, TC_G5, true}};
+        mma_issue(ps, F32 ? 3 : 1, 64);
       }
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
@@ -1186,9 +1295,23 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     // ---------------- G6: X = [V^T; tril(aq)] (M 128, K C); Y = V^T accumulates tril(aq) V onto
     // S phi(q_t) (rows 64 + t, columns 0..63); Y = alpha^T gives V^T alpha (rows i, columns 128..191)
     {
-      const MmaPass ps[2] = {{Cf::F_T6, Cf::F_T6 + Cf::T6_V, 128, 64, TC_G5, true},
-                             {Cf::F_T6, Cf::F_T6 + Cf::T6_A, 128, 64, TC_G6, false}};
-      if (!mma_run(ps, 2, C)) { failed = true; break; }
+      // float32 I/O: 3xTF32, with the low parts of [V^T; tril(aq); alpha^T] in the P tiles (laid out
+      // like T6; G5, their previous user, is done)
+      if constexpr (F32) {
+        __syncthreads();   // every thread's part of T6 (tril(aq) by rows t, alpha^T, V^T) is written
+        for (int e4 = tid; e4 < 3 * Cf::T6T / 4; e4 += NT) {
+          const float4 x = *reinterpret_cast<const float4*>(sf + Cf::F_T6 + 4 * e4);
+          const float xv[4] = {x.x, x.y, x.z, x.w};
+          st4_lo(Cf::F_P + 4 * e4, xv);
+        }
+      }
+      const MmaPass ps[6] = {{Cf::F_T6, Cf::F_T6 + Cf::T6_V, 128, 64, TC_G5, true},
+                             {Cf::F_T6, Cf::F_T6 + Cf::T6_A, 128, 64, TC_G6, false},
+                             {Cf::F_P, Cf::F_T6 + Cf::T6_V, 128, 64, TC_G5, true},
+                             {Cf::F_T6, Cf::F_P + Cf::T6_V, 128, 64, TC_G5, true},
+                             {Cf::F_P, Cf::F_T6 + Cf::T6_A, 128, 64, TC_G6, true},
+                             {Cf::F_T6, Cf::F_P + Cf::T6_A, 128, 64, TC_G6, true}};
+      if (!mma_run(ps, F32 ? 6 : 2, C)) { failed = true; break; }
     }
     {
       float v32[32];
@@ -1201,17 +1324,27 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
           const int col0 = 32 * half + 16 * cc;
           float (&v)[16] = *reinterpret_cast<float(*)[16]>(v32 + 16 * cc);
           if (t < c) {
-            uint32_t pk[8];
+            float ov[16];
 #pragma unroll
-            for (int j = 0; j < 16; j += 2) {
-              const float o0 = sgt * v[j] * rd, o1 = sgt * v[j + 1] * rd;
-              if (!isfinite(o0) || !isfinite(o1)) flags |= kStatusNonfinite;
-              const __nv_bfloat162 b2 = __floats2bfloat162_rn(o0, o1);
-              pk[j / 2] = *reinterpret_cast<const uint32_t*>(&b2);
+            for (int j = 0; j < 16; ++j) {
+              ov[j] = sgt * v[j] * rd;
+              if (!isfinite(ov[j])) flags |= kStatusNonfinite;
             }
-            uint4* dst = reinterpret_cast<uint4*>(go + (pos + t) * D + col0);
-            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            if constexpr (F32) {
+              float4* dst = reinterpret_cast<float4*>(go + (pos + t) * D + col0);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) dst[j] = make_float4(ov[4 * j], ov[4 * j + 1], ov[4 * j + 2], ov[4 * j + 3]);
+            } else {
+              uint32_t pk[8];
+#pragma unroll
+              for (int j = 0; j < 16; j += 2) {
+                const __nv_bfloat162 b2 = __floats2bfloat162_rn(ov[j], ov[j + 1]);
+                pk[j / 2] = *reinterpret_cast<const uint32_t*>(&b2);
+              }
+              uint4* dst = reinterpret_cast<uint4*>(go + (pos + t) * D + col0);
+              dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            }
           }
         }
       } else {           // S_1 = sigma (S + V^T alpha), rows i, columns 32 half .. 32 half + 31
@@ -1258,7 +1391,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     if (tid < D) gn[tid] = misc[Cf::M_N + tid];
   } else if (tid == 0) {
     flags |= kStatusTimeout;
-    if (*issued > loaded) (void)mbar_wait_bounded(in_bar, (uint32_t)((loaded + 1) & 1));   // a copy in flight
+    if (!F32 && *issued > loaded) (void)mbar_wait_bounded(in_bar, (uint32_t)((loaded + 1) & 1));   // a copy in flight
   }
   if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
   if (flags) atomicOr(&a.status->flags, flags);

@@ -94,6 +94,8 @@ def test_tensor_flops_of_the_chunked_kernel():
     assert bench.chunk_tensor_flops_per_token_head(1) == 13 * base / 64
     # r = 4, 16 steps a chunk: G6 has K = 16
     assert bench.chunk_tensor_flops_per_token_head(4) == (9 * base + 2 * base + 2 * base / 4) / 16
+    # float32 I/O: 3 passes everywhere
+    assert bench.chunk_tensor_flops_per_token_head(1, True) == (12 * base + 6 * base + 6 * base) / 64
 
 
 def test_oracle_leg_shares_the_pairs_over_processes():

@@ -1,12 +1,13 @@
 """GPU parity of the chunked (exact Woodbury / LDL^T, tcgen05) scan.
 
 The chunked mode takes 64 directions per chunk (64 steps at r = 1, 16 at r = 4)
-with the dense contractions on tensor cores in tf32, for d = d_v = 64 and
-bfloat16 I/O.  It is checked against the float64 oracle and against the
-sequential kernel at the bfloat16 gate (2e-2), on full-length workloads with a
-sample of pairs and on edge cases: ragged lengths, nudges that split chunks
-(t0 phase), renormalisation firing (the exact per-step path) and the
-singularity guard (the step-by-step fallback).
+with the dense contractions on tensor cores in tf32, for d = d_v = 64, bfloat16
+and float32 I/O (float32: 3xTF32 on every product).  It is checked against the
+float64 oracle and against the sequential kernel at the gate of its I/O type
+(bfloat16 2e-2, float32 1e-4 at T <= 4096), on full-length workloads and on edge
+cases: ragged lengths, nudges that split chunks (t0 phase), renormalisation
+firing (the exact per-step path) and the singularity guard (the step-by-step
+fallback).
 """
 from __future__ import annotations
 
@@ -20,6 +21,7 @@ from _util import ensure_built, errs, gpu_scan, oracle_scan
 pytestmark = pytest.mark.gpu
 
 TOL = 2e-2
+TOL_F32 = 1e-4
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -61,35 +63,52 @@ EDGE = [
 ]
 
 
+@pytest.mark.parametrize("io", ["bf16", "f32"])
 @pytest.mark.parametrize("N,T,r,P,tau,t0", EDGE)
-def test_chunked_edges(N, T, r, P, tau, t0):
-    x = workloads.gaussian_inputs(N, T, 64, 64, r, "bf16", seed=500 + T + r)
+def test_chunked_edges(N, T, r, P, tau, t0, io):
+    x = workloads.gaussian_inputs(N, T, 64, 64, r, io, seed=500 + T + r)
     kw = dict(P=P, eps_n=1e-3, tau=tau, t0=t0)
     got = gpu_scan(x, 1, N, mode="chunked", chunk=0, **kw)
     ref = oracle_scan(x, **kw, trace=True)
-    _check(errs(got, ref), TOL, f"chunked edge N{N} T{T} r{r} P{P} tau{tau}")
+    _check(errs(got, ref), TOL if io == "bf16" else TOL_F32, f"chunked edge {io} N{N} T{T} r{r} P{P} tau{tau}")
     assert got[4]["renorm_count"] == int(ref[4]["renorm"].sum())
 
 
-def test_chunked_guard_falls_back_step_by_step():
+def test_chunked_f32_workload_parity():
+    """b4h8_t4096_d64_f32 (float32 I/O, 32 pairs) in chunked mode: every pair against the
+    oracle at the float32 gate, and against the sequential kernel."""
+    w = workloads.get(1)
+    x = workloads.make_inputs(w)
+    kw = dict(P=w.P, eps_n=w.eps_n, tau=w.tau)
+    got = gpu_scan(x, w.B, w.H, mode="chunked", chunk=0, **kw)
+    assert got[4]["flags"] == 0 and got[4]["chunk_fallbacks"] == 0
+    ref = oracle_scan(x, **kw)
+    _check(errs(got, ref), TOL_F32, f"chunked {w.name} vs oracle")
+    seq = gpu_scan(x, w.B, w.H, **kw)
+    import oracle
+    _check(oracle.errors(*got[:4], *seq[:4]), TOL_F32, f"chunked vs sequential {w.name}")
+
+
+@pytest.mark.parametrize("io", ["bf16", "f32"])
+def test_chunked_guard_falls_back_step_by_step(io):
     N, T = 2, 40
-    x = workloads.gaussian_inputs(N, T, 64, 64, 1, "bf16", seed=77)
+    x = workloads.gaussian_inputs(N, T, 64, 64, 1, io, seed=77)
     x["A0"] = -torch.eye(64).expand(N, 64, 64).contiguous()
     x["u"][:, 0] = 0.0
-    x["u"][:, 0, 0, 5] = 1.0          # exactly unit in bf16: delta = 1 - 1 = 0 at step 1
-    x["u"][:, 1:] = (x["u"][:, 1:].float() * 0.5).bfloat16()
+    x["u"][:, 0, 0, 5] = 1.0          # exactly unit: delta = 1 - 1 = 0 at step 1
+    x["u"][:, 1:] = (x["u"][:, 1:].float() * 0.5).to(x["u"].dtype)
     kw = dict(P=0, eps_n=0.0, tau=1e30)
     got = gpu_scan(x, 1, N, mode="chunked", chunk=0, **kw)
     ref = oracle_scan(x, **kw, trace=True)
     assert ref[4]["guard"][:, 0, 0].all()
     assert got[4]["chunk_fallbacks"] >= 1
     assert got[4]["guard_count"] == int(ref[4]["guard"].sum())
-    _check(errs(got, ref), TOL, "chunked guard fallback")
+    _check(errs(got, ref), TOL if io == "bf16" else TOL_F32, f"chunked guard fallback {io}")
 
 
 def test_chunked_rejects_shapes_it_does_not_build():
     import sherman_morrison_inverse_gb300 as vla
-    x = workloads.gaussian_inputs(1, 8, 64, 64, 1, "f32", seed=3)
+    x = workloads.gaussian_inputs(1, 8, 64, 64, 2, "f32", seed=3)   # r = 2
     with pytest.raises(vla.VlaError, match="UNSUPPORTED"):
         gpu_scan(x, 1, 1, mode="chunked", P=0, eps_n=0.0, tau=1e4)
     x = workloads.gaussian_inputs(1, 8, 16, 16, 1, "bf16", seed=3)
