@@ -50,8 +50,13 @@
 // drops the low 13 mantissa bits (truncation).  The products that carry A forward (G1's
 // A_0, G3, G4) are 3xTF32: the fp32 operand x is its own high part, lo = x - hi is stored
 // beside it, and hi*hi + lo*hi + hi*lo is accumulated, so A tracks the fp32 recurrence.
-// G2, G5 and G6 are plain tf32.  The state (A, S) stays fp32.  Built for d = d_v = 64
-// and bfloat16 I/O.
+// With bfloat16 I/O, G2, G5 and G6 are plain tf32 (U is exact in tf32; the outputs are
+// rounded to bf16).  With float32 I/O every product is 3xTF32: [U; Sigma] lo for G1; G2's
+// X lo (G1's accumulator minus its tf32 part) stored back into TMEM columns 448..511; the
+// low parts of G5's and G6's operands in the P and Q tiles, free by then.  There is no raw
+// stage with float32 I/O (it would not fit): the prologue reads q, k, v, u from global
+// memory, the next tile having been prefetched into L2.  The state (A, S) stays fp32.
+// Built for d = d_v = 64, r = 1 and 4, bfloat16 and float32 I/O.
 #pragma once
 
 #include "vla_tc.cuh"
