@@ -184,8 +184,8 @@ def test_host_path_zero_sizes_and_errors():
     kw = dict(P=0, eps_n=0.0, tau=1e4)
     with pytest.raises(vla.VlaError, match="INVALID_ARG"):
         h.scan_fwd_host(hx["q"], hx["k"], hx["v"], hx["u"], A, S, n, seg=-1, **kw)
-    with pytest.raises(vla.VlaError, match="UNSUPPORTED"):
-        xf = workloads.gaussian_inputs(1, 8, 64, 64, 1, "f32", seed=5)
+    with pytest.raises(vla.VlaError, match="UNSUPPORTED"):   # chunked mode is built for d = 64 only
+        xf = workloads.gaussian_inputs(1, 8, 16, 16, 1, "bf16", seed=5)
         hf = _host(xf, 1, 1)
         h.scan_fwd_host(hf["q"], hf["k"], hf["v"], hf["u"], hf["A0"], hf["S0"], hf["n0"], mode="chunked", **kw)
     with pytest.raises(ValueError, match="expected cpu"):
