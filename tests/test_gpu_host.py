@@ -196,3 +196,25 @@ def test_host_path_zero_sizes_and_errors():
     o = h.scan_fwd_host(e["q"], e["k"], e["v"], e["u"], A, S, n, **kw)
     assert o.shape[2] == 0 and torch.equal(A, A0)
     assert h.status()["flags"] == 0
+
+
+def test_host_path_chunked_float32_matches_the_device_windows():
+    """Float32 I/O in chunked mode (3xTF32, inputs read from global memory) through the host
+    path: bit for bit the device entry point called once per window, and within the float32
+    gate of the oracle."""
+    import sherman_morrison_inverse_gb300 as vla
+    h = vla.default_handle()
+    N, T = 3, 640
+    x = workloads.gaussian_inputs(N, T, 64, 64, 1, "f32", seed=83)
+    kw = dict(P=100, eps_n=1e-3, tau=1e4, mode="chunked")
+    hx = _host(x, 1, N)
+    A, S, n = (hx[k].clone().pin_memory() for k in ("A0", "S0", "n0"))
+    o = h.scan_fwd_host(hx["q"], hx["k"], hx["v"], hx["u"], A, S, n, seg=256, **kw)
+    assert h.status()["flags"] == 0
+    ref_dev = _device_windows(h, x, 1, N, 256, **kw)
+    _same((o, A, S, n), ref_dev, "float32 chunked")
+    import oracle
+    ref = oracle_scan(x, P=100, eps_n=1e-3, tau=1e4)
+    e = oracle.errors(o.reshape(N, T, 64).double().numpy(), A.reshape(N, 64, 64).double().numpy(),
+                      S.reshape(N, 64, 64).double().numpy(), n.reshape(N, 64).double().numpy(), *ref[:4])
+    assert max(e.values()) <= 1e-4, e
