@@ -7,8 +7,9 @@
 // but at about half of it when the rows of several tensors alternate in 128 KB pieces.
 // SM loads through the mapped device address of the host buffer keep the full rate for
 // any window, provided enough 16-byte loads are in flight to cover the link's latency:
-// 1024 threads on each of a few SMs, each with up to 8 loads issued before its stores.
-// So the window is gathered by a small kernel that runs on the SMs the scan leaves idle.
+// 1024 threads on each of a few SMs, each with up to 8 loads issued before its stores, the
+// grid reading consecutive addresses.  So the window is gathered by a small kernel that runs
+// on the SMs the scan leaves idle.
 #include "vla_internal.cuh"
 
 namespace vla {
@@ -24,37 +25,41 @@ struct GatherArgs {
 constexpr int kGatherThreads = 1024;
 constexpr int kGatherUnroll = 8;   // independent 16-byte loads in flight per thread
 
-// The window of tensor t for pair p is one contiguous run of tj * w16[t] vectors on both
-// sides (from step `off` of the pair's [T, w] block into the pair's [tj, w] block).  The
-// 4 * pairs runs are taken whole, one per CTA at a time (run = blockIdx.x, + gridDim.x, ...);
-// each thread issues up to kGatherUnroll loads before it stores them, so a CTA keeps up to
-// 128 KB of host reads in flight.
+// Each tensor's window is one flat index space of pairs * tj * w16 vectors (pair-major, as the
+// staging buffer); thread g copies the vectors g, g + G, g + 2 G, ... (G threads in the grid), so
+// the grid as a whole streams consecutive host addresses.  Up to kGatherUnroll loads are issued
+// before their stores.  Indices fit in 32 bits (the host checks), so the row of an index costs
+// one 32-bit division.
 __global__ void __launch_bounds__(kGatherThreads) gather_window_kernel(GatherArgs g) {
-  const long long runs = 4 * g.pairs;
+  const uint32_t G = gridDim.x * (uint32_t)kGatherThreads;
+  const uint32_t gtid = blockIdx.x * (uint32_t)kGatherThreads + threadIdx.x;
 #pragma unroll 1
-  for (long long run = blockIdx.x; run < runs; run += gridDim.x) {
-    const int t = (int)(run / g.pairs);
-    const long long p = run - t * g.pairs;
+  for (int t = 0; t < 4; ++t) {
     // tensor t's fields by a static selection (a run-time index into the parameter block
     // would copy it to local memory)
     const long long w16 = t == 0 ? g.w16[0] : t == 1 ? g.w16[1] : t == 2 ? g.w16[2] : g.w16[3];
-    const uint4* s0 = t == 0 ? g.src[0] : t == 1 ? g.src[1] : t == 2 ? g.src[2] : g.src[3];
-    uint4* d0 = t == 0 ? g.dst[0] : t == 1 ? g.dst[1] : t == 2 ? g.dst[2] : g.dst[3];
-    const long long len = g.tj * w16;
-    const uint4* __restrict__ src = s0 + (p * g.T + g.off) * w16;
-    uint4* __restrict__ dst = d0 + p * len;
-    constexpr long long kBatch = (long long)kGatherUnroll * kGatherThreads;
-    long long j0 = threadIdx.x;
+    const uint4* __restrict__ src = t == 0 ? g.src[0] : t == 1 ? g.src[1] : t == 2 ? g.src[2] : g.src[3];
+    uint4* __restrict__ dst = t == 0 ? g.dst[0] : t == 1 ? g.dst[1] : t == 2 ? g.dst[2] : g.dst[3];
+    const uint32_t len = (uint32_t)(g.tj * w16);              // vectors of one pair's window
+    const uint32_t n = (uint32_t)(g.pairs * (long long)len);  // vectors of the window
+    const long long pitch = g.T * w16, first = g.off * w16;
 #pragma unroll 1
-    for (; j0 + (kGatherUnroll - 1) * kGatherThreads < len; j0 += kBatch) {   // whole batches
+    for (uint32_t i0 = gtid; i0 < n; i0 += kGatherUnroll * G) {
       uint4 v[kGatherUnroll];
 #pragma unroll
-      for (int k = 0; k < kGatherUnroll; ++k) v[k] = src[j0 + k * kGatherThreads];
+      for (int k = 0; k < kGatherUnroll; ++k) {
+        const uint32_t i = i0 + k * G;
+        if (i < n) {
+          const uint32_t p = i / len;
+          v[k] = src[(long long)p * pitch + first + (i - p * len)];
+        }
+      }
 #pragma unroll
-      for (int k = 0; k < kGatherUnroll; ++k) dst[j0 + k * kGatherThreads] = v[k];
+      for (int k = 0; k < kGatherUnroll; ++k) {
+        const uint32_t i = i0 + k * G;
+        if (i < n) dst[i] = v[k];
+      }
     }
-#pragma unroll 1
-    for (; j0 < len; j0 += kGatherThreads) dst[j0] = src[j0];   // the rest of the run
   }
 }
 
@@ -73,6 +78,11 @@ cudaError_t launch_gather_window(const void* const src[4], void* const dst[4], c
   g.T = T;
   g.off = off;
   g.tj = tj;
+  // 32-bit indices: every window of every tensor below 2^31 vectors, with room for the
+  // strided indices of the last batch (kGatherUnroll * threads beyond the end)
+  const long long limit = (1ll << 31) - (long long)kGatherUnroll * kGatherThreads * ctas;
+  for (int t = 0; t < 4; ++t)
+    if (pairs * tj * g.w16[t] >= limit) return cudaErrorInvalidValue;
   gather_window_kernel<<<ctas, kGatherThreads, 0, s>>>(g);
   return cudaGetLastError();
 }
