@@ -54,8 +54,9 @@
 // rounded to bf16).  With float32 I/O every product is 3xTF32: [U; Sigma] lo for G1; G2's
 // X lo (G1's accumulator minus its tf32 part) stored back into TMEM columns 448..511; the
 // low parts of G5's and G6's operands in the P and Q tiles, free by then.  There is no raw
-// stage with float32 I/O (it would not fit): the prologue reads q, k, v, u from global
-// memory, the next tile having been prefetched into L2.  The state (A, S) stays fp32.
+// stage with float32 I/O (it would not fit): bulk copies issued right after a chunk's G6 bring
+// the next chunk's q, k, v, u into tiles that G6 and its drain leave alone (PQ, Q tile 1, vb,
+// AL), and the prologue converts them there.  The state (A, S) stays fp32.
 // Built for d = d_v = 64, r = 1 and 4, bfloat16 and float32 I/O.
 #pragma once
 
@@ -102,11 +103,6 @@ __device__ __forceinline__ float rcp_approx(float x) {
   float r;
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
   return r;
-}
-
-// bring [p, p + bytes) into L2 (16-byte aligned, a multiple of 16 bytes); nothing waits for it
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // named barriers (ids 1..5; 0 is __syncthreads): `n` threads take part, a multiple of 32
@@ -226,20 +222,27 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     const long long t_start = (long long)tile * TS;
     const int nst = (int)min((long long)TS, T - t_start);
     const uint32_t qb = (uint32_t)nst * D * sizeof(TIO), ub = (uint32_t)nst * R * D * sizeof(TIO);
-    if constexpr (F32) {   // into L2 only: the prologue reads the tile from global memory
-      prefetch_l2(gq + t_start * D, qb);
-      prefetch_l2(gk + t_start * D, qb);
-      prefetch_l2(gv + t_start * D, qb);
-      prefetch_l2(gu + t_start * R * D, ub);
-    } else {
-      mbar_arrive_expect_tx(in_bar, 3 * qb + ub);
-      bulk_g2s(raw, gq + t_start * D, qb, in_bar);
-      bulk_g2s(raw + Cf::QB, gk + t_start * D, qb, in_bar);
-      bulk_g2s(raw + 2 * Cf::QB, gv + t_start * D, qb, in_bar);
-      bulk_g2s(raw + 3 * Cf::QB, gu + t_start * R * D, ub, in_bar);
-    }
+    mbar_arrive_expect_tx(in_bar, 3 * qb + ub);
+    bulk_g2s(raw, gq + t_start * D, qb, in_bar);
+    bulk_g2s(raw + Cf::QB, gk + t_start * D, qb, in_bar);
+    bulk_g2s(raw + 2 * Cf::QB, gv + t_start * D, qb, in_bar);
+    bulk_g2s(raw + 3 * Cf::QB, gu + t_start * R * D, ub, in_bar);
   };
-  if (tid == 0) issue(0);
+  if (!F32 && tid == 0) issue(0);
+  // Float32 I/O has no raw stage: a chunk's q, k, v, u are copied into the tiles that are free
+  // from the previous chunk's G6 until this chunk's prologue (q -> PQ, k -> Q tile 1, v -> vb,
+  // where it stays as it is, u -> AL), issued right after that G6 so that they land beside it.
+  long long staged_pos = -1;   // the chunk whose inputs were issued last (all threads agree)
+  bool stage_pending = false;  // issued and not yet waited for
+  uint32_t stage_phase = 0;
+  auto stage = [&](long long p0, int cc) {   // one thread
+    const uint32_t qb = (uint32_t)cc * D * sizeof(TIO), ub = (uint32_t)cc * R * D * sizeof(TIO);
+    mbar_arrive_expect_tx(in_bar, 3 * qb + ub);
+    bulk_g2s(sf + Cf::F_PQ, gq + p0 * D, qb, in_bar);
+    bulk_g2s(sf + Cf::F_Q + TILE, gk + p0 * D, qb, in_bar);
+    bulk_g2s(vb, gv + p0 * D, qb, in_bar);
+    bulk_g2s(sf + Cf::F_AL, gu + p0 * R * D, ub, in_bar);
+  };
 
   uint32_t mma_phase = 0;
   unsigned int flags = 0;
@@ -401,12 +404,22 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     if (a.P > 0) {
       if (to_nudge <= c) { c = (int)to_nudge; nudge = true; }
     }
-    if (tile != loaded) {
-      if constexpr (!F32) {
-        if (tid == 0 && !mbar_wait_bounded(in_bar, (uint32_t)(tile & 1))) *flag = 1;
-        __syncthreads();
-        if (*flag) { failed = true; break; }
+    if constexpr (F32) {
+      if (staged_pos != pos) {   // not issued ahead: the first chunk, or after a step-by-step chunk
+        if (tid == 0) stage(pos, c);
+        staged_pos = pos;
+        stage_pending = true;
       }
+      if (tid == 0 && !mbar_wait_bounded(in_bar, stage_phase)) *flag = 1;
+      stage_phase ^= 1u;
+      __syncthreads();
+      if (*flag) { failed = true; break; }
+      stage_pending = false;
+      loaded = tile;
+    } else if (tile != loaded) {
+      if (tid == 0 && !mbar_wait_bounded(in_bar, (uint32_t)(tile & 1))) *flag = 1;
+      __syncthreads();
+      if (*flag) { failed = true; break; }
       loaded = tile;
     }
     const TIO* rq = reinterpret_cast<const TIO*>(raw);
@@ -421,9 +434,9 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
       // Rows of 8-element pieces: in each group of 8 lanes the rows (row % 8) and the pieces
       // differ, so the 16-byte reads of the bf16 rows and the float4 stores into the
       // core-matrix layout are both free of bank conflicts.
-      auto ld8f = [](const TIO* g, float (&x)[8]) {   // float32 I/O: 8 values from global memory
-        const float4 a0 = __ldg(reinterpret_cast<const float4*>(g));
-        const float4 a1 = __ldg(reinterpret_cast<const float4*>(g) + 1);
+      auto ld8s = [](const float* s, float (&x)[8]) {   // float32 I/O: 8 staged values
+        const float4 a0 = *reinterpret_cast<const float4*>(s);
+        const float4 a1 = *reinterpret_cast<const float4*>(s + 4);
         x[0] = a0.x; x[1] = a0.y; x[2] = a0.z; x[3] = a0.w; x[4] = a1.x; x[5] = a1.y; x[6] = a1.z; x[7] = a1.w;
       };
       auto unpack8 = [](const uint4& w, float (&x)[8]) {
@@ -440,7 +453,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
         float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         if (arow / R < c) {
           if constexpr (F32)
-            ld8f(gu + (pos * R + arow) * D + 8 * pc, x);
+            ld8s(sf + Cf::F_AL + arow * D + 8 * pc, x);
           else
             unpack8(*reinterpret_cast<const uint4*>(ru + (ts * R + arow) * D + 8 * pc), x);
         }
@@ -451,50 +464,107 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
           st4_lo(Cf::F_Q + tk_off(arow, 8 * pc + 4, 64), x + 4);
         }
       }
-      for (int f = tid; f < C * 8; f += NT) {    // step rows t < C; rows c.. are zero (Sigma, phi(q), V)
-        const int t = (f >> 6) * 8 + (f & 7), pc = ((f & 7) + (f >> 3)) & 7;
-        float kx[8], qx[8], vx[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        uint4 vw = make_uint4(0u, 0u, 0u, 0u);
-        if (t < c) {
-          if constexpr (F32) {
-            const long long goff = (pos + t) * D + 8 * pc;
-            ld8f(gk + goff, kx);
-            ld8f(gq + goff, qx);
-            ld8f(gv + goff, vx);
+      if constexpr (F32) {
+        // step rows t < C; rows c.. are zero (Sigma, phi(q), V)
+        constexpr int NSI = (C * 8 + NT - 1) / NT;
+        [[maybe_unused]] float kr[NSI][8], qr[NSI][8];
+        if constexpr (F32) {
+          // the staged k (Q tile 1) and q (PQ) are overwritten by this loop's outputs: every
+          // thread reads its pieces first
+#pragma unroll
+          for (int s = 0; s < NSI; ++s) {
+            const int f = tid + NT * s;
+            const int t = (f >> 6) * 8 + (f & 7), pc = ((f & 7) + (f >> 3)) & 7;
+            if (f < C * 8 && t < c) {
+              ld8s(sf + Cf::F_Q + TILE + t * D + 8 * pc, kr[s]);
+              ld8s(sf + Cf::F_PQ + t * D + 8 * pc, qr[s]);
+            }
+          }
+          __syncthreads();
+        }
+#pragma unroll
+        for (int s = 0; s < NSI; ++s) {
+          const int f = tid + NT * s;
+          if (f >= C * 8) break;
+          const int t = (f >> 6) * 8 + (f & 7), pc = ((f & 7) + (f >> 3)) & 7;
+          float kx[8], qx[8];
+          uint4 vw = make_uint4(0u, 0u, 0u, 0u);
+          if (t < c) {
+            if constexpr (F32) {
+#pragma unroll
+              for (int m = 0; m < 8; ++m) {
+                kx[m] = kr[s][m];
+                qx[m] = qr[s][m];
+              }
+            } else {
+              const int off = (ts + t) * D + 8 * pc;
+              unpack8(*reinterpret_cast<const uint4*>(rk + off), kx);
+              unpack8(*reinterpret_cast<const uint4*>(rq + off), qx);
+              vw = *reinterpret_cast<const uint4*>(rv + off);
+            }
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+              kx[m] = phi_fast(kx[m]);
+              qx[m] = phi_fast(qx[m]);
+            }
           } else {
+#pragma unroll
+            for (int m = 0; m < 8; ++m) kx[m] = qx[m] = 0.f;
+          }
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int col = 8 * pc + 4 * h;
+            const float* k4 = kx + 4 * h;
+            const float* q4p = qx + 4 * h;
+            st4(Cf::F_P + tk_off(64 + t, col, 64), k4[0] * kInvSqrtD, k4[1] * kInvSqrtD, k4[2] * kInvSqrtD,
+                k4[3] * kInvSqrtD);
+            if constexpr (F32) {
+              const float s4[4] = {k4[0] * kInvSqrtD, k4[1] * kInvSqrtD, k4[2] * kInvSqrtD, k4[3] * kInvSqrtD};
+              st4_lo(Cf::F_Q + tk_off(64 + t, col, 64), s4);
+            }
+            st4(Cf::F_PQ + tk_off(t, col, 64), q4p[0], q4p[1], q4p[2], q4p[3]);
+            *reinterpret_cast<float4*>(pk + t * PLD + col) = make_float4(k4[0], k4[1], k4[2], k4[3]);
+            *reinterpret_cast<float4*>(pq + t * PLD + col) = make_float4(q4p[0], q4p[1], q4p[2], q4p[3]);
+          }
+          if constexpr (F32) {   // V was staged into vb as it is; rows past c are zeroed
+            if (t >= c) {
+              *reinterpret_cast<float4*>(vb + t * 64 + 8 * pc) = make_float4(0.f, 0.f, 0.f, 0.f);
+              *reinterpret_cast<float4*>(vb + t * 64 + 8 * pc + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+          } else {
+            *reinterpret_cast<uint4*>(vb + t * 64 + 8 * pc) = vw;
+          }
+        }
+      } else {
+        for (int f = tid; f < C * 8; f += NT) {    // step rows t < C; rows c.. are zero (Sigma, phi(q), V)
+          const int t = (f >> 6) * 8 + (f & 7), pc = ((f & 7) + (f >> 3)) & 7;
+          float kx[8], qx[8];
+          uint4 vw = make_uint4(0u, 0u, 0u, 0u);
+          if (t < c) {
             const int off = (ts + t) * D + 8 * pc;
             unpack8(*reinterpret_cast<const uint4*>(rk + off), kx);
             unpack8(*reinterpret_cast<const uint4*>(rq + off), qx);
             vw = *reinterpret_cast<const uint4*>(rv + off);
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+              kx[m] = phi_fast(kx[m]);
+              qx[m] = phi_fast(qx[m]);
+            }
+          } else {
+#pragma unroll
+            for (int m = 0; m < 8; ++m) kx[m] = qx[m] = 0.f;
           }
 #pragma unroll
-          for (int m = 0; m < 8; ++m) {
-            kx[m] = phi_fast(kx[m]);
-            qx[m] = phi_fast(qx[m]);
+          for (int h = 0; h < 2; ++h) {
+            const int col = 8 * pc + 4 * h;
+            const float* k4 = kx + 4 * h;
+            const float* q4p = qx + 4 * h;
+            st4(Cf::F_P + tk_off(64 + t, col, 64), k4[0] * kInvSqrtD, k4[1] * kInvSqrtD, k4[2] * kInvSqrtD,
+                k4[3] * kInvSqrtD);
+            st4(Cf::F_PQ + tk_off(t, col, 64), q4p[0], q4p[1], q4p[2], q4p[3]);
+            *reinterpret_cast<float4*>(pk + t * PLD + col) = make_float4(k4[0], k4[1], k4[2], k4[3]);
+            *reinterpret_cast<float4*>(pq + t * PLD + col) = make_float4(q4p[0], q4p[1], q4p[2], q4p[3]);
           }
-        } else {
-#pragma unroll
-          for (int m = 0; m < 8; ++m) kx[m] = qx[m] = 0.f;
-        }
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int col = 8 * pc + 4 * h;
-          const float* k4 = kx + 4 * h;
-          const float* q4p = qx + 4 * h;
-          st4(Cf::F_P + tk_off(64 + t, col, 64), k4[0] * kInvSqrtD, k4[1] * kInvSqrtD, k4[2] * kInvSqrtD,
-              k4[3] * kInvSqrtD);
-          if constexpr (F32) {
-            const float s4[4] = {k4[0] * kInvSqrtD, k4[1] * kInvSqrtD, k4[2] * kInvSqrtD, k4[3] * kInvSqrtD};
-            st4_lo(Cf::F_Q + tk_off(64 + t, col, 64), s4);
-          }
-          st4(Cf::F_PQ + tk_off(t, col, 64), q4p[0], q4p[1], q4p[2], q4p[3]);
-          *reinterpret_cast<float4*>(pk + t * PLD + col) = make_float4(k4[0], k4[1], k4[2], k4[3]);
-          *reinterpret_cast<float4*>(pq + t * PLD + col) = make_float4(q4p[0], q4p[1], q4p[2], q4p[3]);
-        }
-        if constexpr (F32) {
-          *reinterpret_cast<float4*>(vb + t * 64 + 8 * pc) = make_float4(vx[0], vx[1], vx[2], vx[3]);
-          *reinterpret_cast<float4*>(vb + t * 64 + 8 * pc + 4) = make_float4(vx[4], vx[5], vx[6], vx[7]);
-        } else {
           *reinterpret_cast<uint4*>(vb + t * 64 + 8 * pc) = vw;
         }
       }
@@ -576,7 +646,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
       }
       __syncthreads();
       // the raw stage is free once the tile's last chunk is converted
-      if (tid == 0 && ts + c == TS && tile + 1 < ntiles) {
+      if (!F32 && tid == 0 && ts + c == TS && tile + 1 < ntiles) {
         fence_proxy_async_smem();
         issue(tile + 1);
       }
@@ -1316,7 +1386,26 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
                              {Cf::F_T6, Cf::F_P + Cf::T6_V, 128, 64, TC_G5, true},
                              {Cf::F_P, Cf::F_T6 + Cf::T6_A, 128, 64, TC_G6, true},
                              {Cf::F_T6, Cf::F_P + Cf::T6_A, 128, 64, TC_G6, true}};
-      if (!mma_run(ps, F32 ? 6 : 2, C)) { failed = true; break; }
+      sync_tc();
+      if (tid == 0) mma_issue(ps, F32 ? 6 : 2, C);
+      if constexpr (F32) {
+        // the next chunk's inputs into AL, PQ, Q tile 1 and vb: G6 and its drain do not touch
+        // them, and every earlier access to them is fenced by the barrier above
+        const long long np = pos + c;
+        if (np < T) {
+          long long tn = to_nudge;
+          if (a.P > 0) {
+            tn -= c;
+            if (tn == 0) tn = a.P;
+          }
+          int nc = (int)min((long long)(TS - np % TS), T - np);
+          if (a.P > 0 && tn <= nc) nc = (int)tn;
+          if (tid == 0) stage(np, nc);
+          staged_pos = np;
+          stage_pending = true;
+        }
+      }
+      if (!mma_wait()) { failed = true; break; }
     }
     {
       float v32[32];
@@ -1397,6 +1486,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
   } else if (tid == 0) {
     flags |= kStatusTimeout;
     if (!F32 && *issued > loaded) (void)mbar_wait_bounded(in_bar, (uint32_t)((loaded + 1) & 1));   // a copy in flight
+    if (F32 && stage_pending) (void)mbar_wait_bounded(in_bar, stage_phase);                            // staged inputs
   }
   if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
   if (flags) atomicOr(&a.status->flags, flags);
