@@ -21,7 +21,9 @@
 //
 // Every product accumulates in its own range of the 512 TMEM columns, so a result can
 // stay there while later products run: G2 takes its X operand straight from G1's
-// accumulator, and alpha reads Q from it.  The other drains (lane = row of the result)
+// accumulator, and alpha reads Q from it.  G4's X operand [Z D^{-1}; E^T] is written back
+// into tensor memory by G3's drain (tcgen05.st; its rows are the drain threads' lanes), so
+// G4 reads only its Y operand from shared memory.  The other drains (lane = row of the result)
 // write the next operand row-major: float4 stores into the K-major core-matrix layout,
 // free of bank conflicts; the transposed operands (W, alpha^T) are written with a
 // per-lane register rotation that spreads the lanes over all banks.  G2 is issued as
@@ -82,7 +84,7 @@ constexpr int TC_G3 = 128;    // [Z; F^T]
 constexpr int TC_G4 = 192;    // [Z D^{-1} Z^T; (Z E)^T]
 constexpr int TC_G5 = 256;    // 128 columns: [S alpha, alpha.alpha; S phi(q), phi(q).alpha]; G6 adds tril(aq) V
 constexpr int TC_G6 = 384;    // V^T alpha
-constexpr int TC_XL = 448;    // float32 I/O: the low part of G1's accumulator, G2's X lo
+constexpr int TC_XL = 448;    // X low parts: G2's (float32 I/O), then G4's (hi in TC_G2's columns)
 
 // High part of a 3xTF32 split: the value with the low 13 mantissa bits cleared
 // (exactly representable in tf32); the low part is x - hi.
@@ -1085,36 +1087,40 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
       if (!mma_run(ps, 3, 64)) { failed = true; break; }
     }
     {
-      float v32[32];
+      // G4's X operand [Z D^{-1}; E^T] goes straight back into tensor memory (this thread's lane
+      // is its row): hi into G2's columns (drained), lo into TC_XL; Z, G4's Y operand, goes to
+      // the L tile (hi) and Q tile 0 (lo)
+      float v32[32], xh[32], xl[32];
       tld32(TC_G3 + 32 * half, v32);
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int col0 = 32 * half + 16 * cc;
-        float (&v)[16] = *reinterpret_cast<float(*)[16]>(v32 + 16 * cc);
+      for (int j = 0; j < 32; j += 4) {
+        const int l = 32 * half + j;
+        const float id4[4] = {misc[Cf::M_ID + l], misc[Cf::M_ID + l + 1], misc[Cf::M_ID + l + 2],
+                              misc[Cf::M_ID + l + 3]};
+        if (row < 64) {   // Z (rows i, K = l); Z D^{-1} rows i
 #pragma unroll
-        for (int j = 0; j < 16; j += 4) {
-          const int l = col0 + j;
-          const float id4[4] = {misc[Cf::M_ID + l], misc[Cf::M_ID + l + 1], misc[Cf::M_ID + l + 2],
-                                misc[Cf::M_ID + l + 3]};
-          if (row < 64) {   // Z (rows i, K = l): hi -> L tile, lo -> Q tile 0; Z D^{-1} -> R / P rows i
-            const float zd[4] = {v[j] * id4[0], v[j + 1] * id4[1], v[j + 2] * id4[2], v[j + 3] * id4[3]};
-            st4_split(Cf::F_L + tk_off(row, l, 64), Cf::F_Q + tk_off(row, l, 64), v + j);
-            st4_split(Cf::F_R + tk_off(row, l, 64), Cf::F_P + tk_off(row, l, 64), zd);
-          } else {          // E^T (rows t, K = l), masked to directions of steps <= t
-            const int t = row - 64, lim = (t + 1) * R - 1;
-            float e4[4];
+          for (int m = 0; m < 4; ++m) xh[j + m] = v32[j + m] * id4[m];
+          st4_split(Cf::F_L + tk_off(row, l, 64), Cf::F_Q + tk_off(row, l, 64), v32 + j);
+        } else {          // E^T (rows t, K = l), masked to directions of steps <= t
+          const int t = row - 64, lim = (t + 1) * R - 1;
 #pragma unroll
-            for (int m = 0; m < 4; ++m) e4[m] = (l + m <= lim) ? v[j + m] * id4[m] : 0.f;
-            st4_split(Cf::F_R + tk_off(row, l, 64), Cf::F_P + tk_off(row, l, 64), e4);
-          }
+          for (int m = 0; m < 4; ++m) xh[j + m] = (l + m <= lim) ? v32[j + m] * id4[m] : 0.f;
         }
       }
+#pragma unroll
+      for (int j = 0; j < 32; ++j) xl[j] = xh[j] - tf32_hi(xh[j]);
+      const uint32_t tq = tmem + ((uint32_t)(32 * q4) << 16);
+      tc::tmem_st32(tq + (uint32_t)(TC_G2 + 32 * half), xh);
+      tc::tmem_st32(tq + (uint32_t)(TC_XL + 32 * half), xl);
     }
-    // ---------------- G4: [Z D^{-1} Z^T ; (Z E)^T] = [Z/D; E^T] Z^T  (M 128, N 64, K 64), 3xTF32
+    // ---------------- G4: [Z D^{-1} Z^T ; (Z E)^T] = [Z/D; E^T] Z^T  (M 128, N 64, K 64), 3xTF32, X in TMEM
     {
-      const MmaPass ps[3] = {{Cf::F_R, Cf::F_L, 128, 64, TC_G4, false},
-                             {Cf::F_P, Cf::F_L, 128, 64, TC_G4, true},
-                             {Cf::F_R, Cf::F_Q, 128, 64, TC_G4, true}};
+      MmaPass ps[3] = {{0, Cf::F_L, 128, 64, TC_G4, false},
+                       {0, Cf::F_L, 128, 64, TC_G4, true},
+                       {0, Cf::F_Q, 128, 64, TC_G4, true}};
+      ps[0].tx = TC_G2;
+      ps[1].tx = TC_XL;
+      ps[2].tx = TC_G2;
       if (!mma_run(ps, 3, 64)) { failed = true; break; }
     }
     {
