@@ -103,11 +103,12 @@ bool shape_built(int d, int dv, int r, bool bf16, vla_mode_t mode, int chunk, in
   return false;
 }
 
-// Argument checks shared by the device and host entry points; sets *ctas (sequential
-// and delta modes: CTAs per pair).  By default a cluster of two for d = 128 while 2 B H
-// CTAs fit on the SMs (one CTA of 4 d threads would be capped at 128 registers a thread
-// and spill); one otherwise (at d <= 64 the hand-off between two SMs costs more than the
-// issue slots it frees).
+// Argument checks shared by the device and host entry points; sets *ctas (CTAs per pair).
+// Sequential and delta modes: by default a cluster of two for d = 128 while 2 B H CTAs fit
+// on the SMs (one CTA of 4 d threads would be capped at 128 registers a thread and spill);
+// one otherwise (at d <= 64 the hand-off between two SMs costs more than the issue slots it
+// frees).  Chunked mode: a cluster of two (the A side and the S side of each chunk on two
+// SMs) while 2 B H CTAs fit on the SMs, else one.
 vla_err_t check_scan(vla_handle_t h, const char* fn, int B, int H, long long T, int d, int dv, int r, int P,
                      float eps_n, float tau, long long t0, vla_dtype_t io_dtype, vla_mode_t mode, int chunk,
                      int* ctas) {
@@ -125,7 +126,8 @@ vla_err_t check_scan(vla_handle_t h, const char* fn, int B, int H, long long T, 
   if (pairs > 0x7fffffffLL) return fail(h, VLA_ERR_INVALID_ARG, f + ": B*H too large");
   if (d != dv) return fail(h, VLA_ERR_UNSUPPORTED, f + ": built only for d == dv");
   const int auto_ctas = (d == 128 && 2 * pairs <= h->sm_count) ? 2 : 1;
-  *ctas = mode == VLA_SEQUENTIAL ? (chunk != 0 ? chunk : auto_ctas) : mode == VLA_DELTA ? auto_ctas : 0;
+  const int chunk_ctas = (2 * pairs <= h->sm_count) ? 2 : 1;
+  *ctas = mode == VLA_SEQUENTIAL ? (chunk != 0 ? chunk : auto_ctas) : mode == VLA_DELTA ? auto_ctas : chunk_ctas;
   const bool bf16 = io_dtype == VLA_BF16;
   if (!shape_built(d, dv, r, bf16, mode, chunk, *ctas)) {
     char buf[400];
@@ -148,7 +150,7 @@ cudaError_t dispatch(const vla::ScanArgs& a, int d, int r, bool bf16, vla_mode_t
   bool built = false;
   cudaError_t e = mode == VLA_SEQUENTIAL ? vla::launch_seq(d, r, bf16, ctas, a, s, &built)
                   : mode == VLA_DELTA    ? vla::launch_delta(d, r, bf16, ctas, a, s, &built)
-                                         : vla::launch_chunked(d, r, bf16, chunk, a, s, &built);
+                                         : vla::launch_chunked(d, r, bf16, chunk, ctas, a, s, &built);
   return built ? e : cudaErrorNotSupported;
 }
 

@@ -48,6 +48,17 @@
 // guard inside the chunk; the chunk is then taken step by step on CUDA cores.
 // Chunks end at nudge steps (A += eps_n I is not a rank-1 update).
 //
+// Few pairs (two CTAs per pair fit on the SMs): each pair runs on a cluster of two CTAs,
+// one SM each.  CTA 0 carries A (the prologue's [U; Sigma], G1..G4, the LDL^T, the A update
+// and alpha), CTA 1 carries S (phi(q), V, n and 1/den, G5, G6, the renormalisation, the
+// outputs and S).  The only data that crosses is alpha, 64 x 64 fp32: CTA 0 writes it into
+// its own AL tile and sends it with one bulk copy into CTA 1's AL tile, completing on an
+// mbarrier there; CTA 1 arrives on an mbarrier of CTA 0 once it is done with it.  So the A
+// side, the longer chain, runs up to a chunk ahead of the S side.  Each side computes what
+// the one-CTA form computes, in the same order, so the two forms agree bit for bit, except
+// in a chunk where the guard fires: the A side then takes alpha step by step, and the S side
+// its chunk path.
+//
 // Precision: operands are fp32 in shared memory, read by the tensor core as tf32, which
 // drops the low 13 mantissa bits (truncation).  The products that carry A forward (G1's
 // A_0, G3, G4) are 3xTF32: the fp32 operand x is its own high part, lo = x - hi is stored
@@ -166,7 +177,8 @@ struct MmaPass {
 
 }  // namespace chk
 
-template <int R, typename TIO>
+// SPLIT: a cluster of two CTAs per pair, CTA 0 the A side and CTA 1 the S side (above).
+template <int R, typename TIO, bool SPLIT>
 __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
   using namespace chk;
   using Cf = Cfg<R, TIO>;
@@ -184,10 +196,15 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
   uint32_t* tslot = reinterpret_cast<uint32_t*>(in_bar + 2);
   volatile int* flag = reinterpret_cast<volatile int*>(in_bar + 3);
   volatile int* issued = reinterpret_cast<volatile int*>(in_bar + 4);   // the last tile whose copy was issued
+  uint64_t* full_bar = in_bar + 5;    // SPLIT, S side: alpha has landed in AL
+  uint64_t* empty_bar = in_bar + 6;   // SPLIT, A side: the S side is done with the alpha it was sent
   const uint32_t sbase = smem_u32(sf);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const long long pair = blockIdx.x;
+  const uint32_t crank = SPLIT ? cluster_ctarank() : 0u;
+  const bool doA = !SPLIT || crank == 0;   // this CTA carries A
+  const bool doS = !SPLIT || crank == 1;   // this CTA carries S
+  const long long pair = SPLIT ? (long long)(blockIdx.x >> 1) : (long long)blockIdx.x;
   const long long T = a.T;
   const TIO* gq = static_cast<const TIO*>(a.q) + pair * T * D;
   const TIO* gk = static_cast<const TIO*>(a.k) + pair * T * D;
@@ -201,14 +218,18 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
   // ---- state into the operand tiles
   for (int e = tid; e < D * D; e += NT) {
     const int i = e >> 6, j = e & 63;
-    sf[Cf::F_A + tk_off(i, j, 64)] = gA[e];
-    sf[Cf::F_S + tk_off(i, j, 64)] = gS[e];
+    if (doA) sf[Cf::F_A + tk_off(i, j, 64)] = gA[e];
+    if (doS) sf[Cf::F_S + tk_off(i, j, 64)] = gS[e];
   }
-  if (tid < D) misc[Cf::M_N + tid] = gn[tid];
+  if (doS && tid < D) misc[Cf::M_N + tid] = gn[tid];
   if (tid == 0) misc[Cf::M_SSV] = 0.f;   // ||S||^2 of the initial state: computed by the first chunk
   if (tid == 0) {
     mbar_init(in_bar, 1);
     mbar_init(mma_bar, 1);
+    if (SPLIT) {
+      mbar_init(full_bar, 1);      // the S side's own arrival with the bytes it expects
+      mbar_init(empty_bar, NT);    // every thread of the S side, remotely
+    }
     fence_mbar_init();
     *flag = 0;
   }
@@ -216,7 +237,13 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
+  if constexpr (SPLIT) cluster_sync_all();   // both CTAs' barriers are initialised before either uses the other's
   const uint32_t tmem = *tslot;
+  // SPLIT: alphas sent (A side) and received (S side); the peer's AL tile and barriers
+  uint32_t n_sent = 0, n_recv = 0;
+  const uint32_t peer_al = SPLIT ? mapa_shared(smem_u32(sf + Cf::F_AL), crank ^ 1u) : 0u;
+  const uint32_t peer_full = SPLIT ? mapa_shared(smem_u32(full_bar), crank ^ 1u) : 0u;
+  const uint32_t peer_empty = SPLIT ? mapa_shared(smem_u32(empty_bar), crank ^ 1u) : 0u;
 
   const int ntiles = (int)((T + TS - 1) / TS);
   auto issue = [&](int tile) {  // one thread
@@ -224,26 +251,30 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     const long long t_start = (long long)tile * TS;
     const int nst = (int)min((long long)TS, T - t_start);
     const uint32_t qb = (uint32_t)nst * D * sizeof(TIO), ub = (uint32_t)nst * R * D * sizeof(TIO);
-    mbar_arrive_expect_tx(in_bar, 3 * qb + ub);
-    bulk_g2s(raw, gq + t_start * D, qb, in_bar);
+    // each side copies what it reads: k both, u the A side, q and v the S side
+    mbar_arrive_expect_tx(in_bar, qb + (doS ? 2 * qb : 0u) + (doA ? ub : 0u));
+    if (doS) bulk_g2s(raw, gq + t_start * D, qb, in_bar);
     bulk_g2s(raw + Cf::QB, gk + t_start * D, qb, in_bar);
-    bulk_g2s(raw + 2 * Cf::QB, gv + t_start * D, qb, in_bar);
-    bulk_g2s(raw + 3 * Cf::QB, gu + t_start * R * D, ub, in_bar);
+    if (doS) bulk_g2s(raw + 2 * Cf::QB, gv + t_start * D, qb, in_bar);
+    if (doA) bulk_g2s(raw + 3 * Cf::QB, gu + t_start * R * D, ub, in_bar);
   };
   if (!F32 && tid == 0) issue(0);
   // Float32 I/O has no raw stage: a chunk's q, k, v, u are copied into the tiles that are free
   // from the previous chunk's G6 until this chunk's prologue (q -> PQ, k -> Q tile 1, v -> vb,
   // where it stays as it is, u -> AL), issued right after that G6 so that they land beside it.
+  // The A side of a cluster has neither G5 nor G6: it takes u into PQ (AL carries alpha) and
+  // issues the next chunk's k and u as soon as its G1 is done.
+  constexpr int F_UST = SPLIT ? Cf::F_PQ : Cf::F_AL;   // where a float32 chunk's u is staged
   long long staged_pos = -1;   // the chunk whose inputs were issued last (all threads agree)
   bool stage_pending = false;  // issued and not yet waited for
   uint32_t stage_phase = 0;
   auto stage = [&](long long p0, int cc) {   // one thread
     const uint32_t qb = (uint32_t)cc * D * sizeof(TIO), ub = (uint32_t)cc * R * D * sizeof(TIO);
-    mbar_arrive_expect_tx(in_bar, 3 * qb + ub);
-    bulk_g2s(sf + Cf::F_PQ, gq + p0 * D, qb, in_bar);
+    mbar_arrive_expect_tx(in_bar, qb + (doS ? 2 * qb : 0u) + (doA ? ub : 0u));
+    if (doS) bulk_g2s(sf + Cf::F_PQ, gq + p0 * D, qb, in_bar);
     bulk_g2s(sf + Cf::F_Q + TILE, gk + p0 * D, qb, in_bar);
-    bulk_g2s(vb, gv + p0 * D, qb, in_bar);
-    bulk_g2s(sf + Cf::F_AL, gu + p0 * R * D, ub, in_bar);
+    if (doS) bulk_g2s(vb, gv + p0 * D, qb, in_bar);
+    if (doA) bulk_g2s(sf + F_UST, gu + p0 * R * D, ub, in_bar);
   };
 
   uint32_t mma_phase = 0;
@@ -396,6 +427,57 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
       if (to_nudge == 0) to_nudge = a.P;
     }
   };
+  // float32 I/O: issue the copies of the next chunk's inputs (all threads call it; the tiles
+  // they land in must be free, every earlier access to them fenced by a barrier)
+  auto stage_next = [&]() {
+    const long long np = pos + c;
+    if (np >= T) return;
+    long long tn = to_nudge;
+    if (a.P > 0) {
+      tn -= c;
+      if (tn == 0) tn = a.P;
+    }
+    int nc = (int)min((long long)(TS - np % TS), T - np);
+    if (a.P > 0 && tn <= nc) nc = (int)tn;
+    if (tid == 0) stage(np, nc);
+    staged_pos = np;
+    stage_pending = true;
+  };
+  // SPLIT, S side: every thread signals the A side that it is done with the chunk's alpha
+  auto release_alpha = [&]() {
+    if constexpr (SPLIT) mbar_arrive_remote(peer_empty);
+  };
+  // A_1 = A_0 - Z D^{-1} Z^T (+ eps_n I at a nudge): row `row`, columns col0 .. col0 + 15, from
+  // the 16 values of G4's result in v
+  auto a_update = [&](int row, int col0, const float (&v)[16], bool nudge) {
+#pragma unroll
+    for (int j = 0; j < 16; j += 4) {
+      float4* ap = reinterpret_cast<float4*>(sf + Cf::F_A + tk_off(row, col0 + j, 64));
+      float4 x = *ap;
+      x.x -= v[j];
+      x.y -= v[j + 1];
+      x.z -= v[j + 2];
+      x.w -= v[j + 3];
+      if (nudge && (row >> 2) == ((col0 + j) >> 2)) {
+        const int dg = row & 3;
+        if (dg == 0) x.x += a.eps_n;
+        if (dg == 1) x.y += a.eps_n;
+        if (dg == 2) x.z += a.eps_n;
+        if (dg == 3) x.w += a.eps_n;
+      }
+      *ap = x;
+    }
+  };
+  // SPLIT, A side: send the chunk's alpha (the AL tile, written by all threads) into the S
+  // side's AL tile; the copy completes on the S side's full_bar
+  auto ship_alpha = [&]() {
+    if constexpr (SPLIT) {
+      fence_proxy_async_smem();   // the generic writes of AL, visible to the bulk copy
+      __syncthreads();
+      if (tid == 0) bulk_s2s_cluster(peer_al, sf + Cf::F_AL, TILE * sizeof(float), peer_full);
+      ++n_sent;
+    }
+  };
   int loaded = -1;
   while (pos < T && !failed) {
     // ---------------- schedule: chunk [pos, pos + c) inside one input tile, ending at a nudge
@@ -450,12 +532,12 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
           x[2 * m + 1] = f.y;
         }
       };
-      for (int f = tid; f < 64 * 8; f += NT) {   // U rows a (64 x 8 pieces)
+      for (int f = tid; doA && f < 64 * 8; f += NT) {   // U rows a (64 x 8 pieces)
         const int arow = (f >> 6) * 8 + (f & 7), pc = ((f & 7) + (f >> 3)) & 7;
         float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         if (arow / R < c) {
           if constexpr (F32)
-            ld8s(sf + Cf::F_AL + arow * D + 8 * pc, x);
+            ld8s(sf + F_UST + arow * D + 8 * pc, x);
           else
             unpack8(*reinterpret_cast<const uint4*>(ru + (ts * R + arow) * D + 8 * pc), x);
         }
@@ -479,7 +561,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
             const int t = (f >> 6) * 8 + (f & 7), pc = ((f & 7) + (f >> 3)) & 7;
             if (f < C * 8 && t < c) {
               ld8s(sf + Cf::F_Q + TILE + t * D + 8 * pc, kr[s]);
-              ld8s(sf + Cf::F_PQ + t * D + 8 * pc, qr[s]);
+              if (doS) ld8s(sf + Cf::F_PQ + t * D + 8 * pc, qr[s]);
             }
           }
           __syncthreads();
@@ -496,7 +578,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
 #pragma unroll
               for (int m = 0; m < 8; ++m) {
                 kx[m] = kr[s][m];
-                qx[m] = qr[s][m];
+                qx[m] = doS ? qr[s][m] : 0.f;
               }
             } else {
               const int off = (ts + t) * D + 8 * pc;
@@ -518,18 +600,22 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
             const int col = 8 * pc + 4 * h;
             const float* k4 = kx + 4 * h;
             const float* q4p = qx + 4 * h;
-            st4(Cf::F_P + tk_off(64 + t, col, 64), k4[0] * kInvSqrtD, k4[1] * kInvSqrtD, k4[2] * kInvSqrtD,
-                k4[3] * kInvSqrtD);
-            if constexpr (F32) {
-              const float s4[4] = {k4[0] * kInvSqrtD, k4[1] * kInvSqrtD, k4[2] * kInvSqrtD, k4[3] * kInvSqrtD};
-              st4_lo(Cf::F_Q + tk_off(64 + t, col, 64), s4);
+            if (doA) {
+              st4(Cf::F_P + tk_off(64 + t, col, 64), k4[0] * kInvSqrtD, k4[1] * kInvSqrtD, k4[2] * kInvSqrtD,
+                  k4[3] * kInvSqrtD);
+              if constexpr (F32) {
+                const float s4[4] = {k4[0] * kInvSqrtD, k4[1] * kInvSqrtD, k4[2] * kInvSqrtD, k4[3] * kInvSqrtD};
+                st4_lo(Cf::F_Q + tk_off(64 + t, col, 64), s4);
+              }
             }
-            st4(Cf::F_PQ + tk_off(t, col, 64), q4p[0], q4p[1], q4p[2], q4p[3]);
-            *reinterpret_cast<float4*>(pk + t * PLD + col) = make_float4(k4[0], k4[1], k4[2], k4[3]);
-            *reinterpret_cast<float4*>(pq + t * PLD + col) = make_float4(q4p[0], q4p[1], q4p[2], q4p[3]);
+            if (doS) {
+              st4(Cf::F_PQ + tk_off(t, col, 64), q4p[0], q4p[1], q4p[2], q4p[3]);
+              *reinterpret_cast<float4*>(pk + t * PLD + col) = make_float4(k4[0], k4[1], k4[2], k4[3]);
+              *reinterpret_cast<float4*>(pq + t * PLD + col) = make_float4(q4p[0], q4p[1], q4p[2], q4p[3]);
+            }
           }
           if constexpr (F32) {   // V was staged into vb as it is; rows past c are zeroed
-            if (t >= c) {
+            if (doS && t >= c) {
               *reinterpret_cast<float4*>(vb + t * 64 + 8 * pc) = make_float4(0.f, 0.f, 0.f, 0.f);
               *reinterpret_cast<float4*>(vb + t * 64 + 8 * pc + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
             }
@@ -545,8 +631,13 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
           if (t < c) {
             const int off = (ts + t) * D + 8 * pc;
             unpack8(*reinterpret_cast<const uint4*>(rk + off), kx);
-            unpack8(*reinterpret_cast<const uint4*>(rq + off), qx);
-            vw = *reinterpret_cast<const uint4*>(rv + off);
+            if (doS) {   // the A side's stage holds no q or v
+              unpack8(*reinterpret_cast<const uint4*>(rq + off), qx);
+              vw = *reinterpret_cast<const uint4*>(rv + off);
+            } else {
+#pragma unroll
+              for (int m = 0; m < 8; ++m) qx[m] = 0.f;
+            }
 #pragma unroll
             for (int m = 0; m < 8; ++m) {
               kx[m] = phi_fast(kx[m]);
@@ -561,22 +652,27 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
             const int col = 8 * pc + 4 * h;
             const float* k4 = kx + 4 * h;
             const float* q4p = qx + 4 * h;
-            st4(Cf::F_P + tk_off(64 + t, col, 64), k4[0] * kInvSqrtD, k4[1] * kInvSqrtD, k4[2] * kInvSqrtD,
-                k4[3] * kInvSqrtD);
-            st4(Cf::F_PQ + tk_off(t, col, 64), q4p[0], q4p[1], q4p[2], q4p[3]);
-            *reinterpret_cast<float4*>(pk + t * PLD + col) = make_float4(k4[0], k4[1], k4[2], k4[3]);
-            *reinterpret_cast<float4*>(pq + t * PLD + col) = make_float4(q4p[0], q4p[1], q4p[2], q4p[3]);
+            if (doA)
+              st4(Cf::F_P + tk_off(64 + t, col, 64), k4[0] * kInvSqrtD, k4[1] * kInvSqrtD, k4[2] * kInvSqrtD,
+                  k4[3] * kInvSqrtD);
+            if (doS) {
+              st4(Cf::F_PQ + tk_off(t, col, 64), q4p[0], q4p[1], q4p[2], q4p[3]);
+              *reinterpret_cast<float4*>(pk + t * PLD + col) = make_float4(k4[0], k4[1], k4[2], k4[3]);
+              *reinterpret_cast<float4*>(pq + t * PLD + col) = make_float4(q4p[0], q4p[1], q4p[2], q4p[3]);
+            }
           }
-          *reinterpret_cast<uint4*>(vb + t * 64 + 8 * pc) = vw;
+          if (doS) *reinterpret_cast<uint4*>(vb + t * 64 + 8 * pc) = vw;
         }
       }
       for (int e4 = tid; e4 < (64 - C) * 16; e4 += NT) {   // zero rows C..63 of Sigma and phi(q)
         const int t = C + (e4 >> 4), col = (e4 & 15) * 4;
-        st4(Cf::F_P + tk_off(64 + t, col, 64), 0.f, 0.f, 0.f, 0.f);
-        st4(Cf::F_PQ + tk_off(t, col, 64), 0.f, 0.f, 0.f, 0.f);
-        if constexpr (F32) st4(Cf::F_Q + tk_off(64 + t, col, 64), 0.f, 0.f, 0.f, 0.f);
+        if (doA) st4(Cf::F_P + tk_off(64 + t, col, 64), 0.f, 0.f, 0.f, 0.f);
+        if (doS) st4(Cf::F_PQ + tk_off(t, col, 64), 0.f, 0.f, 0.f, 0.f);
+        if (F32 && doA) st4(Cf::F_Q + tk_off(64 + t, col, 64), 0.f, 0.f, 0.f, 0.f);
       }
       __syncthreads();
+      if (doA && tid < D) misc[Cf::M_SL + tid] = sf[Cf::F_P + tk_off(64 + c - 1, tid, 64)];   // s of the chunk's last step
+      if (doS) {
       // n_t = n_{t-1} + phi(k_t): column i, four segments of C/4 steps (one per thread)
       constexpr int SEG = C / 4;
       const int ci = tid & 63, sg4 = tid >> 6;
@@ -589,7 +685,6 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
         for (int j = 0; j < SEG; ++j) tot += kseg[j];
         misc[Cf::M_NSEG + sg4 * 64 + ci] = tot;
       }
-      if (tid < D) misc[Cf::M_SL + tid] = sf[Cf::F_P + tk_off(64 + c - 1, tid, 64)];   // s of the chunk's last step
 #pragma unroll
       for (int j = 0; j < SEG; ++j) qseg[j] = pq[(SEG * sg4 + j) * PLD + ci];
       __syncthreads();
@@ -647,19 +742,21 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
         }
       }
       __syncthreads();
+      }   // doS
       // the raw stage is free once the tile's last chunk is converted
       if (!F32 && tid == 0 && ts + c == TS && tile + 1 < ntiles) {
         fence_proxy_async_smem();
         issue(tile + 1);
       }
       // A's low part -> R tile 1 (A itself is the high part)
-      for (int e4 = tid; e4 < TILE / 4; e4 += NT) {
+      for (int e4 = tid; doA && e4 < TILE / 4; e4 += NT) {
         const float4 x = *reinterpret_cast<const float4*>(sf + Cf::F_A + 4 * e4);
         const float xv[4] = {x.x, x.y, x.z, x.w};
         st4_lo(Cf::F_R + TILE + 4 * e4, xv);
       }
     }
 
+    if (doA) {   // ======== the A side: G1 .. G4, the LDL^T, A and alpha
     // ---------------- G1: [W^T; Q^T] = [U; Sigma] A_0^T  (M 128, N 64, K 64), A_0 hi + lo (and, with
     // float32 I/O, [U; Sigma] lo)
     {
@@ -668,6 +765,8 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
                              {Cf::F_Q, Cf::F_A, 128, 64, TC_G1, true}};
       if (!mma_run(ps, F32 ? 3 : 2, 64)) { failed = true; break; }
     }
+    // the A side of a cluster: the next chunk's u (PQ) and k (Q tile 1), free once G1 is done
+    if constexpr (SPLIT && F32) stage_next();
     // ---------------- G2: [G - I; H^T] = [W^T; Q^T] U^T  (M 128, N 64, K 64), X read from G1's
     // accumulator in tensor memory; it runs while G1's W is drained.  Q^T stays there for alpha.
     if constexpr (F32) {
@@ -985,6 +1084,11 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     if (bad) {
       // ============ fallback: the chunk step by step on CUDA cores
       ++fallback_cnt;
+      if constexpr (SPLIT) {   // alpha goes into AL step by step: the S side must be done with the last one
+        if (tid == 0 && n_sent > 0 && !mbar_wait_cluster_bounded(empty_bar, (n_sent - 1) & 1u)) *flag = 1;
+        __syncthreads();
+        if (*flag) { failed = true; break; }
+      }
       float* vec = misc + Cf::M_VEC;     // u, then s
       float* vec2 = misc + Cf::M_VEC2;   // z, alpha
       const int ar = tid >> 2, cq = tid & 3;   // row of A / S and a 16-column quarter
@@ -1023,6 +1127,10 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
         ap += __shfl_xor_sync(0xffffffffu, ap, 2);
         if (cq == 0) vec2[ar] = ap;
         __syncthreads();
+        if constexpr (SPLIT) {   // alpha_t -> AL row t; the S side takes the chunk from there
+          if (tid < 64) sf[Cf::F_AL + tk_off(t, tid, 64)] = vec2[tid];
+          continue;
+        }
         // S += v alpha^T, then the norm
         const float vr = to_f32(vb[t * 64 + ar]);   // v of step t
         float sq = 0.f;
@@ -1051,7 +1159,12 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
         if (cq == 0) go[st * D + ar] = from_f32<TIO>(op * misc[Cf::M_RDEN + t]);
         __syncthreads();
       }
-      if (tid == 0) misc[Cf::M_SSV] = 0.f;   // S changed step by step: its norm is recomputed
+      if constexpr (SPLIT) {
+        for (int e = tid; e < (64 - c) * 64; e += NT) sf[Cf::F_AL + tk_off(c + (e >> 6), e & 63, 64)] = 0.f;
+        ship_alpha();
+      } else {
+        if (tid == 0) misc[Cf::M_SSV] = 0.f;   // S changed step by step: its norm is recomputed
+      }
       advance(c);
       continue;
     }
@@ -1121,27 +1234,68 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
       ps[0].tx = TC_G2;
       ps[1].tx = TC_XL;
       ps[2].tx = TC_G2;
-      if (!mma_run(ps, 3, 64)) { failed = true; break; }
+      sync_tc();
+      if (tid == 0) {
+        mma_issue(ps, 3, 64);
+        // the A side of a cluster writes alpha into AL next: the S side must be done with the last one
+        if (SPLIT && n_sent > 0 && !mbar_wait_cluster_bounded(empty_bar, (n_sent - 1) & 1u)) *flag = 1;
+      }
+      if (!mma_wait()) { failed = true; break; }
     }
+    }   // doA
     {
       float v32[32], al32[32];
       float an = 0.f;
-      tld32(TC_G4 + 32 * half, v32);
+      if (doA) tld32(TC_G4 + 32 * half, v32);
+      if constexpr (SPLIT) {
+        if (doS) {   // the S side of a cluster: wait for the chunk's alpha in AL
+          if (tid == 0) {
+            mbar_arrive_expect_tx(full_bar, TILE * sizeof(float));
+            if (!mbar_wait_cluster_bounded(full_bar, n_recv & 1u)) *flag = 1;
+          }
+          ++n_recv;
+          __syncthreads();
+          if (*flag) { failed = true; break; }
+        }
+      }
       if (row >= 64) {   // alpha_t = Q_t - (Z E)_t (+ eps_n s_t at a nudge step), rows t (warp-uniform)
         const int t = row - 64;
-        tld32(TC_G1 + 32 * half, al32);   // Q^T rows, from G1's accumulator
+        if (doA) {
+          tld32(TC_G1 + 32 * half, al32);   // Q^T rows, from G1's accumulator
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          float x = al32[j] - v32[j];
-          if (nudge && t == c - 1) x = fmaf(a.eps_n, misc[Cf::M_SL + 32 * half + j], x);
-          if (t >= c) x = 0.f;
-          al32[j] = x;
-          an = fmaf(x, x, an);
+          for (int j = 0; j < 32; ++j) {
+            float x = al32[j] - v32[j];
+            if (nudge && t == c - 1) x = fmaf(a.eps_n, misc[Cf::M_SL + 32 * half + j], x);
+            if (t >= c) x = 0.f;
+            al32[j] = x;
+            an = fmaf(x, x, an);
+          }
+#pragma unroll
+          for (int j = 0; j < 32; j += 4)
+            st4(Cf::F_AL + tk_off(t, 32 * half + j, 64), al32[j], al32[j + 1], al32[j + 2], al32[j + 3]);
+        } else {   // the S side of a cluster: the same values, from the alpha it was sent
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            const float4 x4 = *reinterpret_cast<const float4*>(sf + Cf::F_AL + tk_off(t, 32 * half + j, 64));
+            al32[j] = x4.x;
+            al32[j + 1] = x4.y;
+            al32[j + 2] = x4.z;
+            al32[j + 3] = x4.w;
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) an = fmaf(al32[j], al32[j], an);
         }
+        if (doS) misc[Cf::M_AN2 + 64 * half + t] = an;   // |alpha_t|^2, two halves
+      }
+      if (SPLIT && doA) {   // the A side of a cluster: the A update, then alpha to the S side
+        if (row < 64) {
 #pragma unroll
-        for (int j = 0; j < 32; j += 4)
-          st4(Cf::F_AL + tk_off(t, 32 * half + j, 64), al32[j], al32[j + 1], al32[j + 2], al32[j + 3]);
-        misc[Cf::M_AN2 + 64 * half + t] = an;   // |alpha_t|^2, two halves
+          for (int cc = 0; cc < 2; ++cc)
+            a_update(row, 32 * half + 16 * cc, *reinterpret_cast<float(*)[16]>(v32 + 16 * cc), nudge);
+        }
+        ship_alpha();
+        advance(c);
+        continue;
       }
       // ---------------- G5: [S alpha ; S phi(q) | alpha.alpha ; phi(q).alpha] = [alpha; phi(q)] [S; alpha]^T,
       // issued as soon as alpha is written; the rest of G4's drain runs beside it.  With float32
@@ -1172,24 +1326,8 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
       for (int cc = 0; cc < 2; ++cc) {
         const int col0 = 32 * half + 16 * cc;
         float (&v)[16] = *reinterpret_cast<float(*)[16]>(v32 + 16 * cc);
-        if (row < 64) {   // A_1 = A_0 - Z D^{-1} Z^T (+ eps_n I at a nudge)
-#pragma unroll
-          for (int j = 0; j < 16; j += 4) {
-            float4* ap = reinterpret_cast<float4*>(sf + Cf::F_A + tk_off(row, col0 + j, 64));
-            float4 x = *ap;
-            x.x -= v[j];
-            x.y -= v[j + 1];
-            x.z -= v[j + 2];
-            x.w -= v[j + 3];
-            if (nudge && (row >> 2) == ((col0 + j) >> 2)) {
-              const int dg = row & 3;
-              if (dg == 0) x.x += a.eps_n;
-              if (dg == 1) x.y += a.eps_n;
-              if (dg == 2) x.z += a.eps_n;
-              if (dg == 3) x.w += a.eps_n;
-            }
-            *ap = x;
-          }
+        if (row < 64) {
+          if (doA) a_update(row, col0, v, nudge);
         } else if (row - 64 < C) {
           // alpha^T (rows j, K = t): lane group g = lane / 4 writes column col0 + ((jj + g) & 15) in
           // store jj, so the 8 groups hit 8 different core-matrix rows (32 distinct banks)
@@ -1361,6 +1499,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
           if (tid == 0) misc[Cf::M_SSV] = 0.f;   // S changed step by step: its norm is recomputed
           tc::fence_before_sync();
           __syncthreads();
+          release_alpha();
           advance(c);
           continue;
         }
@@ -1394,23 +1533,9 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
                              {Cf::F_T6, Cf::F_P + Cf::T6_A, 128, 64, TC_G6, true}};
       sync_tc();
       if (tid == 0) mma_issue(ps, F32 ? 6 : 2, C);
-      if constexpr (F32) {
-        // the next chunk's inputs into AL, PQ, Q tile 1 and vb: G6 and its drain do not touch
-        // them, and every earlier access to them is fenced by the barrier above
-        const long long np = pos + c;
-        if (np < T) {
-          long long tn = to_nudge;
-          if (a.P > 0) {
-            tn -= c;
-            if (tn == 0) tn = a.P;
-          }
-          int nc = (int)min((long long)(TS - np % TS), T - np);
-          if (a.P > 0 && tn <= nc) nc = (int)tn;
-          if (tid == 0) stage(np, nc);
-          staged_pos = np;
-          stage_pending = true;
-        }
-      }
+      // the next chunk's inputs into AL, PQ, Q tile 1 and vb: G6 and its drain do not touch
+      // them, and every earlier access to them is fenced by the barrier above
+      if constexpr (F32) stage_next();
       if (!mma_wait()) { failed = true; break; }
     }
     {
@@ -1476,6 +1601,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     }
     tc::fence_before_sync();
     __syncthreads();
+    release_alpha();
     advance(c);
   }
 
@@ -1485,14 +1611,21 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
   if (!failed) {
     for (int e = tid; e < D * D; e += NT) {
       const int i = e >> 6, j = e & 63;
-      gA[e] = sf[Cf::F_A + tk_off(i, j, 64)];
-      gS[e] = sf[Cf::F_S + tk_off(i, j, 64)];
+      if (doA) gA[e] = sf[Cf::F_A + tk_off(i, j, 64)];
+      if (doS) gS[e] = sf[Cf::F_S + tk_off(i, j, 64)];
     }
-    if (tid < D) gn[tid] = misc[Cf::M_N + tid];
+    if (doS && tid < D) gn[tid] = misc[Cf::M_N + tid];
   } else if (tid == 0) {
     flags |= kStatusTimeout;
     if (!F32 && *issued > loaded) (void)mbar_wait_bounded(in_bar, (uint32_t)((loaded + 1) & 1));   // a copy in flight
     if (F32 && stage_pending) (void)mbar_wait_bounded(in_bar, stage_phase);                            // staged inputs
+  }
+  if constexpr (SPLIT) {
+    // The A side's AL is the source of the last copy: it stays until the S side has taken it
+    // (or the wait gives up, long after any copy has landed); then neither CTA touches the
+    // other's shared memory again
+    if (doA && tid == 0 && n_sent > 0) (void)mbar_wait_cluster_bounded(empty_bar, (n_sent - 1) & 1u);
+    cluster_sync_all();
   }
   if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
   if (flags) atomicOr(&a.status->flags, flags);
@@ -1503,14 +1636,33 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
   }
 }
 
+// ctas = 2: a cluster of two CTAs per pair (the A side and the S side)
 template <int R, typename TIO>
-cudaError_t launch_chunk_t(const ScanArgs& a, cudaStream_t s) {
+cudaError_t launch_chunk_t(const ScanArgs& a, int ctas, cudaStream_t s) {
   using Cf = chk::Cfg<R, TIO>;
-  auto kern = chunk_scan_kernel<R, TIO>;
+  if (ctas != 2) {
+    auto kern = chunk_scan_kernel<R, TIO, false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::bytes);
+    if (e != cudaSuccess) return e;
+    kern<<<a.pairs, chk::NT, Cf::bytes, s>>>(a);
+    return cudaGetLastError();
+  }
+  auto kern = chunk_scan_kernel<R, TIO, true>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::bytes);
   if (e != cudaSuccess) return e;
-  kern<<<a.pairs, chk::NT, Cf::bytes, s>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2 * a.pairs), 1, 1);
+  cfg.blockDim = dim3(chk::NT, 1, 1);
+  cfg.dynamicSmemBytes = Cf::bytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 }  // namespace vla

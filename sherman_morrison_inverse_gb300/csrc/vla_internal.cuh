@@ -50,7 +50,7 @@ struct ScanArgs {
 
 // Host-side launchers; each returns cudaSuccess or the launch error.
 cudaError_t launch_seq(int d, int r, bool bf16, int ctas, const ScanArgs& a, cudaStream_t s, bool* built);
-cudaError_t launch_chunked(int d, int r, bool bf16, int chunk, const ScanArgs& a, cudaStream_t s,
+cudaError_t launch_chunked(int d, int r, bool bf16, int chunk, int ctas, const ScanArgs& a, cudaStream_t s,
                            bool* built);
 cudaError_t launch_delta(int d, int r, bool bf16, int ctas, const ScanArgs& a, cudaStream_t s, bool* built);
 cudaError_t launch_project_u(int d, bool bf16, const void* k, const float* W, void* u, long long n, int r,
@@ -193,6 +193,18 @@ __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, u
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
           smem_u32(dst_smem)),
       "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Shared -> shared bulk copy into another CTA of the cluster: dst and bar are that CTA's
+// addresses (mapa_shared), completion is a complete_tx of `bytes` on its mbarrier bar
+// (16-byte aligned addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_s2s_cluster(uint32_t dst_cluster, const void* src_smem, uint32_t bytes,
+                                                 uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst_cluster),
+      "r"(smem_u32(src_smem)), "r"(bytes), "r"(bar_cluster)
       : "memory");
 }
 

@@ -8,6 +8,13 @@ float64 oracle and against the sequential kernel at the gate of its I/O type
 cases: ragged lengths, nudges that split chunks (t0 phase), renormalisation
 firing (the exact per-step path) and the singularity guard (the step-by-step
 fallback).
+
+While two CTAs per pair fit on the SMs, each pair runs on a cluster of two (the A
+side and the S side of every chunk on two SMs, alpha handed over through
+distributed shared memory); with more pairs, on one CTA.  Both forms compute the
+same values in the same order, so they must agree bit for bit wherever the guard
+does not fire; the edge cases (few pairs) run the cluster form, the full
+workloads of 128 and 256 pairs the one-CTA form.
 """
 from __future__ import annotations
 
@@ -89,9 +96,33 @@ def test_chunked_f32_workload_parity():
     _check(oracle.errors(*got[:4], *seq[:4]), TOL_F32, f"chunked vs sequential {w.name}")
 
 
+def _one_cta_pairs():
+    """The smallest pair count that no longer fits two CTAs per pair on the SMs."""
+    return torch.cuda.get_device_properties(0).multi_processor_count // 2 + 1
+
+
 @pytest.mark.parametrize("io", ["bf16", "f32"])
-def test_chunked_guard_falls_back_step_by_step(io):
-    N, T = 2, 40
+@pytest.mark.parametrize("r,T,P,tau,t0", [(1, 300, 50, 12.0, 7), (4, 130, 20, 6.0, 3)])
+def test_chunked_one_cta_and_cluster_agree(io, r, T, P, tau, t0):
+    """The first three pairs alone (a cluster of two CTAs each) and inside a launch of
+    SMs / 2 + 1 pairs (one CTA each): the same bits in o, A, S and n, with nudges that
+    split chunks, a t0 phase, a ragged last chunk and renormalisation firing."""
+    N = _one_cta_pairs()
+    x = workloads.gaussian_inputs(N, T, 64, 64, r, io, seed=900 + r)
+    kw = dict(P=P, eps_n=1e-3, tau=tau, t0=t0)
+    one = gpu_scan(x, 1, N, mode="chunked", chunk=0, **kw)
+    few = {k: v[:3].contiguous() for k, v in x.items()}
+    clu = gpu_scan(few, 1, 3, mode="chunked", chunk=0, **kw)
+    assert clu[4]["renorm_count"] > 0
+    for i, name in enumerate("oASn"):
+        assert np.array_equal(one[i][:3], clu[i]), name
+    assert one[4]["flags"] == 0 and clu[4]["flags"] == 0
+
+
+@pytest.mark.parametrize("form", ["cluster", "one_cta"])
+@pytest.mark.parametrize("io", ["bf16", "f32"])
+def test_chunked_guard_falls_back_step_by_step(io, form):
+    N, T = (2 if form == "cluster" else _one_cta_pairs()), 40
     x = workloads.gaussian_inputs(N, T, 64, 64, 1, io, seed=77)
     x["A0"] = -torch.eye(64).expand(N, 64, 64).contiguous()
     x["u"][:, 0] = 0.0
@@ -101,9 +132,9 @@ def test_chunked_guard_falls_back_step_by_step(io):
     got = gpu_scan(x, 1, N, mode="chunked", chunk=0, **kw)
     ref = oracle_scan(x, **kw, trace=True)
     assert ref[4]["guard"][:, 0, 0].all()
-    assert got[4]["chunk_fallbacks"] >= 1
+    assert got[4]["chunk_fallbacks"] >= N
     assert got[4]["guard_count"] == int(ref[4]["guard"].sum())
-    _check(errs(got, ref), TOL if io == "bf16" else TOL_F32, f"chunked guard fallback {io}")
+    _check(errs(got, ref), TOL if io == "bf16" else TOL_F32, f"chunked guard fallback {io} {form}")
 
 
 def test_chunked_rejects_shapes_it_does_not_build():
