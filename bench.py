@@ -463,16 +463,23 @@ def link_bound_ms(h2d: int, d2h: int, link: dict) -> float:
                      d2h / (link["d2h_gbs"] * 1e9))
 
 
-def ctas_label(mode: str, d: int, chunk: int, pairs: int, sms: int) -> str:
-    """How the library places one (b, h) pair: the sequential and delta modes take `chunk`
-    CTAs per pair (0: a two-CTA cluster at d = 128 while 2 B H CTAs fit on the SMs)."""
+def ctas_per_pair(mode: str, d: int, chunk: int, pairs: int, sms: int) -> int:
+    """CTAs the library gives one (b, h) pair: the sequential mode takes `chunk` (0: the
+    default), the sequential and delta defaults are a two-CTA cluster at d = 128 while 2 B H
+    CTAs fit on the SMs, the chunked mode a two-CTA cluster at any d while they fit."""
     if mode == "chunked":
-        return "one CTA per (b,h) pair"
-    ctas = chunk if (mode == "sequential" and chunk) else (2 if d == 128 and 2 * pairs <= sms else 1)
+        return 2 if 2 * pairs <= sms else 1
+    return chunk if (mode == "sequential" and chunk) else (2 if d == 128 and 2 * pairs <= sms else 1)
+
+
+def ctas_label(mode: str, d: int, chunk: int, pairs: int, sms: int) -> str:
+    """How the library places one (b, h) pair (ctas_per_pair)."""
+    ctas = ctas_per_pair(mode, d, chunk, pairs, sms)
     if ctas == 1:
         return "one CTA per (b,h) pair"
     if ctas == 2:
-        return "a two-CTA cluster per (b,h) pair (A and S on separate SMs)"
+        what = "the A side and the S side of each chunk" if mode == "chunked" else "A and S"
+        return f"a two-CTA cluster per (b,h) pair ({what} on separate SMs)"
     return f"a cluster of {ctas} CTAs per (b,h) pair (rows of A and columns of S split)"
 
 
@@ -761,7 +768,8 @@ def main():
                                      / (ms_per_step / 1e3) / 1e12) / peak_tf,
                 "hbm_gbs": bytes_step / (ms_per_step / 1e3) / 1e9,
                 "hbm_frac": bytes_step / (ms_per_step / 1e3) / 1e9 / float(peaks["hbm_gbs"]),
-                "sm_count": sms, "sm_ceiling": min(1.0, B * H / sms)}
+                "sm_count": sms,
+                "sm_ceiling": min(1.0, B * H * ctas_per_pair(args.mode, w.d, args.chunk, B * H, sms) / sms)}
     if args.mode == "chunked":
         tf32_peak = float(peaks["bf16_tflops"]) / 2.0
         tfl = B * H * T * chunk_tensor_flops_per_token_head(w.r, w.io == "f32") / (ms_per_step / 1e3) / 1e12

@@ -51,10 +51,11 @@
 // Few pairs (two CTAs per pair fit on the SMs): each pair runs on a cluster of two CTAs,
 // one SM each.  CTA 0 carries A (the prologue's [U; Sigma], G1..G4, the LDL^T, the A update
 // and alpha), CTA 1 carries S (phi(q), V, n and 1/den, G5, G6, the renormalisation, the
-// outputs and S).  The only data that crosses is alpha, 64 x 64 fp32: CTA 0 writes it into
-// its own AL tile and sends it with one bulk copy into CTA 1's AL tile, completing on an
-// mbarrier there; CTA 1 arrives on an mbarrier of CTA 0 once it is done with it.  So the A
-// side, the longer chain, runs up to a chunk ahead of the S side.  Each side computes what
+// outputs and S).  The only data that crosses is alpha, 64 x 64 fp32: the threads of CTA 0
+// that form it store their rows straight into CTA 1's AL tile with asynchronous stores
+// (st.async into distributed shared memory) that count their bytes on an mbarrier there;
+// CTA 1 arrives on an mbarrier of CTA 0 once it is done with it.  So the A side, the longer chain, runs up to a chunk ahead
+// of the S side (its rows of alpha go out while the other warps update A).  Each side computes what
 // the one-CTA form computes, in the same order, so the two forms agree bit for bit, except
 // in a chunk where the guard fires: the A side then takes alpha step by step, and the S side
 // its chunk path.
@@ -196,7 +197,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
   uint32_t* tslot = reinterpret_cast<uint32_t*>(in_bar + 2);
   volatile int* flag = reinterpret_cast<volatile int*>(in_bar + 3);
   volatile int* issued = reinterpret_cast<volatile int*>(in_bar + 4);   // the last tile whose copy was issued
-  uint64_t* full_bar = in_bar + 5;    // SPLIT, S side: alpha has landed in AL
+  uint64_t* full_bar = in_bar + 5;    // SPLIT, S side: alpha is in AL
   uint64_t* empty_bar = in_bar + 6;   // SPLIT, A side: the S side is done with the alpha it was sent
   const uint32_t sbase = smem_u32(sf);
 
@@ -227,8 +228,8 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     mbar_init(in_bar, 1);
     mbar_init(mma_bar, 1);
     if (SPLIT) {
-      mbar_init(full_bar, 1);      // the S side's own arrival with the bytes it expects
-      mbar_init(empty_bar, NT);    // every thread of the S side, remotely
+      mbar_init(full_bar, 1);      // the S side's own arrival with the 16 KB it expects
+      mbar_init(empty_bar, 1);     // thread 0 of the S side, remotely, after a CTA barrier
     }
     fence_mbar_init();
     *flag = 0;
@@ -241,7 +242,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
   const uint32_t tmem = *tslot;
   // SPLIT: alphas sent (A side) and received (S side); the peer's AL tile and barriers
   uint32_t n_sent = 0, n_recv = 0;
-  const uint32_t peer_al = SPLIT ? mapa_shared(smem_u32(sf + Cf::F_AL), crank ^ 1u) : 0u;
+  const uint32_t peer_al = SPLIT ? mapa_shared(smem_u32(sf + Cf::F_AL), crank ^ 1u) : 0u;   // bytes
   const uint32_t peer_full = SPLIT ? mapa_shared(smem_u32(full_bar), crank ^ 1u) : 0u;
   const uint32_t peer_empty = SPLIT ? mapa_shared(smem_u32(empty_bar), crank ^ 1u) : 0u;
 
@@ -443,9 +444,12 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     staged_pos = np;
     stage_pending = true;
   };
-  // SPLIT, S side: every thread signals the A side that it is done with the chunk's alpha
+  // SPLIT, S side: after a CTA barrier that follows every access to the chunk's alpha, thread 0
+  // signals the A side (release, cluster scope) that AL may be written again
   auto release_alpha = [&]() {
-    if constexpr (SPLIT) mbar_arrive_remote(peer_empty);
+    if constexpr (SPLIT) {
+      if (tid == 0) mbar_arrive_remote(peer_empty);
+    }
   };
   // A_1 = A_0 - Z D^{-1} Z^T (+ eps_n I at a nudge): row `row`, columns col0 .. col0 + 15, from
   // the 16 values of G4's result in v
@@ -468,14 +472,15 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
       *ap = x;
     }
   };
-  // SPLIT, A side: send the chunk's alpha (the AL tile, written by all threads) into the S
-  // side's AL tile; the copy completes on the S side's full_bar
-  auto ship_alpha = [&]() {
+  // SPLIT, A side, the 128 threads of rows 64 + t: store this thread's half of alpha_t (32
+  // values, 128 bytes) into the S side's AL tile, counted on its full_bar; the thread does
+  // not wait for them
+  auto send_alpha = [&](int t, const float (&al)[32]) {
     if constexpr (SPLIT) {
-      fence_proxy_async_smem();   // the generic writes of AL, visible to the bulk copy
-      __syncthreads();
-      if (tid == 0) bulk_s2s_cluster(peer_al, sf + Cf::F_AL, TILE * sizeof(float), peer_full);
-      ++n_sent;
+#pragma unroll
+      for (int j = 0; j < 32; j += 4)
+        st_async_v4(peer_al + 4u * (uint32_t)tk_off(t, 32 * half + j, 64), al[j], al[j + 1], al[j + 2], al[j + 3],
+                    peer_full);
     }
   };
   int loaded = -1;
@@ -589,7 +594,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
 #pragma unroll
             for (int m = 0; m < 8; ++m) {
               kx[m] = phi_fast(kx[m]);
-              qx[m] = phi_fast(qx[m]);
+              if (doS) qx[m] = phi_fast(qx[m]);
             }
           } else {
 #pragma unroll
@@ -641,7 +646,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
 #pragma unroll
             for (int m = 0; m < 8; ++m) {
               kx[m] = phi_fast(kx[m]);
-              qx[m] = phi_fast(qx[m]);
+              if (doS) qx[m] = phi_fast(qx[m]);
             }
           } else {
 #pragma unroll
@@ -1159,9 +1164,17 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
         if (cq == 0) go[st * D + ar] = from_f32<TIO>(op * misc[Cf::M_RDEN + t]);
         __syncthreads();
       }
-      if constexpr (SPLIT) {
+      if constexpr (SPLIT) {   // AL (rows c.. zero) -> the S side, by the threads that send it in a normal chunk
         for (int e = tid; e < (64 - c) * 64; e += NT) sf[Cf::F_AL + tk_off(c + (e >> 6), e & 63, 64)] = 0.f;
-        ship_alpha();
+        __syncthreads();
+        if (row >= 64) {
+          float al[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) al[j] = sf[Cf::F_AL + tk_off(row - 64, 32 * half + j, 64)];
+          send_alpha(row - 64, al);
+        }
+        ++n_sent;
+        __syncthreads();
       } else {
         if (tid == 0) misc[Cf::M_SSV] = 0.f;   // S changed step by step: its norm is recomputed
       }
@@ -1270,9 +1283,11 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
             al32[j] = x;
             an = fmaf(x, x, an);
           }
+          if (!SPLIT) {
 #pragma unroll
-          for (int j = 0; j < 32; j += 4)
-            st4(Cf::F_AL + tk_off(t, 32 * half + j, 64), al32[j], al32[j + 1], al32[j + 2], al32[j + 3]);
+            for (int j = 0; j < 32; j += 4)
+              st4(Cf::F_AL + tk_off(t, 32 * half + j, 64), al32[j], al32[j + 1], al32[j + 2], al32[j + 3]);
+          }
         } else {   // the S side of a cluster: the same values, from the alpha it was sent
 #pragma unroll
           for (int j = 0; j < 32; j += 4) {
@@ -1287,13 +1302,16 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
         }
         if (doS) misc[Cf::M_AN2 + 64 * half + t] = an;   // |alpha_t|^2, two halves
       }
-      if (SPLIT && doA) {   // the A side of a cluster: the A update, then alpha to the S side
-        if (row < 64) {
+      if (SPLIT && doA) {   // the A side of a cluster: alpha to the S side while A is updated
+        if (row >= 64) {
+          send_alpha(row - 64, al32);
+        } else {
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc)
             a_update(row, 32 * half + 16 * cc, *reinterpret_cast<float(*)[16]>(v32 + 16 * cc), nudge);
         }
-        ship_alpha();
+        ++n_sent;
+        __syncthreads();
         advance(c);
         continue;
       }
@@ -1621,9 +1639,8 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     if (F32 && stage_pending) (void)mbar_wait_bounded(in_bar, stage_phase);                            // staged inputs
   }
   if constexpr (SPLIT) {
-    // The A side's AL is the source of the last copy: it stays until the S side has taken it
-    // (or the wait gives up, long after any copy has landed); then neither CTA touches the
-    // other's shared memory again
+    // The asynchronous stores of the last alpha have landed once the S side has taken it (or
+    // the wait gives up, long after); then neither CTA touches the other's shared memory again
     if (doA && tid == 0 && n_sent > 0) (void)mbar_wait_cluster_bounded(empty_bar, (n_sent - 1) & 1u);
     cluster_sync_all();
   }

@@ -153,6 +153,16 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
+// Asynchronous store of four floats into another CTA of the cluster (addr and bar are that
+// CTA's shared-memory addresses, from mapa_shared): 16 bytes of complete_tx on its mbarrier
+// bar, which makes them visible to the threads that see the phase complete.
+__device__ __forceinline__ void st_async_v4(uint32_t addr, float x, float y, float z, float w, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   addr),
+               "f"(x), "f"(y), "f"(z), "f"(w), "r"(bar)
+               : "memory");
+}
+
 __device__ __forceinline__ void st_cluster_s32(uint32_t addr, int v) {
   asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
@@ -193,18 +203,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, u
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
           smem_u32(dst_smem)),
       "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// Shared -> shared bulk copy into another CTA of the cluster: dst and bar are that CTA's
-// addresses (mapa_shared), completion is a complete_tx of `bytes` on its mbarrier bar
-// (16-byte aligned addresses, size a multiple of 16).
-__device__ __forceinline__ void bulk_s2s_cluster(uint32_t dst_cluster, const void* src_smem, uint32_t bytes,
-                                                 uint32_t bar_cluster) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst_cluster),
-      "r"(smem_u32(src_smem)), "r"(bytes), "r"(bar_cluster)
       : "memory");
 }
 

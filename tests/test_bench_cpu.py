@@ -140,7 +140,9 @@ def test_no_function_shadows_a_module_function_it_calls():
 
 
 def test_ctas_label_names_the_placement_the_library_takes():
-    assert bench.ctas_label("chunked", 64, 0, 128, 152) == "one CTA per (b,h) pair"
+    assert bench.ctas_label("chunked", 64, 0, 128, 152) == "one CTA per (b,h) pair"   # 256 > 152 SMs
+    assert "A side and the S side" in bench.ctas_label("chunked", 64, 0, 32, 152)
+    assert bench.ctas_per_pair("chunked", 64, 0, 76, 152) == 2 and bench.ctas_per_pair("chunked", 64, 0, 77, 152) == 1
     assert bench.ctas_label("sequential", 64, 0, 32, 152) == "one CTA per (b,h) pair"
     assert "two-CTA cluster" in bench.ctas_label("sequential", 128, 0, 16, 152)
     assert bench.ctas_label("sequential", 128, 0, 128, 152) == "one CTA per (b,h) pair"   # 256 > 152 SMs
