@@ -263,8 +263,8 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
   // Float32 I/O has no raw stage: a chunk's q, k, v, u are copied into the tiles that are free
   // from the previous chunk's G6 until this chunk's prologue (q -> PQ, k -> Q tile 1, v -> vb,
   // where it stays as it is, u -> AL), issued right after that G6 so that they land beside it.
-  // The A side of a cluster has neither G5 nor G6: it takes u into PQ (AL carries alpha) and
-  // issues the next chunk's k and u as soon as its G1 is done.
+  // The A side of a cluster has neither G5 nor G6: it takes u into PQ (free there) and issues
+  // the next chunk's k and u before its G3.
   constexpr int F_UST = SPLIT ? Cf::F_PQ : Cf::F_AL;   // where a float32 chunk's u is staged
   long long staged_pos = -1;   // the chunk whose inputs were issued last (all threads agree)
   bool stage_pending = false;  // issued and not yet waited for
@@ -770,8 +770,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
                              {Cf::F_Q, Cf::F_A, 128, 64, TC_G1, true}};
       if (!mma_run(ps, F32 ? 3 : 2, 64)) { failed = true; break; }
     }
-    // the A side of a cluster: the next chunk's u (PQ) and k (Q tile 1), free once G1 is done
-    if constexpr (SPLIT && F32) stage_next();
+
     // ---------------- G2: [G - I; H^T] = [W^T; Q^T] U^T  (M 128, N 64, K 64), X read from G1's
     // accumulator in tensor memory; it runs while G1's W is drained.  Q^T stays there for alpha.
     if constexpr (F32) {
@@ -1205,6 +1204,10 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
         st4_lo(Cf::F_P + 4 * e4, xv);
       }
     }
+    // the A side of a cluster: the next chunk's u (PQ) and k (Q tile 1), free since G1; issued
+    // after the LDL^T, which runs faster without the copies landing beside it, and still in
+    // time for the next chunk
+    if constexpr (SPLIT && F32) stage_next();
     // ---------------- G3: [Z; F^T] = [W; H^T] Linv^T  (M 128, N 64, K 64), 3xTF32
     {
       const MmaPass ps[3] = {{Cf::F_R, Cf::F_L, 128, 64, TC_G3, false},
