@@ -119,7 +119,11 @@ vla_err_t vla_create(vla_handle_t* h, int device);
  *             carry A and, with float32 I/O, everywhere).  Both compute the same
  *             recurrence; they differ in rounding only.  VLA_DELTA computes the delta-rule variant (every
  *             built shape; `chunk` must be 0).
- *   chunk     VLA_CHUNKED: steps per chunk (0 = the built default).
+ *   chunk     VLA_CHUNKED: steps per chunk (0 = the built default).  The library
+ *             runs each pair on a cluster of two CTAs (the A side and the S side
+ *             of every chunk on two SMs) while 2 B H CTAs fit on the device's
+ *             SMs, on one CTA otherwise; both forms give the same bits except in
+ *             a chunk where the guard fires (the same values up to rounding).
  *             VLA_SEQUENTIAL: CTAs per (batch, head) pair: 1 = one CTA holds
  *             both halves of the step; 2 = a cluster of two CTAs on two SMs, one
  *             tracking A, the other S (the same arithmetic and the same results
