@@ -102,9 +102,9 @@ TRAFFIC = {
     ("b2h8_t65536_d128_f32", "sequential"): (156.39e6 * 16, 4096, "2d1fb8f16cca4b57"),
     ("b8h16_t16384_d64_bf16_recall", "sequential"): (325.31e6 * 4, 4096, "2d1fb8f16cca4b57"),
     ("b8h16_t16384_d64_bf16_recall", "delta"): (325.57e6 * 4, 4096, "4c6f6c798db6d4c6"),
-    ("b8h16_t16384_d64_bf16_recall", "chunked"): (156.36e6 * 8, 2048, "b82d74d23ad0e752"),
-    ("b16h16_t8192_d64_bf16_r4", "chunked"): (274.80e6 * 8, 1024, "b82d74d23ad0e752"),
-    ("b4h8_t4096_d64_f32", "chunked"): (153.38e6, 4096, "b82d74d23ad0e752"),
+    ("b8h16_t16384_d64_bf16_recall", "chunked"): (156.45e6 * 8, 2048, "533bafc27e61f48a"),
+    ("b16h16_t8192_d64_bf16_r4", "chunked"): (274.48e6 * 8, 1024, "533bafc27e61f48a"),
+    ("b4h8_t4096_d64_f32", "chunked"): (153.30e6, 4096, "533bafc27e61f48a"),
     # the u projection's TMA form (whole workload captured)
     ("b8h16_t16384_d64_bf16_recall", "project_u"): (483.84e6, 16384, "29d4409f456223ca"),
     ("b16h16_t8192_d64_bf16_r4", "project_u"): (1281.11e6, 8192, "29d4409f456223ca"),
