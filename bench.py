@@ -98,10 +98,10 @@ def kernel_source_hash(mode: str) -> str:
 # from ncu captures: (bytes per full-length launch, captured T, kernel source hash).  Captures
 # at a truncated T are scaled by the units processed (traffic grows with T).
 TRAFFIC = {
-    ("b4h8_t4096_d64_f32", "sequential"): (154.31e6, 4096, "2d1fb8f16cca4b57"),
-    ("b2h8_t65536_d128_f32", "sequential"): (156.39e6 * 16, 4096, "2d1fb8f16cca4b57"),
-    ("b8h16_t16384_d64_bf16_recall", "sequential"): (325.31e6 * 4, 4096, "2d1fb8f16cca4b57"),
-    ("b8h16_t16384_d64_bf16_recall", "delta"): (325.57e6 * 4, 4096, "4c6f6c798db6d4c6"),
+    ("b4h8_t4096_d64_f32", "sequential"): (154.42e6, 4096, "09b46c6b7e90fb86"),
+    ("b2h8_t65536_d128_f32", "sequential"): (155.86e6 * 16, 4096, "09b46c6b7e90fb86"),
+    ("b8h16_t16384_d64_bf16_recall", "sequential"): (324.69e6 * 4, 4096, "09b46c6b7e90fb86"),
+    ("b8h16_t16384_d64_bf16_recall", "delta"): (324.66e6 * 4, 4096, "a1a90440234bd2e5"),
     ("b8h16_t16384_d64_bf16_recall", "chunked"): (156.45e6 * 8, 2048, "533bafc27e61f48a"),
     ("b16h16_t8192_d64_bf16_r4", "chunked"): (274.48e6 * 8, 1024, "533bafc27e61f48a"),
     ("b4h8_t4096_d64_f32", "chunked"): (153.30e6, 4096, "533bafc27e61f48a"),
