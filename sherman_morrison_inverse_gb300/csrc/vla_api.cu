@@ -17,6 +17,8 @@ cudaError_t launch_seq_block_d128(int r, bool bf16, bool cluster, const ScanArgs
 
 // the row-split scan on a cluster of `ctas` (4 or 8) CTAs per pair (vla_rows.cu)
 cudaError_t launch_rows(int d, int r, bool bf16, int ctas, const ScanArgs& a, cudaStream_t s, bool* built);
+// two-CTA clusters of the chunked kernel resident at once (vla_chunked.cu)
+int chunked_cluster_capacity(int r, bool bf16);
 
 cudaError_t launch_seq(int d, int r, bool bf16, int ctas, const ScanArgs& a, cudaStream_t s, bool* built) {
   if (ctas == 4 || ctas == 8) return launch_rows(d, r, bf16, ctas, a, s, built);
@@ -108,7 +110,8 @@ bool shape_built(int d, int dv, int r, bool bf16, vla_mode_t mode, int chunk, in
 // on the SMs (one CTA of 4 d threads would be capped at 128 registers a thread and spill);
 // one otherwise (at d <= 64 the hand-off between two SMs costs more than the issue slots it
 // frees).  Chunked mode: a cluster of two (the A side and the S side of each chunk on two
-// SMs) while 2 B H CTAs fit on the SMs, else one.
+// SMs) while 2 B H CTAs fit on the SMs and B H such clusters can be resident at once (the
+// occupancy query), else one: clusters in two waves would take longer than one CTA each.
 vla_err_t check_scan(vla_handle_t h, const char* fn, int B, int H, long long T, int d, int dv, int r, int P,
                      float eps_n, float tau, long long t0, vla_dtype_t io_dtype, vla_mode_t mode, int chunk,
                      int* ctas) {
@@ -126,9 +129,10 @@ vla_err_t check_scan(vla_handle_t h, const char* fn, int B, int H, long long T, 
   if (pairs > 0x7fffffffLL) return fail(h, VLA_ERR_INVALID_ARG, f + ": B*H too large");
   if (d != dv) return fail(h, VLA_ERR_UNSUPPORTED, f + ": built only for d == dv");
   const int auto_ctas = (d == 128 && 2 * pairs <= h->sm_count) ? 2 : 1;
-  const int chunk_ctas = (2 * pairs <= h->sm_count) ? 2 : 1;
-  *ctas = mode == VLA_SEQUENTIAL ? (chunk != 0 ? chunk : auto_ctas) : mode == VLA_DELTA ? auto_ctas : chunk_ctas;
   const bool bf16 = io_dtype == VLA_BF16;
+  const int chunk_ctas =
+      (mode == VLA_CHUNKED && 2 * pairs <= h->sm_count && pairs <= vla::chunked_cluster_capacity(r, bf16)) ? 2 : 1;
+  *ctas = mode == VLA_SEQUENTIAL ? (chunk != 0 ? chunk : auto_ctas) : mode == VLA_DELTA ? auto_ctas : chunk_ctas;
   if (!shape_built(d, dv, r, bf16, mode, chunk, *ctas)) {
     char buf[400];
     std::snprintf(buf, sizeof buf,

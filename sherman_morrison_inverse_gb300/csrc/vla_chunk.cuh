@@ -669,8 +669,11 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
           if (doS) *reinterpret_cast<uint4*>(vb + t * 64 + 8 * pc) = vw;
         }
       }
-      for (int e4 = tid; e4 < (64 - C) * 16; e4 += NT) {   // zero rows C..63 of Sigma and phi(q)
-        const int t = C + (e4 >> 4), col = (e4 & 15) * 4;
+      // zero rows C..63 of Sigma and phi(q): the lanes of a warp take 8 rows (8 distinct bank
+      // groups of the core-matrix layout) x 4 column groups
+      static_assert(C % 8 == 0, "zero rows in groups of 8");
+      for (int e4 = tid; e4 < (64 - C) * 16; e4 += NT) {
+        const int t = C + 8 * (e4 >> 7) + (e4 & 7), col = ((e4 >> 3) & 15) * 4;
         if (doA) st4(Cf::F_P + tk_off(64 + t, col, 64), 0.f, 0.f, 0.f, 0.f);
         if (doS) st4(Cf::F_PQ + tk_off(t, col, 64), 0.f, 0.f, 0.f, 0.f);
         if (F32 && doA) st4(Cf::F_Q + tk_off(64 + t, col, 64), 0.f, 0.f, 0.f, 0.f);
@@ -1654,6 +1657,27 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     if (renorm_cnt) atomicAdd(&a.status->renorm_count, renorm_cnt);
     if (fallback_cnt) atomicAdd(&a.status->chunk_fallbacks, fallback_cnt);
   }
+}
+
+// How many two-CTA clusters of chunk_scan_kernel<R, TIO, true> fit on the device at once.
+template <int R, typename TIO>
+cudaError_t cluster_capacity_t(int* n) {
+  using Cf = chk::Cfg<R, TIO>;
+  auto kern = chunk_scan_kernel<R, TIO, true>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::bytes);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(chk::NT, 1, 1);
+  cfg.dynamicSmemBytes = Cf::bytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(n, kern, &cfg);
 }
 
 // ctas = 2: a cluster of two CTAs per pair (the A side and the S side)

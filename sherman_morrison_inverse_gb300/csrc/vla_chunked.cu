@@ -20,4 +20,27 @@ cudaError_t launch_chunked(int d, int r, bool bf16, int chunk, int ctas, const S
   return cudaSuccess;
 }
 
+// Two-CTA clusters of the chunked kernel that can be resident at once on the current device
+// (0 when the shape is not built or the query fails), cached per device and shape.
+int chunked_cluster_capacity(int r, bool bf16) {
+  constexpr int kDevices = 64;
+  static int cache[kDevices][2][2];   // +1: 0 means not queried yet
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevices || (r != 1 && r != 4)) {
+    cudaGetLastError();
+    return 0;
+  }
+  int& slot = cache[dev][r == 4][bf16 ? 1 : 0];
+  if (slot > 0) return slot - 1;
+  int n = 0;
+  cudaError_t e = r == 1 ? (bf16 ? cluster_capacity_t<1, __nv_bfloat16>(&n) : cluster_capacity_t<1, float>(&n))
+                         : (bf16 ? cluster_capacity_t<4, __nv_bfloat16>(&n) : cluster_capacity_t<4, float>(&n));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  slot = n + 1;
+  return n;
+}
+
 }  // namespace vla
