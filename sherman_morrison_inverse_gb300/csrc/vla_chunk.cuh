@@ -1418,7 +1418,44 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
           misc[Cf::M_IS + tid] = 1.f;   // 1 / sigma before step t
         }
       } else {
-        // v_t . S alpha_t and the alpha Gram from the G5 result still in TMEM (rows t < 64)
+        // V (rows t, K = i) as an operand tile in P tile 0 (its low part in P tile 1 with float32
+        // I/O; both tiles are free since G5), and its Gram V V^T on the tensor core into G1's
+        // columns (free since alpha was formed).  Rows C.. of the tile keep stale values: they
+        // reach only rows and columns >= C of the product, which are never read.
+        for (int f = tid; f < C * 8; f += NT) {
+          const int t = (f >> 6) * 8 + (f & 7), pc = ((f & 7) + (f >> 3)) & 7;
+          float x[8];
+          if constexpr (F32) {
+            const float4 a0 = *reinterpret_cast<const float4*>(vb + t * 64 + 8 * pc);
+            const float4 a1 = *reinterpret_cast<const float4*>(vb + t * 64 + 8 * pc + 4);
+            x[0] = a0.x; x[1] = a0.y; x[2] = a0.z; x[3] = a0.w; x[4] = a1.x; x[5] = a1.y; x[6] = a1.z; x[7] = a1.w;
+          } else {
+            const uint4 w = *reinterpret_cast<const uint4*>(vb + t * 64 + 8 * pc);
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              const float2 f2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ww[m]));
+              x[2 * m] = f2.x;
+              x[2 * m + 1] = f2.y;
+            }
+          }
+          st4(Cf::F_P + tk_off(t, 8 * pc, 64), x[0], x[1], x[2], x[3]);
+          st4(Cf::F_P + tk_off(t, 8 * pc + 4, 64), x[4], x[5], x[6], x[7]);
+          if constexpr (F32) {
+            st4_lo(Cf::F_P + TILE + tk_off(t, 8 * pc, 64), x);
+            st4_lo(Cf::F_P + TILE + tk_off(t, 8 * pc + 4, 64), x + 4);
+          }
+        }
+        {
+          const MmaPass ps[3] = {{Cf::F_P, Cf::F_P, 128, 64, TC_G1, false},
+                                 {Cf::F_P + TILE, Cf::F_P, 128, 64, TC_G1, true},
+                                 {Cf::F_P, Cf::F_P + TILE, 128, 64, TC_G1, true}};
+          if (!mma_run(ps, F32 ? 3 : 1, 64)) { failed = true; break; }
+        }
+        // rows t < 64 (lanes of quadrants 0, 1): v_t . S alpha_t from G5's S alpha and the V
+        // tile; the products PP[t][t'] = (v_t . v_t') (alpha_t . alpha_t') of row t: their
+        // exclusive prefix sums Q[t][m] = sum_{t'<m} PP[t][t'] -> F_Q at m C + t, the diagonal
+        // PP[t][t] -> M_VEC
         if (row < 64) {
           float v[16];
           const int t = row;
@@ -1428,66 +1465,125 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
             for (int cc = 0; cc < 4; ++cc) {
               tld(TC_G5 + 16 * cc, v);
 #pragma unroll
-              for (int j = 0; j < 16; ++j)
-                if (t < c) xs = fmaf(to_f32(vb[t * 64 + 16 * cc + j]), v[j], xs);
+              for (int j = 0; j < 16; j += 4) {
+                const float4 v4 = *reinterpret_cast<const float4*>(sf + Cf::F_P + tk_off(t, 16 * cc + j, 64));
+                xs = fmaf(v4.x, v[j], xs);
+                xs = fmaf(v4.y, v[j + 1], xs);
+                xs = fmaf(v4.z, v[j + 2], xs);
+                xs = fmaf(v4.w, v[j + 3], xs);
+              }
             }
-            misc[Cf::M_XS + t] = xs;
+            misc[Cf::M_XS + t] = (t < c) ? xs : 0.f;
           } else {
+            float w[16], q = 0.f;
 #pragma unroll
             for (int cc = 0; cc < (C + 15) / 16; ++cc) {
-              tld(TC_G5 + 64 + 16 * cc, v);
+              tld(TC_G5 + 64 + 16 * cc, v);   // alpha_t . alpha_t'
+              tld(TC_G1 + 16 * cc, w);        // v_t . v_t'
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
                 const int tp = 16 * cc + j;
-                if (tp < C && t < C) sf[Cf::F_Q + tp * C + t] = v[j];   // alpha_t' . alpha_t (symmetric)
+                const float pp = v[j] * w[j];
+                if (tp < C && t < C) {
+                  sf[Cf::F_Q + tp * C + t] = q;
+                  if (tp == t) misc[Cf::M_VEC + t] = pp;
+                  if (tp < t) q += pp;
+                }
               }
             }
           }
         }
-        float* VV = sf + Cf::F_Q + TILE;   // v_t . v_t' for t, t' < c  ([C][C])
-        for (int e = tid; e < C * C; e += NT) {
-          const int t = e / C, tp = e - t * C;
-          float vv = 0.f;
-          if (t < c && tp < c) {
-            for (int i = 0; i < 64; ++i) vv = fmaf(to_f32(vb[t * 64 + i]), to_f32(vb[tp * 64 + i]), vv);
-          }
-          VV[e] = vv;
-        }
         __syncthreads();
-        if (tid == 0) {
+        if (warp == 0) {
           // S_t = sigma_t S_reg,t with S_reg,t = S_0 + sum_{t'<=t} v_t' alpha_t'^T / sigma_{t'-1}.
           // The norms are tracked unscaled (bounded by about tau), the cross terms through
           // the ratios sigma_{t-1} / sigma_{t'-1} <= 1, so nothing overflows however small
           // sigma gets.  Below 2^-64 the folded operands of G6 would grow past 2^64: the
           // chunk's S then goes step by step instead.
-          float n2 = ns, sg = 1.f;          // ||S_{t-1}||^2 and sigma_{t-1}
+          //   ||S_t||^2 = ||S_{t-1}||^2 + 2 sigma_{t-1} (v_t . S_reg alpha_t + R_t) + PP[t][t],
+          //   R_t = sum_{t'<t} PP[t][t'] / sigma_{t'-1}.
+          // The decisions are taken in order by one warp.  Lane l keeps, for the steps l and
+          // l + 32, x = v . S_reg alpha + R as far as the decisions taken so far go (the scales
+          // of the steps not yet decided taken as the current one): at first R_t = Q[t][t].  A
+          // renormalisation at step t changes 1/sigma by d for every t' > t, so each later x
+          // gains d (Q[t][t] - Q[t][t + 1]) for its own row.
+          constexpr int NSL = (C + 31) / 32;
+          const float* QB = sf + Cf::F_Q;   // Q[t][m] at m C + t
+          float xv[NSL], dg[NSL], qd[NSL];
+#pragma unroll
+          for (int sl = 0; sl < NSL; ++sl) {
+            const int tq = lane + 32 * sl;
+            const bool in = tq < c;
+            qd[sl] = in ? QB[tq * C + tq] : 0.f;
+            xv[sl] = in ? misc[Cf::M_XS + tq] + qd[sl] : 0.f;
+            dg[sl] = in ? misc[Cf::M_VEC + tq] : 0.f;
+          }
+          float n2 = ns, sg = 1.f, isg = 1.f;   // ||S_{t-1}||^2, sigma_{t-1}, 1 / sigma_{t-1}
           unsigned int rc = 0;
           int deep_at = 0;
-          const float* AA = sf + Cf::F_Q;   // alpha Gram [C][C]
+          // ||S_t|| > tau is decided as ||S_t||^2 > tau^2.  Where a step renormalises, the
+          // factor tau / ||S_t|| comes from one reciprocal square root (rsqrt.approx, a few ulp),
+          // and 1 / sigma follows by multiplication, keeping the chain of steps short.
+          const float tau2 = a.tau * a.tau, itau = 1.f / a.tau;
+          float rec_sg[NSL], rec_is[NSL];   // sigma_t and 1 / sigma_{t-1} of this lane's steps
+#pragma unroll
+          for (int s2 = 0; s2 < NSL; ++s2) rec_sg[s2] = rec_is[s2] = 1.f;
+          int t_end = c;
           for (int t = 0; t < c; ++t) {
-            misc[Cf::M_IS + t] = 1.f / sg;
-            float cross = sg * misc[Cf::M_XS + t];   // sigma_{t-1} v_t^T S_reg,t-1 alpha_t
-            for (int tp = 0; tp < t; ++tp)
-              cross = fmaf(VV[t * C + tp] * AA[t * C + tp], sg * misc[Cf::M_IS + tp], cross);
-            const float vn = misc[Cf::M_VN + t];
-            const float npre2 = fmaf(vn * vn, AA[t * C + t], fmaf(2.f, cross, n2));
-            const float npre = sqrtf(fmaxf(npre2, 0.f));
-            if (npre > a.tau) {
-              sg *= a.tau / npre;
-              n2 = a.tau * a.tau;
+            const int sl = (NSL > 1 && t >= 32) ? 1 : 0;
+            const float x = __shfl_sync(0xffffffffu, NSL > 1 && sl ? xv[NSL - 1] : xv[0], t & 31);
+            const float dd = __shfl_sync(0xffffffffu, NSL > 1 && sl ? dg[NSL - 1] : dg[0], t & 31);
+            float qn[NSL];   // Q[t'][t + 1] of this lane's later steps, loaded ahead of the decision
+            bool later[NSL];
+#pragma unroll
+            for (int s2 = 0; s2 < NSL; ++s2) {
+              const int tq = lane + 32 * s2;
+              later[s2] = tq >= t + 2 && tq < c;
+              qn[s2] = later[s2] ? QB[(t + 1) * C + tq] : 0.f;
+            }
+            const float isg_t = isg;
+            const float npre2 = fmaf(2.f, sg * x, n2) + dd;
+            if (!isfinite(npre2)) flags |= kStatusNonfinite;
+            if (npre2 > tau2) {   // the same decision in every lane
+              const float rs = rsqrtf(npre2);
+              const float sgn = sg * (a.tau * rs);
+              const float isn = isg * (npre2 * rs) * itau;
+              const float dl = isn - isg;
+#pragma unroll
+              for (int s2 = 0; s2 < NSL; ++s2) xv[s2] = later[s2] ? fmaf(dl, qd[s2] - qn[s2], xv[s2]) : xv[s2];
+              sg = sgn;
+              isg = isn;
+              n2 = tau2;
               ++rc;
             } else {
               n2 = npre2;
             }
-            if (!isfinite(npre)) flags |= kStatusNonfinite;
-            misc[Cf::M_SG + t] = sg;
-            if (!(sg >= 0x1p-64f)) { deep_at = 1; break; }
+            if (lane == (t & 31)) {   // static register indices
+              if (sl == 0) {
+                rec_sg[0] = sg;
+                rec_is[0] = isg_t;
+              } else {
+                rec_sg[NSL - 1] = sg;
+                rec_is[NSL - 1] = isg_t;
+              }
+            }
+            if (!(sg >= 0x1p-64f)) { deep_at = 1; t_end = t + 1; break; }
           }
-          if (!deep_at) renorm_cnt += rc;
-          misc[Cf::M_SCAL] = deep_at ? 1.f : 0.f;
-          for (int t = c; t < 64; ++t) {
+#pragma unroll
+          for (int s2 = 0; s2 < NSL; ++s2) {
+            const int tq = lane + 32 * s2;
+            if (tq < t_end) {
+              misc[Cf::M_SG + tq] = rec_sg[s2];
+              misc[Cf::M_IS + tq] = rec_is[s2];
+            }
+          }
+          if (lane == 0) {
+            if (!deep_at) renorm_cnt += rc;
+            misc[Cf::M_SCAL] = deep_at ? 1.f : 0.f;
+          }
+          for (int t = c + lane; t < 64; t += 32) {
             misc[Cf::M_SG + t] = sg;
-            misc[Cf::M_IS + t] = 1.f / sg;
+            misc[Cf::M_IS + t] = isg;
           }
         }
         __syncthreads();
@@ -1527,12 +1623,18 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
           advance(c);
           continue;
         }
-        // fold the per-step scales into tril(aq) (columns t') and alpha^T (columns t)
-        for (int e = tid; e < 64 * C; e += NT) {
-          const int r = e / C, k = e - r * C;
-          const float is = misc[Cf::M_IS + k];
-          sf[Cf::F_T6 + Cf::T6_Q + tk_off(r, k, C)] *= is;
-          sf[Cf::F_T6 + Cf::T6_A + tk_off(r, k, C)] *= is;
+        // fold the per-step scales into tril(aq) (columns t') and alpha^T (columns t), in the
+        // tiles' memory order: four consecutive floats are one row and columns k0 .. k0 + 3
+        for (int e4 = tid; e4 < 16 * C; e4 += NT) {
+          const int o = 4 * e4, k0 = ((o % (8 * C)) >> 5) << 2;
+          const float4 i4 = *reinterpret_cast<const float4*>(misc + Cf::M_IS + k0);
+          float4* pq = reinterpret_cast<float4*>(sf + Cf::F_T6 + Cf::T6_Q + o);
+          float4* pa = reinterpret_cast<float4*>(sf + Cf::F_T6 + Cf::T6_A + o);
+          float4 xq = *pq, xa = *pa;
+          xq.x *= i4.x; xq.y *= i4.y; xq.z *= i4.z; xq.w *= i4.w;
+          xa.x *= i4.x; xa.y *= i4.y; xa.z *= i4.z; xa.w *= i4.w;
+          *pq = xq;
+          *pa = xa;
         }
       }
     }
