@@ -714,18 +714,21 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
         constexpr int EPT = 64 / TPS;
         const int t = tid / TPS, part = tid - t * TPS;
         float dn = 0.f, vv = 0.f;
-        static_assert(EPT % 4 == 0, "den reduction layout");
+        static_assert(EPT % 4 == 0 && (EPT & (EPT - 1)) == 0, "den reduction layout");
         if (t < c) {
 #pragma unroll
           for (int j = 0; j < EPT; j += 4) {
             const float4 p4 = *reinterpret_cast<const float4*>(pk + t * PLD + part * EPT + j);
+            // the rows of vb are 128 bytes apart (bf16): each step reads its pieces in its own
+            // rotation, so the steps of a warp do not all hit the same banks (|v|^2 only)
+            const int jv = (j + 4 * t) & (EPT - 1);
             float2 v01, v23;
             if constexpr (F32) {
-              const float4 v4 = *reinterpret_cast<const float4*>(vb + t * 64 + part * EPT + j);
+              const float4 v4 = *reinterpret_cast<const float4*>(vb + t * 64 + part * EPT + jv);
               v01 = make_float2(v4.x, v4.y);
               v23 = make_float2(v4.z, v4.w);
             } else {
-              const uint2 w2 = *reinterpret_cast<const uint2*>(vb + t * 64 + part * EPT + j);
+              const uint2 w2 = *reinterpret_cast<const uint2*>(vb + t * 64 + part * EPT + jv);
               v01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w2.x));
               v23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w2.y));
             }
@@ -1189,14 +1192,21 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
       // Linv (rows l, K = j) -> hi (L tile) + lo (Q tile 0); [W; H^T] -> hi in place + lo (P tiles)
       float lv[4][4];
       int loff[4];
+      // a warp takes two 8 x 8 blocks (bi, bj), (bi, bj + 1): lane (row r, half h) reads a
+      // 16-byte piece of its block's row (consecutive, conflict-free) and stores it into row
+      // 8 bi + r of the operand tile (the 8 rows fall in 8 different bank groups)
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
         const int f = tid + NT * s;
-        const int l = (f >> 7) * 8 + (f & 7), j4 = ((f >> 3) & 15) * 4;
-        const int bi = l >> 3, bj = j4 >> 3;
+        const int bi = f >> 7, bj = (f >> 4) & 7, r = (f >> 1) & 7, h = f & 1;
+        const int l = 8 * bi + r, j4 = 8 * bj + 4 * h;
         loff[s] = tk_off(l, j4, 64);
-#pragma unroll
-        for (int m = 0; m < 4; ++m) lv[s][m] = (bi >= bj) ? Xp[pb8(bi, bj) + (l & 7) * 8 + (j4 & 7) + m] : 0.f;
+        float4 x4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (bi >= bj) x4 = *reinterpret_cast<const float4*>(Xp + pb8(bi, bj) + r * 8 + 4 * h);
+        lv[s][0] = x4.x;
+        lv[s][1] = x4.y;
+        lv[s][2] = x4.z;
+        lv[s][3] = x4.w;
       }
       __syncthreads();
 #pragma unroll
@@ -1369,10 +1379,12 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
         const float ns = (misc[Cf::M_SS] + misc[Cf::M_SS + 1]) + (misc[Cf::M_SS + 2] + misc[Cf::M_SS + 3]);
         bound_test(ns);
       }
-      // V^T (rows i, K = t) for G6: lanes cover 8 rows x 4 steps of one core matrix
-      for (int e = tid; e < 64 * C; e += NT) {
-        const int i = ((e >> 5) & 7) * 8 + ((e >> 2) & 7), t = (e >> 8) * 4 + (e & 3);
-        sf[Cf::F_T6 + Cf::T6_V + tk_off(i, t, C)] = to_f32(vb[t * 64 + i]);
+      // V^T (rows i, K = t) for G6: a lane reads column i of four steps (the lanes of a warp
+      // read 32 consecutive columns of one step, conflict-free) and stores them as one float4
+      for (int e = tid; e < 16 * C; e += NT) {
+        const int i = e & 63, t0 = (e >> 6) * 4;
+        st4(Cf::F_T6 + Cf::T6_V + tk_off(i, t0, C), to_f32(vb[t0 * 64 + i]), to_f32(vb[(t0 + 1) * 64 + i]),
+            to_f32(vb[(t0 + 2) * 64 + i]), to_f32(vb[(t0 + 3) * 64 + i]));
       }
       if (!mma_wait()) { failed = true; break; }
     }
