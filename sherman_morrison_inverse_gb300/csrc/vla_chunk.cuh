@@ -1192,21 +1192,14 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
       // Linv (rows l, K = j) -> hi (L tile) + lo (Q tile 0); [W; H^T] -> hi in place + lo (P tiles)
       float lv[4][4];
       int loff[4];
-      // a warp takes two 8 x 8 blocks (bi, bj), (bi, bj + 1): lane (row r, half h) reads a
-      // 16-byte piece of its block's row (consecutive, conflict-free) and stores it into row
-      // 8 bi + r of the operand tile (the 8 rows fall in 8 different bank groups)
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
         const int f = tid + NT * s;
-        const int bi = f >> 7, bj = (f >> 4) & 7, r = (f >> 1) & 7, h = f & 1;
-        const int l = 8 * bi + r, j4 = 8 * bj + 4 * h;
+        const int l = (f >> 7) * 8 + (f & 7), j4 = ((f >> 3) & 15) * 4;
+        const int bi = l >> 3, bj = j4 >> 3;
         loff[s] = tk_off(l, j4, 64);
-        float4 x4 = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (bi >= bj) x4 = *reinterpret_cast<const float4*>(Xp + pb8(bi, bj) + r * 8 + 4 * h);
-        lv[s][0] = x4.x;
-        lv[s][1] = x4.y;
-        lv[s][2] = x4.z;
-        lv[s][3] = x4.w;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) lv[s][m] = (bi >= bj) ? Xp[pb8(bi, bj) + (l & 7) * 8 + (j4 & 7) + m] : 0.f;
       }
       __syncthreads();
 #pragma unroll
