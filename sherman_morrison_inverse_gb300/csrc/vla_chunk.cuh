@@ -537,7 +537,10 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
           x[2 * m + 1] = f.y;
         }
       };
-      for (int f = tid; doA && f < 64 * 8; f += NT) {   // U rows a (64 x 8 pieces)
+#pragma unroll
+      for (int s8 = 0; s8 < 64 * 8 / NT; ++s8) {   // U rows a (64 x 8 pieces)
+        if (!doA) break;
+        const int f = tid + NT * s8;
         const int arow = (f >> 6) * 8 + (f & 7), pc = ((f & 7) + (f >> 3)) & 7;
         float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         if (arow / R < c) {
@@ -629,7 +632,10 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
           }
         }
       } else {
-        for (int f = tid; f < C * 8; f += NT) {    // step rows t < C; rows c.. are zero (Sigma, phi(q), V)
+#pragma unroll
+        for (int s8 = 0; s8 < (C * 8 + NT - 1) / NT; ++s8) {   // step rows t < C; rows c.. are zero (Sigma, phi(q), V)
+          const int f = tid + NT * s8;
+          if (C * 8 % NT != 0 && f >= C * 8) break;
           const int t = (f >> 6) * 8 + (f & 7), pc = ((f & 7) + (f >> 3)) & 7;
           float kx[8], qx[8];
           uint4 vw = make_uint4(0u, 0u, 0u, 0u);
