@@ -760,8 +760,10 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
       }
       __syncthreads();
       }   // doS
-      // the raw stage is free once the tile's last chunk is converted
-      if (!F32 && tid == 0 && ts + c == TS && tile + 1 < ntiles) {
+      // the raw stage is free once the tile's last chunk is converted: the S side of a cluster
+      // issues the next tile's copies here, the A side (and the one-CTA form) from a helper warp
+      // at the start of the LDL^T
+      if (!F32 && !doA && tid == 0 && ts + c == TS && tile + 1 < ntiles) {
         fence_proxy_async_smem();
         issue(tile + 1);
       }
@@ -990,6 +992,11 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
       }
         } else {
       const int ot = (warp - 1) * 32 + lane;   // 0 .. kHelpers - 1
+      // the next tile's copies, issued here where the helpers wait for warp 0's first column
+      if (!F32 && ot == kHelpers - 32 && ts + c == TS && tile + 1 < ntiles) {
+        fence_proxy_async_smem();
+        issue(tile + 1);
+      }
       auto ld4 = [](const float* pp) { return *reinterpret_cast<const float4*>(pp); };
       auto ldrow8 = [&](const float* pp, float (&v)[8]) {
         const float4 x0 = ld4(pp), x1 = ld4(pp + 4);
