@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
   // from the previous chunk's G6 until this chunk's prologue (q -> PQ, k -> Q tile 1, v -> vb,
   // where it stays as it is, u -> AL), issued right after that G6 so that they land beside it.
   // The A side of a cluster has neither G5 nor G6: it takes u into PQ (free there) and issues
-  // the next chunk's k and u before its G3.
+  // the next chunk's k and u at the start of its LDL^T.
   constexpr int F_UST = SPLIT ? Cf::F_PQ : Cf::F_AL;   // where a float32 chunk's u is staged
   long long staged_pos = -1;   // the chunk whose inputs were issued last (all threads agree)
   bool stage_pending = false;  // issued and not yet waited for
@@ -430,7 +430,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
   };
   // float32 I/O: issue the copies of the next chunk's inputs (all threads call it; the tiles
   // they land in must be free, every earlier access to them fenced by a barrier)
-  auto stage_next = [&]() {
+  auto stage_next = [&](int issuer) {   // `issuer`: the thread that issues them
     const long long np = pos + c;
     if (np >= T) return;
     long long tn = to_nudge;
@@ -440,7 +440,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     }
     int nc = (int)min((long long)(TS - np % TS), T - np);
     if (a.P > 0 && tn <= nc) nc = (int)tn;
-    if (tid == 0) stage(np, nc);
+    if (tid == issuer) stage(np, nc);
     staged_pos = np;
     stage_pending = true;
   };
@@ -787,6 +787,8 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
 
     // ---------------- G2: [G - I; H^T] = [W^T; Q^T] U^T  (M 128, N 64, K 64), X read from G1's
     // accumulator in tensor memory; it runs while G1's W is drained.  Q^T stays there for alpha.
+    // A thread of warp 3 issues it: the W drain is warps 0, 1, 4 and 5's (rows < 64).
+    constexpr int kG2Issuer = 96;
     if constexpr (F32) {
       // 3xTF32 for G2 as well: the low part of G1's accumulator goes to TMEM columns TC_XL.., and
       // G2 takes X hi * U hi + X lo * U hi + X hi * U lo (U lo in the Q tiles)
@@ -799,7 +801,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
       tc::fence_before_sync();
       __syncthreads();
       tc::fence_after_sync();
-      if (tid == 0) {
+      if (tid == kG2Issuer) {
         MmaPass ps[3] = {{0, Cf::F_P, 128, 64, TC_G2, false}, {0, Cf::F_P, 128, 64, TC_G2, true},
                          {0, Cf::F_Q, 128, 64, TC_G2, true}};
         ps[0].tx = TC_G1;
@@ -822,7 +824,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     {
       MmaPass ps[1] = {{0, Cf::F_P, 128, 64, TC_G2, false}};
       ps[0].tx = TC_G1;
-      if (tid == 0) mma_issue(ps, 1, 64);
+      if (tid == kG2Issuer) mma_issue(ps, 1, 64);
     }
     if (row < 64) {   // W[i][a] = W^T[a][i], a = row (warp-uniform): fp32 -> R tile 0
       float v32[32];
@@ -873,6 +875,10 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     // beyond k + 1.  Warp 0 and the helpers hand over through named barriers (LB: column k of
     // L is written; UB: the helpers' trailing update for column k is done), used in
     // alternation so that a barrier is never reused before its previous round completed.
+    // the A side of a cluster: the next chunk's u (PQ) and k (Q tile 1), free since G1, issued
+    // by the thread that issues a bf16 tile's copies (a helper, which waits for warp 0's first
+    // column anyway)
+    if constexpr (SPLIT && F32) stage_next(32 + kHelpers - 32);
     float* XB = sf + Cf::F_Q;   // X = L^{-1}: 36 lower 8 x 8 blocks
     float* BB = sf + Cf::F_L;   // B: 28 strictly lower 8 x 8 blocks
     if (warp == 0) {
@@ -993,6 +999,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
         } else {
       const int ot = (warp - 1) * 32 + lane;   // 0 .. kHelpers - 1
       // the next tile's copies, issued here where the helpers wait for warp 0's first column
+      // (thread 32 + kHelpers - 32 = warp 7, lane 0)
       if (!F32 && ot == kHelpers - 32 && ts + c == TS && tile + 1 < ntiles) {
         fence_proxy_async_smem();
         issue(tile + 1);
@@ -1223,10 +1230,6 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
         st4_lo(Cf::F_P + 4 * e4, xv);
       }
     }
-    // the A side of a cluster: the next chunk's u (PQ) and k (Q tile 1), free since G1; issued
-    // after the LDL^T, which runs faster without the copies landing beside it, and still in
-    // time for the next chunk
-    if constexpr (SPLIT && F32) stage_next();
     // ---------------- G3: [Z; F^T] = [W; H^T] Linv^T  (M 128, N 64, K 64), 3xTF32
     {
       const MmaPass ps[3] = {{Cf::F_R, Cf::F_L, 128, 64, TC_G3, false},
@@ -1679,7 +1682,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
       if (tid == 0) mma_issue(ps, F32 ? 6 : 2, C);
       // the next chunk's inputs into AL, PQ, Q tile 1 and vb: G6 and its drain do not touch
       // them, and every earlier access to them is fenced by the barrier above
-      if constexpr (F32) stage_next();
+      if constexpr (F32) stage_next(0);
       if (!mma_wait()) { failed = true; break; }
     }
     {
