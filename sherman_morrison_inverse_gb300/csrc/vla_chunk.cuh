@@ -106,10 +106,13 @@ __device__ __forceinline__ float tf32_hi(float x) { return __uint_as_float(__flo
 // the chunked path serves bf16 I/O, whose rounding is far coarser)
 __device__ __forceinline__ float phi_fast(float x) { return x > 0.f ? x + 1.f : __expf(x); }
 
-// packed 8 x 8 blocks (row-major, 64 floats) of a 64 x 64 lower-triangular matrix: block (bi, bj)
-// with bi >= bj, and the strictly lower blocks (bi > bj) of a second one
-__host__ __device__ constexpr int pb8(int bi, int bj) { return (bi * (bi + 1) / 2 + bj) * 64; }
-__host__ __device__ constexpr int pbB(int bi, int bj) { return (bi * (bi - 1) / 2 + bj) * 64; }
+// packed 8 x 8 blocks (row-major, 64 floats, 72 apart) of a 64 x 64 lower-triangular matrix:
+// block (bi, bj) with bi >= bj, and the strictly lower blocks (bi > bj) of a second one.  The
+// padding puts consecutive blocks two 16-byte bank groups apart, so the blocks that the lanes
+// of a helper warp read at once fall in different banks.
+constexpr int kBlk = 72;
+__host__ __device__ constexpr int pb8(int bi, int bj) { return (bi * (bi + 1) / 2 + bj) * kBlk; }
+__host__ __device__ constexpr int pbB(int bi, int bj) { return (bi * (bi - 1) / 2 + bj) * kBlk; }
 
 // 1/x by the SFU's approximate reciprocal (rcp.approx.ftz.f32: about 1 ulp; the pivots of D are >=
 // 1 for an SPD A, far from the flushed range; a pivot below the guard threshold is caught anyway)
