@@ -35,14 +35,16 @@
 // applies the column's contribution to the next block column, keeping its rows in
 // registers; the seven other warps form L^{-1} block row by block row (the forward
 // elimination of the identity) and the trailing updates one step behind, handing over
-// through named barriers.
+// through named barriers.  The chain of phases pays for serial work wherever the other
+// threads wait, so single-thread jobs go to warps with slack: a helper issues the next
+// chunk's input copies at the start of the LDL^T, a thread of an idle warp issues G2.
 //
 // Renormalisation: ||S_t||^2 = ||S||^2 + 2 sum v_t'^T S alpha_t' + sum (v.v)(alpha.alpha) from the
 // products above; the bound ||S|| + sum |v_t||alpha_t| (||S||^2 carried from the previous
 // chunk's state update; one warp tests it while G5 runs) decides that no step can exceed
-// tau, otherwise the exact per-step
-// norms give the decisions and the per-step scales are folded into tril(aq), alpha^T and
-// the outputs.  When the scales of one chunk fall below 2^-64 (tau far below the norm
+// tau, otherwise the exact per-step norms give the decisions (V V^T on the tensor core; the
+// decisions in order on one warp, the cross terms from row prefix sums) and the per-step
+// scales are folded into tril(aq), alpha^T and the outputs.  When the scales of one chunk fall below 2^-64 (tau far below the norm
 // each step adds), that chunk's S and outputs are taken step by step from its alpha instead.
 // A pivot |D_jj| < 1e-6 means the sequential recurrence takes the singularity
 // guard inside the chunk; the chunk is then taken step by step on CUDA cores.
@@ -85,6 +87,7 @@ constexpr int TILE = 64 * 64;         // floats of a TK(64, 64) operand tile
 constexpr int PLD = 68;               // leading dimension of the prologue's phi(k) / phi(q) scratch
 constexpr int GLD = 68;               // leading dimension of the fp32 G / L staging (16-byte rows)
 constexpr int kHelpers = 224;         // threads of the LDL^T helper warps (warps 1..7)
+constexpr int kCopyIssuer = NT - 32;  // warp 7, lane 0 (a helper): issues the next chunk's input copies
 constexpr float kGuardEps = 1e-6f;
 constexpr float kReadoutEps = 1e-6f;
 constexpr float kInvSqrtD = 0.125f;
@@ -881,7 +884,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
     // the A side of a cluster: the next chunk's u (PQ) and k (Q tile 1), free since G1, issued
     // by the thread that issues a bf16 tile's copies (a helper, which waits for warp 0's first
     // column anyway)
-    if constexpr (SPLIT && F32) stage_next(32 + kHelpers - 32);
+    if constexpr (SPLIT && F32) stage_next(kCopyIssuer);
     float* XB = sf + Cf::F_Q;   // X = L^{-1}: 36 lower 8 x 8 blocks
     float* BB = sf + Cf::F_L;   // B: 28 strictly lower 8 x 8 blocks
     if (warp == 0) {
@@ -1002,8 +1005,7 @@ __global__ void __launch_bounds__(chk::NT, 1) chunk_scan_kernel(ScanArgs a) {
         } else {
       const int ot = (warp - 1) * 32 + lane;   // 0 .. kHelpers - 1
       // the next tile's copies, issued here where the helpers wait for warp 0's first column
-      // (thread 32 + kHelpers - 32 = warp 7, lane 0)
-      if (!F32 && ot == kHelpers - 32 && ts + c == TS && tile + 1 < ntiles) {
+      if (!F32 && tid == kCopyIssuer && ts + c == TS && tile + 1 < ntiles) {
         fence_proxy_async_smem();
         issue(tile + 1);
       }
