@@ -1,6 +1,8 @@
 // Instantiations of the chunked (Woodbury / LDL^T, tcgen05) scan: d = d_v = 64, bfloat16 or
 // float32 I/O, r = 1 (64 steps per chunk) and r = 4 (16 steps per chunk); one CTA per pair
 // (ctas = 1) or a cluster of two (ctas = 2: the A side and the S side).
+#include <atomic>
+
 #include "vla_chunk.cuh"
 
 namespace vla {
@@ -24,14 +26,17 @@ cudaError_t launch_chunked(int d, int r, bool bf16, int chunk, int ctas, const S
 // (0 when the shape is not built or the query fails), cached per device and shape.
 int chunked_cluster_capacity(int r, bool bf16) {
   constexpr int kDevices = 64;
-  static int cache[kDevices][2][2];   // +1: 0 means not queried yet
+  // n + 1 once queried, 0 before; host threads with different handles may query at once and
+  // store the same value
+  static std::atomic<int> cache[kDevices][2][2];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevices || (r != 1 && r != 4)) {
     cudaGetLastError();
     return 0;
   }
-  int& slot = cache[dev][r == 4][bf16 ? 1 : 0];
-  if (slot > 0) return slot - 1;
+  std::atomic<int>& slot = cache[dev][r == 4][bf16 ? 1 : 0];
+  const int known = slot.load(std::memory_order_relaxed);
+  if (known > 0) return known - 1;
   int n = 0;
   cudaError_t e = r == 1 ? (bf16 ? cluster_capacity_t<1, __nv_bfloat16>(&n) : cluster_capacity_t<1, float>(&n))
                          : (bf16 ? cluster_capacity_t<4, __nv_bfloat16>(&n) : cluster_capacity_t<4, float>(&n));
@@ -39,7 +44,7 @@ int chunked_cluster_capacity(int r, bool bf16) {
     cudaGetLastError();
     return 0;
   }
-  slot = n + 1;
+  slot.store(n + 1, std::memory_order_relaxed);
   return n;
 }
 
