@@ -102,9 +102,9 @@ TRAFFIC = {
     ("b2h8_t65536_d128_f32", "sequential"): (155.86e6 * 16, 4096, "09b46c6b7e90fb86"),
     ("b8h16_t16384_d64_bf16_recall", "sequential"): (324.69e6 * 4, 4096, "09b46c6b7e90fb86"),
     ("b8h16_t16384_d64_bf16_recall", "delta"): (324.66e6 * 4, 4096, "a1a90440234bd2e5"),
-    ("b8h16_t16384_d64_bf16_recall", "chunked"): (156.74e6 * 8, 2048, "69e15e9d21eb32ad"),
-    ("b16h16_t8192_d64_bf16_r4", "chunked"): (274.79e6 * 8, 1024, "69e15e9d21eb32ad"),
-    ("b4h8_t4096_d64_f32", "chunked"): (153.33e6, 4096, "69e15e9d21eb32ad"),
+    ("b8h16_t16384_d64_bf16_recall", "chunked"): (156.03e6 * 8, 2048, "d7624e73d18c2b23"),
+    ("b16h16_t8192_d64_bf16_r4", "chunked"): (274.33e6 * 8, 1024, "d7624e73d18c2b23"),
+    ("b4h8_t4096_d64_f32", "chunked"): (153.79e6, 4096, "d7624e73d18c2b23"),
     # the u projection's TMA form (whole workload captured)
     ("b8h16_t16384_d64_bf16_recall", "project_u"): (483.84e6, 16384, "29d4409f456223ca"),
     ("b16h16_t8192_d64_bf16_r4", "project_u"): (1281.11e6, 8192, "29d4409f456223ca"),
