@@ -106,8 +106,8 @@ TRAFFIC = {
     ("b16h16_t8192_d64_bf16_r4", "chunked"): (274.33e6 * 8, 1024, "d7624e73d18c2b23"),
     ("b4h8_t4096_d64_f32", "chunked"): (153.79e6, 4096, "d7624e73d18c2b23"),
     # the u projection's TMA form (whole workload captured)
-    ("b8h16_t16384_d64_bf16_recall", "project_u"): (483.84e6, 16384, "29d4409f456223ca"),
-    ("b16h16_t8192_d64_bf16_r4", "project_u"): (1281.11e6, 8192, "29d4409f456223ca"),
+    ("b8h16_t16384_d64_bf16_recall", "project_u"): (482.59e6, 16384, "bad2b2f554b35e74"),
+    ("b16h16_t8192_d64_bf16_r4", "project_u"): (1280.58e6, 8192, "bad2b2f554b35e74"),
 }
 
 
